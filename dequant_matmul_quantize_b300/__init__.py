@@ -1,0 +1,247 @@
+"""nf4q: NF4 / FP4 blockwise quantization with double quantization and the
+"4-bit stored, 16-bit computed" matmul, as hand-written CUDA for B300.
+
+This module is a thin ctypes binding over ``libnf4q.so`` (the C ABI declared
+in ``include/nf4q.h``): it marshals torch tensors' device pointers and the
+current CUDA stream, nothing else.  Every step runs in the library's kernels.
+There is no CPU or PyTorch fallback: if the library is missing the import of
+the first op raises.
+
+The user-facing knobs mirror ``BitsAndBytesConfig`` as the bitsandbytes
+pages describe it (tutorial at mlqm.cn/news/394670, section 四): the 4-bit
+type ``nf4`` or ``fp4``, ``double_quant`` on or off, and the compute dtype,
+which is bf16 here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnf4q.so")
+
+CODES = {"nf4": 0, "fp4": 1}
+IN_F32, IN_BF16 = 0, 1
+BLOCKSIZE, DQ_BLOCKSIZE = 64, 256
+GEMV_MAX_M = 16
+
+STATUS = {
+    0: "NF4Q_OK", 1: "NF4Q_ERR_INVALID_ARG", 2: "NF4Q_ERR_ALIGNMENT",
+    3: "NF4Q_ERR_UNSUPPORTED", 4: "NF4Q_ERR_WORKSPACE", 5: "NF4Q_ERR_CUDA",
+    6: "NF4Q_ERR_TIMEOUT",
+}
+
+
+class Nf4qError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: {STATUS.get(status, status)}")
+
+
+class NF4QWeight(ctypes.Structure):
+    """Mirror of ``nf4q_weight`` in include/nf4q.h."""
+    _fields_ = [
+        ("packed", ctypes.c_void_p),
+        ("absmax_q", ctypes.c_void_p),
+        ("absmax", ctypes.c_void_p),
+        ("scale2", ctypes.c_void_p),
+        ("offset", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("blocksize", ctypes.c_int32),
+        ("dq_blocksize", ctypes.c_int32),
+        ("code", ctypes.c_int32),
+        ("double_quant", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libnf4q.so (built in-tree); raise if it is not there."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m dequant_matmul_quantize_b300.build` (no fallback exists)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    W = ctypes.POINTER(NF4QWeight)
+    sig = {
+        "nf4q_version": (i32, []),
+        "nf4q_status_string": (ctypes.c_char_p, [i32]),
+        "nf4q_sizes": (i32, [i64, i64, i32, i32, ctypes.POINTER(sz),
+                             ctypes.POINTER(i64), ctypes.POINTER(i64)]),
+        "nf4q_code_values": (i32, [i32, ctypes.POINTER(ctypes.c_float)]),
+        "nf4q_thresholds": (i32, [i32, ctypes.POINTER(ctypes.c_float),
+                                  ctypes.POINTER(i32)]),
+        "nf4q_quantize": (i32, [vp, i32, W, vp]),
+        "nf4q_double_quant_workspace_bytes": (sz, [i64]),
+        "nf4q_double_quant": (i32, [W, vp, sz, vp]),
+        "nf4q_dequantize": (i32, [W, vp, vp]),
+        "nf4q_gemv": (i32, [W, vp, i32, vp, vp]),
+        "nf4q_gemm": (i32, [W, vp, i64, vp, vp]),
+        "nf4q_matmul": (i32, [W, vp, i64, vp, vp]),
+        "nf4q_device_error": (i32, [ctypes.POINTER(ctypes.c_uint32), i32]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(func: str, status: int):
+    if status != 0:
+        raise Nf4qError(func, status)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+# ------------------------------------------------------------------ host-only
+def sizes(rows: int, cols: int):
+    """(packed_bytes, n_b, n_d) of a [rows x cols] weight."""
+    pb, nb, nd = ctypes.c_size_t(), ctypes.c_int64(), ctypes.c_int64()
+    _check("nf4q_sizes", lib().nf4q_sizes(rows, cols, BLOCKSIZE, DQ_BLOCKSIZE,
+                                          ctypes.byref(pb), ctypes.byref(nb),
+                                          ctypes.byref(nd)))
+    return pb.value, nb.value, nd.value
+
+
+def code_values(code: str = "nf4"):
+    out = (ctypes.c_float * 16)()
+    _check("nf4q_code_values", lib().nf4q_code_values(CODES[code], out))
+    return list(out)
+
+
+def thresholds(code: str = "nf4"):
+    out = (ctypes.c_float * 15)()
+    n = ctypes.c_int32()
+    _check("nf4q_thresholds", lib().nf4q_thresholds(CODES[code], out, ctypes.byref(n)))
+    return list(out)[: n.value]
+
+
+# ------------------------------------------------------------------ state
+@dataclass
+class QuantizedWeight:
+    """Device buffers of one quantized weight (see the layout in nf4q.h)."""
+    packed: torch.Tensor
+    absmax: torch.Tensor
+    absmax_q: Optional[torch.Tensor]
+    scale2: Optional[torch.Tensor]
+    offset: Optional[torch.Tensor]
+    rows: int
+    cols: int
+    code: str = "nf4"
+    double_quant: bool = True
+
+    def struct(self) -> NF4QWeight:
+        return NF4QWeight(_ptr(self.packed), _ptr(self.absmax_q), _ptr(self.absmax),
+                          _ptr(self.scale2), _ptr(self.offset), self.rows, self.cols,
+                          BLOCKSIZE, DQ_BLOCKSIZE, CODES[self.code],
+                          1 if self.double_quant else 0)
+
+    @staticmethod
+    def empty(rows: int, cols: int, code: str = "nf4", double_quant: bool = True,
+              device=None) -> "QuantizedWeight":
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        pb, nb, nd = sizes(rows, cols)
+        u8 = dict(dtype=torch.uint8, device=device)
+        return QuantizedWeight(
+            packed=torch.empty(max(pb, 1), **u8)[:pb],
+            absmax=torch.empty(max(nb, 1), dtype=torch.float32, device=device)[:nb],
+            absmax_q=torch.empty(max(nb, 1), dtype=torch.int8, device=device)[:nb],
+            scale2=torch.empty(max(nd, 1), dtype=torch.float32, device=device)[:nd],
+            offset=torch.empty(1, dtype=torch.float32, device=device),
+            rows=rows, cols=cols, code=code, double_quant=double_quant)
+
+
+# ------------------------------------------------------------------ ops
+def quantize_into(qw: QuantizedWeight, w: torch.Tensor, stream=None):
+    """nf4q_quantize: writes qw.packed and qw.absmax from w (fp32 or bf16)."""
+    assert w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols)
+    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16}[w.dtype]
+    s = qw.struct()
+    _check("nf4q_quantize", lib().nf4q_quantize(_ptr(w), dt, ctypes.byref(s), _stream(stream)))
+
+
+def dq_workspace(n_b: int, device=None) -> torch.Tensor:
+    nbytes = lib().nf4q_double_quant_workspace_bytes(n_b)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def double_quant_into(qw: QuantizedWeight, workspace: Optional[torch.Tensor] = None,
+                      stream=None):
+    """nf4q_double_quant: writes qw.absmax_q, qw.scale2, qw.offset from qw.absmax."""
+    if workspace is None:
+        workspace = dq_workspace(qw.absmax.numel(), qw.absmax.device)
+    s = qw.struct()
+    _check("nf4q_double_quant", lib().nf4q_double_quant(
+        ctypes.byref(s), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def quantize(w: torch.Tensor, code: str = "nf4", double_quant: bool = True,
+             workspace: Optional[torch.Tensor] = None, stream=None) -> QuantizedWeight:
+    """Quantize a [rows x cols] fp32/bf16 CUDA weight (cols % 64 == 0)."""
+    rows, cols = w.shape
+    qw = QuantizedWeight.empty(rows, cols, code, double_quant, w.device)
+    quantize_into(qw, w, stream)
+    if double_quant:
+        double_quant_into(qw, workspace, stream)
+    return qw
+
+
+def dequantize(qw: QuantizedWeight, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(qw.rows, qw.cols, dtype=torch.bfloat16, device=qw.packed.device)
+    s = qw.struct()
+    _check("nf4q_dequantize", lib().nf4q_dequantize(ctypes.byref(s), _ptr(out), _stream(stream)))
+    return out
+
+
+def _mm(name: str, qw: QuantizedWeight, x: torch.Tensor, out, stream):
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    assert x.shape[-1] == qw.cols
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty(M, qw.rows, dtype=torch.bfloat16, device=x.device)
+    s = qw.struct()
+    _check(name, getattr(lib(), name)(ctypes.byref(s), _ptr(x), M, _ptr(out), _stream(stream)))
+    return out
+
+
+def gemv(qw, x, out=None, stream=None):
+    """y = x . w_hat^T for 1 <= M <= 16 (decode)."""
+    return _mm("nf4q_gemv", qw, x, out, stream)
+
+
+def gemm(qw, x, out=None, stream=None):
+    """Y = X . w_hat^T on the tcgen05 tensor cores (prefill)."""
+    return _mm("nf4q_gemm", qw, x, out, stream)
+
+
+def matmul(qw, x, out=None, stream=None):
+    """Dispatch on M: gemv for M <= 16, gemm above."""
+    return _mm("nf4q_matmul", qw, x, out, stream)
+
+
+def device_error(clear: bool = True) -> int:
+    flags = ctypes.c_uint32()
+    _check("nf4q_device_error", lib().nf4q_device_error(ctypes.byref(flags), 1 if clear else 0))
+    return flags.value

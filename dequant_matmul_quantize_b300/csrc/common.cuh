@@ -1,0 +1,80 @@
+// Shared device helpers of the nf4q kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "tables.h"
+
+namespace nf4q {
+
+constexpr int kBlock = 64;      // elements per absmax block
+constexpr int kDqBlock = 256;   // absmax values per double-quant block
+
+// Sticky device error word (bit 0: a pipeline wait gave up).
+__device__ uint32_t g_device_error;
+
+// Everything a dequantizer needs to rebuild one block's scale.
+struct ScaleView {
+  const int8_t* absmax_q;
+  const float* absmax;
+  const float* scale2;
+  const float* offset;
+  int double_quant;
+};
+
+// s_b = fmaf(q_b, scale2[b / 256], offset), or the fp32 absmax without
+// double quantization ("bitsandbytes tutorial", sec. 3.3).
+__device__ __forceinline__ float block_scale(const ScaleView& sv, int64_t b) {
+  if (sv.double_quant) {
+    float q = static_cast<float>(__ldg(sv.absmax_q + b));
+    return __fmaf_rn(q, __ldg(sv.scale2 + (b >> 8)), __ldg(sv.offset));
+  }
+  return __ldg(sv.absmax + b);
+}
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_u4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Two float32 -> packed bf16x2 (lo in the low half), each rounded to nearest
+// even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) {
+  return __uint_as_float(v << 16);
+}
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) {
+  return __uint_as_float(v & 0xFFFF0000u);
+}
+
+}  // namespace nf4q

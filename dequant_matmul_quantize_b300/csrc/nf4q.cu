@@ -1,0 +1,323 @@
+// C-ABI entry points of libnf4q: argument checks on the host, then launches
+// of the kernels in the included headers on the caller's stream.  The whole
+// library is one translation unit.
+#include "nf4q.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "dequantize.cuh"
+#include "double_quant.cuh"
+#include "gemm.cuh"
+#include "gemv.cuh"
+#include "quantize.cuh"
+
+namespace nf4q {
+namespace {
+
+const HostTables& tables() {
+  static HostTables T;
+  static std::once_flag once;
+  std::call_once(once, [] { T = build_host_tables(); });
+  return T;
+}
+
+constexpr int kMaxDevices = 64;
+
+int sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+inline bool aligned4(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
+}
+
+inline nf4q_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
+}
+
+// Shape and layout checks shared by every call on a quantized weight.
+nf4q_status check_shape(const nf4q_weight* wq) {
+  if (!wq) return NF4Q_ERR_INVALID_ARG;
+  if (wq->rows < 0 || wq->cols < 0 || wq->cols % kBlock != 0)
+    return NF4Q_ERR_INVALID_ARG;
+  if (wq->blocksize != kBlock || wq->dq_blocksize != kDqBlock)
+    return NF4Q_ERR_INVALID_ARG;
+  if (wq->code != NF4Q_CODE_NF4 && wq->code != NF4Q_CODE_FP4)
+    return NF4Q_ERR_INVALID_ARG;
+  if (wq->double_quant != 0 && wq->double_quant != 1) return NF4Q_ERR_INVALID_ARG;
+  // n_b must fit the 32-bit divisor of the exact mean
+  if (wq->rows > 0 && wq->cols > 0 &&
+      wq->rows > (static_cast<int64_t>(0x7FFFFFFF) * kBlock) / wq->cols)
+    return NF4Q_ERR_UNSUPPORTED;
+  return NF4Q_OK;
+}
+
+// Checks of the stored state a dequantizer reads.
+nf4q_status check_scales(const nf4q_weight* wq) {
+  if (!wq->packed) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(wq->packed)) return NF4Q_ERR_ALIGNMENT;
+  if (wq->double_quant) {
+    if (!wq->absmax_q || !wq->scale2 || !wq->offset) return NF4Q_ERR_INVALID_ARG;
+    if (!aligned4(wq->scale2) || !aligned4(wq->offset)) return NF4Q_ERR_ALIGNMENT;
+  } else {
+    if (!wq->absmax) return NF4Q_ERR_INVALID_ARG;
+    if (!aligned4(wq->absmax)) return NF4Q_ERR_ALIGNMENT;
+  }
+  return NF4Q_OK;
+}
+
+ScaleView scale_view(const nf4q_weight* wq) {
+  ScaleView sv;
+  sv.absmax_q = wq->absmax_q;
+  sv.absmax = wq->absmax;
+  sv.scale2 = wq->scale2;
+  sv.offset = wq->offset;
+  sv.double_quant = wq->double_quant;
+  return sv;
+}
+
+CodeValues code_values(int code) {
+  CodeValues C;
+  for (int i = 0; i < 16; ++i) C.v[i] = tables().values[code][i];
+  return C;
+}
+
+int64_t grid_for(int64_t work_items, int64_t per_cta, int64_t cap) {
+  int64_t g = (work_items + per_cta - 1) / per_cta;
+  return std::max<int64_t>(1, std::min<int64_t>(g, cap));
+}
+
+}  // namespace
+}  // namespace nf4q
+
+using namespace nf4q;
+
+extern "C" {
+
+int32_t nf4q_version(void) { return (1 << 16) | 0; }
+
+const char* nf4q_status_string(nf4q_status s) {
+  switch (s) {
+    case NF4Q_OK: return "ok";
+    case NF4Q_ERR_INVALID_ARG: return "invalid argument";
+    case NF4Q_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case NF4Q_ERR_UNSUPPORTED: return "unsupported configuration";
+    case NF4Q_ERR_WORKSPACE: return "workspace missing or too small";
+    case NF4Q_ERR_CUDA: return "CUDA error";
+    case NF4Q_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+nf4q_status nf4q_sizes(int64_t rows, int64_t cols, int32_t blocksize,
+                       int32_t dq_blocksize, size_t* packed_bytes, int64_t* n_b,
+                       int64_t* n_d) {
+  if (rows < 0 || cols < 0 || blocksize != kBlock || dq_blocksize != kDqBlock ||
+      cols % kBlock != 0)
+    return NF4Q_ERR_INVALID_ARG;
+  const int64_t n = rows * cols;
+  const int64_t nb = n / kBlock;
+  if (packed_bytes) *packed_bytes = static_cast<size_t>(n / 2);
+  if (n_b) *n_b = nb;
+  if (n_d) *n_d = (nb + kDqBlock - 1) / kDqBlock;
+  return NF4Q_OK;
+}
+
+nf4q_status nf4q_code_values(int32_t code, float* out) {
+  if (!out || (code != NF4Q_CODE_NF4 && code != NF4Q_CODE_FP4)) return NF4Q_ERR_INVALID_ARG;
+  if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
+  for (int i = 0; i < 16; ++i) out[i] = tables().values[code][i];
+  return NF4Q_OK;
+}
+
+nf4q_status nf4q_thresholds(int32_t code, float* out, int32_t* count) {
+  if (!out || !count || (code != NF4Q_CODE_NF4 && code != NF4Q_CODE_FP4))
+    return NF4Q_ERR_INVALID_ARG;
+  if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
+  const int n = tables().nthr[code];
+  for (int i = 0; i < n; ++i) out[i] = tables().thr[code][i];
+  *count = n;
+  return NF4Q_OK;
+}
+
+nf4q_status nf4q_quantize(const void* w, int32_t in_dtype, const nf4q_weight* wq,
+                          void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16) return NF4Q_ERR_INVALID_ARG;
+  const int64_t n = wq->rows * wq->cols;
+  if (n == 0) return NF4Q_OK;
+  if (!w || !wq->packed || !wq->absmax) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(wq->packed) || !aligned16(wq->absmax))
+    return NF4Q_ERR_ALIGNMENT;
+  const HostTables& T = tables();
+  if (!T.ok) return NF4Q_ERR_UNSUPPORTED;
+  QuantParams P;
+  const int c = wq->code;
+  for (int i = 0; i < kLutEntries; ++i) P.lut[i] = T.lut[c][i];
+  for (int i = 0; i < 15; ++i) P.thr[i] = i < T.nthr[c] ? T.thr[c][i] : 2.0f;
+  P.nthr = T.nthr[c];
+  P.lut_scale = T.lut_scale[c];
+  P.lut_bias = T.lut_bias[c] + kMagic;
+  const int64_t n_units = n / 8;
+  constexpr int U = 2;
+  const int64_t grid = grid_for(n_units, 32 * U * (kQuantThreads / 32),
+                                static_cast<int64_t>(sm_count()) * 2);
+  const size_t smem = kLutEntries * 32 * sizeof(uint32_t);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* packed = reinterpret_cast<uint32_t*>(wq->packed);
+  if (c == NF4Q_CODE_NF4) {
+    if (in_dtype == NF4Q_IN_BF16)
+      quantize_kernel<0, true, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
+    else
+      quantize_kernel<0, false, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
+  } else {
+    if (in_dtype == NF4Q_IN_BF16)
+      quantize_kernel<1, true, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
+    else
+      quantize_kernel<1, false, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
+  }
+  return launch_status();
+}
+
+size_t nf4q_double_quant_workspace_bytes(int64_t n_b) {
+  (void)n_b;
+  return sizeof(DqWorkspace);
+}
+
+nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  const int64_t nb = wq->rows * wq->cols / kBlock;
+  if (!wq->absmax_q || !wq->scale2 || !wq->offset) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned4(wq->offset) || !aligned4(wq->scale2)) return NF4Q_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (nb == 0) {
+    if (cudaMemsetAsync(wq->offset, 0, sizeof(float), s) != cudaSuccess) return NF4Q_ERR_CUDA;
+    return NF4Q_OK;
+  }
+  if (!wq->absmax) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(wq->absmax) || !aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < sizeof(DqWorkspace)) return NF4Q_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NF4Q_ERR_ALIGNMENT;
+  if (cudaMemsetAsync(workspace, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
+  const int64_t g1 = grid_for(nb, kDqSumThreads, static_cast<int64_t>(sm_count()) * 2);
+  dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb,
+                                             static_cast<DqWorkspace*>(workspace), wq->offset);
+  if ((st = launch_status()) != NF4Q_OK) return st;
+  const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
+  const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
+  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset,
+                                                  wq->absmax_q, wq->scale2);
+  return launch_status();
+}
+
+nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  const int64_t n = wq->rows * wq->cols;
+  if (n == 0) return NF4Q_OK;
+  if ((st = check_scales(wq)) != NF4Q_OK) return st;
+  if (!out) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(out)) return NF4Q_ERR_ALIGNMENT;
+  if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
+  const int64_t n_units = n / 8;
+  constexpr int U = 4;
+  const int64_t grid = grid_for(n_units, static_cast<int64_t>(kDequantThreads) * U,
+                                static_cast<int64_t>(sm_count()) * 8);
+  dequantize_kernel<U><<<grid, kDequantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint32_t*>(wq->packed), scale_view(wq),
+      static_cast<uint4*>(out), n_units, code_values(wq->code));
+  return launch_status();
+}
+
+nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
+                      void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  if (M < 1 || M > NF4Q_GEMV_MAX_M) return NF4Q_ERR_UNSUPPORTED;
+  if (wq->rows == 0) return NF4Q_OK;
+  if (!x || !y) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return NF4Q_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (wq->cols == 0) {  // empty contraction: y = 0
+    return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * wq->rows * 2, s) == cudaSuccess
+               ? NF4Q_OK : NF4Q_ERR_CUDA;
+  }
+  if ((st = check_scales(wq)) != NF4Q_OK) return st;
+  if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
+  const int64_t grid = grid_for(wq->rows, kGemvSimpleThreads / 32,
+                                static_cast<int64_t>(sm_count()) * 8);
+  const uint32_t* pk = reinterpret_cast<const uint32_t*>(wq->packed);
+  const uint16_t* xp = static_cast<const uint16_t*>(x);
+  uint16_t* yp = static_cast<uint16_t*>(y);
+  const ScaleView sv = scale_view(wq);
+  const CodeValues C = code_values(wq->code);
+#define NF4Q_GEMV_SIMPLE(MT)                                                  \
+  gemv_simple_kernel<MT><<<grid, kGemvSimpleThreads, 0, s>>>(pk, sv, xp, yp, \
+                                                             wq->rows, wq->cols, M, C)
+  if (M <= 1) NF4Q_GEMV_SIMPLE(1);
+  else if (M <= 2) NF4Q_GEMV_SIMPLE(2);
+  else if (M <= 4) NF4Q_GEMV_SIMPLE(4);
+  else if (M <= 8) NF4Q_GEMV_SIMPLE(8);
+  else NF4Q_GEMV_SIMPLE(16);
+#undef NF4Q_GEMV_SIMPLE
+  return launch_status();
+}
+
+nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M, void* Y,
+                      void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  if (M < 0) return NF4Q_ERR_INVALID_ARG;
+  if (M == 0 || wq->rows == 0) return NF4Q_OK;
+  if (!X || !Y) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Y)) return NF4Q_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (wq->cols == 0) {
+    return cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * wq->rows * 2, s) == cudaSuccess
+               ? NF4Q_OK : NF4Q_ERR_CUDA;
+  }
+  if ((st = check_scales(wq)) != NF4Q_OK) return st;
+  if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
+  return gemm_launch(wq, scale_view(wq), code_values(wq->code), X, M, Y, s, sm_count());
+}
+
+nf4q_status nf4q_matmul(const nf4q_weight* wq, const void* X, int64_t M, void* Y,
+                        void* stream) {
+  if (M >= 1 && M <= NF4Q_GEMV_MAX_M)
+    return nf4q_gemv(wq, X, static_cast<int32_t>(M), Y, stream);
+  return nf4q_gemm(wq, X, M, Y, stream);
+}
+
+nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear) {
+  if (!flags) return NF4Q_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return NF4Q_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(flags, g_device_error, sizeof(uint32_t)) != cudaSuccess)
+    return NF4Q_ERR_CUDA;
+  if (clear) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t)) != cudaSuccess)
+      return NF4Q_ERR_CUDA;
+  }
+  return NF4Q_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+/*
+ * nf4q - NF4 / FP4 blockwise weight quantization with double quantization,
+ * and the "4-bit stored, 16-bit computed" matmul, for NVIDIA B300 (sm_103a).
+ *
+ * Plain C ABI.  Every pointer in a compute call is a DEVICE pointer unless
+ * the comment says "host"; every `stream` is a cudaStream_t passed as void*
+ * (NULL = the legacy default stream).  Sizes are element counts unless they
+ * end in `_bytes`.
+ *
+ * Where the operations come from (web pages about the bitsandbytes library):
+ *   - "bitsandbytes tutorial" (mlqm.cn/news/394670)
+ *       sec. 2.3  data-free absmax quantization, one scale per block
+ *       sec. 3.2  NF4: 16 levels spaced by the normal density
+ *       sec. 3.3  double quantization: the block scales quantized again
+ *       sec. 3.4  compute dtype: 4-bit storage, dequantize to bf16, matmul
+ *       sec. 四   config keys: quant type nf4|fp4, double quant, compute dtype
+ *   - "bitsandbytes introduction" (modelers.csdn.net), sec. 一 item 7 and
+ *       sec. 三 examples 1-2: NF4 and FP4 4-bit types
+ *   - "bitsandbytes: quantifier un modèle PyTorch sans quitter PyTorch"
+ *       (hysenlabs.com): blockwise quantization, Linear4bit layers
+ *
+ * Ownership: the caller allocates every buffer (including workspaces) and
+ * keeps it alive until the work enqueued on `stream` has finished.  The
+ * library never allocates device memory, never synchronizes the stream and
+ * never calls exit/abort or executes a device trap.  Inputs marked const are
+ * never written.  Outputs must not alias inputs.
+ *
+ * Errors: arguments are checked on the host before anything is launched
+ * (a failing check launches nothing).  A CUDA launch error is reported as
+ * NF4Q_ERR_CUDA.  Device-side bounded waits that give up set a sticky flag
+ * read with nf4q_device_error().
+ *
+ * Layout of a quantized weight W [rows x cols] (row-major, cols contiguous,
+ * the nn.Linear [out, in] convention):
+ *   packed    uint8 [rows*cols/2]: element 2i -> bits 7..4 of byte i,
+ *             element 2i+1 -> bits 3..0 (4-bit code, see below)
+ *   absmax    fp32  [n_b]  n_b = rows*cols/64, max |w| of each run of 64
+ *             consecutive elements (cols % 64 == 0, so a block never
+ *             straddles two rows)
+ *   absmax_q  int8  [n_b]  double-quantized absmax
+ *   scale2    fp32  [n_d]  n_d = ceil(n_b/256), one per 256 absmax values
+ *   offset    fp32  [1]    mean of absmax (see nf4q_double_quant)
+ * Codes: NF4 - index 0..15 of the 16 ascending NF4 levels (0 is code 7,
+ * +1 is code 15); FP4 - (sign << 3) | j, j indexing the E2M1 magnitudes
+ * {0, 0.5, 1, 1.5, 2, 3, 4, 6}/6.
+ */
+#ifndef NF4Q_H_
+#define NF4Q_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The library is built with hidden visibility; the entry points below are
+ * the only exported symbols. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+typedef enum {
+  NF4Q_OK = 0,
+  NF4Q_ERR_INVALID_ARG = 1,  /* null pointer, bad size, unsupported blocksize */
+  NF4Q_ERR_ALIGNMENT = 2,    /* a pointer is not 16-byte aligned */
+  NF4Q_ERR_UNSUPPORTED = 3,  /* valid but not implemented (e.g. M range) */
+  NF4Q_ERR_WORKSPACE = 4,    /* workspace null or too small */
+  NF4Q_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+  NF4Q_ERR_TIMEOUT = 6       /* a bounded device wait gave up */
+} nf4q_status;
+
+typedef enum { NF4Q_CODE_NF4 = 0, NF4Q_CODE_FP4 = 1 } nf4q_code;
+typedef enum { NF4Q_IN_F32 = 0, NF4Q_IN_BF16 = 1 } nf4q_in_dtype;
+
+/* Views into caller-owned device buffers describing one quantized weight. */
+typedef struct {
+  uint8_t* packed;      /* [rows*cols/2]                                    */
+  int8_t* absmax_q;     /* [n_b]  used when double_quant == 1               */
+  float* absmax;        /* [n_b]  written by nf4q_quantize; the stored scale
+                           when double_quant == 0                           */
+  float* scale2;        /* [n_d]  used when double_quant == 1               */
+  float* offset;        /* [1]    used when double_quant == 1               */
+  int64_t rows;         /* N (output features)                              */
+  int64_t cols;         /* K (input features), K % 64 == 0                  */
+  int32_t blocksize;    /* must be 64                                       */
+  int32_t dq_blocksize; /* must be 256                                      */
+  int32_t code;         /* nf4q_code                                        */
+  int32_t double_quant; /* 1: dequantizers use absmax_q/scale2/offset;
+                           0: they use the fp32 absmax                      */
+} nf4q_weight;
+
+/* Library version, (major << 16) | minor. */
+int32_t nf4q_version(void);
+
+/* Human-readable name of a status (static string, never NULL). */
+const char* nf4q_status_string(nf4q_status s);
+
+/* HOST ONLY.  Buffer sizes of a [rows x cols] weight: packed bytes, number of
+ * 64-blocks n_b and of 256-blocks n_d.  Any output pointer may be NULL. */
+nf4q_status nf4q_sizes(int64_t rows, int64_t cols, int32_t blocksize,
+                       int32_t dq_blocksize, size_t* packed_bytes,
+                       int64_t* n_b, int64_t* n_d);
+
+/* HOST ONLY.  The 16 code values (float32, indexed by code) the kernels use,
+ * built by the library itself: NF4 from its definition (Phi^-1 of 8 points
+ * evenly spaced from 0.9677083 down to 0.5 for the positive side, of 7 for
+ * the negative side, plus 0, normalized by the largest; tutorial sec. 3.2),
+ * FP4 from the E2M1 magnitudes. `out` is a host array of 16 floats. */
+nf4q_status nf4q_code_values(int32_t code, float* out);
+
+/* HOST ONLY.  The decision thresholds of the encoder: the largest float32 not
+ * above the exact midpoint of each pair of neighbouring levels (15 for NF4,
+ * 7 magnitude thresholds for FP4).  `out` is a host array of at least 15
+ * floats; `*count` receives 15 or 7. */
+nf4q_status nf4q_thresholds(int32_t code, float* out, int32_t* count);
+
+/* Blockwise quantization (tutorial sec. 2.3 absmax, sec. 3.2 NF4; FP4 per the
+ * introduction page, sec. 一 item 7).
+ *   w      device, [rows x cols] row-major, fp32 or bf16 per `in_dtype`,
+ *          16-byte aligned.  Values must be finite.
+ *   wq     host struct; wq->packed and wq->absmax are written (both 16-byte
+ *          aligned); rows, cols, blocksize, code are read.
+ * Per 64-block: absmax = max|w| (fp32); wn = fp32(w / absmax) (IEEE
+ * division; 0 when absmax == 0); code = the nearest level, an exact tie
+ * going to the lower NF4 index / the smaller FP4 magnitude; two codes per
+ * byte, first element in the high nibble. */
+nf4q_status nf4q_quantize(const void* w, int32_t in_dtype,
+                          const nf4q_weight* wq, void* stream);
+
+/* Workspace bytes nf4q_double_quant needs for n_b absmax values (>= 64). */
+size_t nf4q_double_quant_workspace_bytes(int64_t n_b);
+
+/* Double quantization of the scales (tutorial sec. 3.3).
+ *   reads wq->absmax [n_b]; writes wq->absmax_q [n_b], wq->scale2 [n_d],
+ *   wq->offset [1].  absmax must be 16-byte aligned.
+ *   workspace: device, >= nf4q_double_quant_workspace_bytes(n_b) bytes,
+ *   16-byte aligned; the call clears it itself (cudaMemsetAsync on `stream`),
+ *   so its previous contents do not matter.
+ * offset = the float32 nearest to the exact mean of all absmax values (ties
+ * to even; the sum is exact for any inputs); c = fp32(absmax - offset); per
+ * 256-block scale2 = fp32(max|c| / 127); absmax_q = clamp(rint_even(
+ * fp32(c / scale2)), -127, 127), 0 where scale2 == 0. */
+nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Dequantization to bf16 (tutorial sec. 3.4).
+ *   out: device bf16 [rows x cols], 16-byte aligned.
+ * s_b = fmaf(absmax_q[b], scale2[b/256], offset) with double quant, else
+ * absmax[b]; out = bf16_rn(fp32(code_value[code] * s_b)). */
+nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream);
+
+/* Decode-shaped matmul, 1 <= M <= 16 (tutorial sec. 3.4, sec. 七 myth 5:
+ * memory-bandwidth bound).  y[m, n] = sum_k x[m, k] * w_hat[n, k] with
+ * w_hat exactly as nf4q_dequantize produces it, fp32 accumulation, bf16
+ * output.
+ *   x: device bf16 [M x cols], y: device bf16 [M x rows]; both 16-byte
+ *   aligned. */
+nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M,
+                      void* y, void* stream);
+
+/* Prefill-shaped matmul on the tcgen05 tensor cores, M >= 1 (intended for
+ * M >= 64).  Same contraction and output as nf4q_gemv: Y [M x rows] =
+ * X [M x cols] . w_hat^T, bf16 in, fp32 accumulate, bf16 out.
+ *   X, Y: device bf16, 16-byte aligned. */
+nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M,
+                      void* Y, void* stream);
+
+/* Dispatch on M: nf4q_gemv for M <= NF4Q_GEMV_MAX_M, nf4q_gemm above. */
+#define NF4Q_GEMV_MAX_M 16
+nf4q_status nf4q_matmul(const nf4q_weight* wq, const void* X, int64_t M,
+                        void* Y, void* stream);
+
+/* Sticky device error flags of the current device (bit 0: a GEMM pipeline
+ * wait gave up).  Synchronizes the device; `clear` != 0 resets the flags. */
+nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NF4Q_H_ */

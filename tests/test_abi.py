@@ -1,0 +1,102 @@
+"""The C-ABI library loads on a machine without a GPU, exports every function
+declared in include/nf4q.h, and its host-only calls (sizes, code tables,
+argument checks) behave as documented.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import dequant_matmul_quantize_b300 as nq
+from oracle import nf4_oracle as o
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nf4q.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nf4q_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from dequant_matmul_quantize_b300 import build
+    build.build()
+    return nq.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert len(names) >= 13
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(L):
+    assert L.nf4q_version() >> 16 == 1
+    for s in range(7):
+        assert L.nf4q_status_string(s)
+    assert L.nf4q_status_string(99) == b"unknown status"
+
+
+def test_sizes(L):
+    assert nq.sizes(4096, 4096) == (4096 * 4096 // 2, 4096 * 4096 // 64, 1024)
+    assert nq.sizes(28672, 8192)[2] == 14336
+    assert nq.sizes(3, 64) == (96, 3, 1)          # partial last DQ block
+    assert nq.sizes(0, 64) == (0, 0, 0)
+    with pytest.raises(nq.Nf4qError):
+        nq.sizes(4, 100)                           # cols % 64 != 0
+
+
+def test_code_values_match_oracle_bit_exact(L):
+    """The library builds its tables itself (Newton on erfc); the oracle uses
+    scipy's ndtri.  Both must give the same float32 bits."""
+    for code, ref in (("nf4", o.nf4_code_table()), ("fp4", o.fp4_code_table())):
+        got = np.array(nq.code_values(code), dtype=np.float32)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), code
+
+
+def test_thresholds_are_round_down_midpoints(L):
+    for code in ("nf4", "fp4"):
+        t = nq.thresholds(code)
+        lv = (o.nf4_code_table() if code == "nf4" else o.FP4_MAGNITUDES.astype(np.float32))
+        lv = lv.astype(np.float64)
+        mids = (lv[:-1] + lv[1:]) / 2
+        assert len(t) == len(mids)
+        for ti, m in zip(t, mids):
+            f = np.float32(ti)
+            assert float(f) <= m < float(np.nextafter(f, np.float32(2)))
+
+
+def test_argument_checks_launch_nothing(L):
+    s = nq.NF4QWeight(None, None, None, None, None, 64, 64, 64, 256, 0, 1)
+    bad = nq.NF4QWeight(None, None, None, None, None, 64, 100, 64, 256, 0, 1)
+    wrongbs = nq.NF4QWeight(None, None, None, None, None, 64, 64, 128, 256, 0, 1)
+    R = ctypes.byref
+    assert L.nf4q_quantize(None, 0, R(s), None) == 1
+    assert L.nf4q_quantize(None, 0, R(bad), None) == 1
+    assert L.nf4q_quantize(None, 0, R(wrongbs), None) == 1
+    assert L.nf4q_quantize(16, 7, R(s), None) == 1               # dtype
+    assert L.nf4q_double_quant(R(s), None, 0, None) == 1          # no outputs
+    assert L.nf4q_dequantize(R(s), None, None) == 1
+    assert L.nf4q_gemv(R(s), 16, 0, 16, None) == 3               # M out of range
+    assert L.nf4q_gemv(R(s), 16, 17, 16, None) == 3
+    assert L.nf4q_gemm(R(s), 16, -1, 16, None) == 1
+    assert L.nf4q_gemv(None, 16, 1, 16, None) == 1
+    # misaligned device pointers are refused before any launch
+    sp = nq.NF4QWeight(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64, 64, 64, 256, 0, 1)
+    assert L.nf4q_quantize(0x1008, 1, R(sp), None) == 2
+    assert L.nf4q_gemv(R(sp), 0x1004, 1, 0x2000, None) == 2
+    # a too-small double-quant workspace
+    assert L.nf4q_double_quant(R(sp), 0x6000, 8, None) == 4
+    # empty weights are a no-op that succeeds
+    e = nq.NF4QWeight(None, None, None, None, None, 0, 64, 64, 256, 0, 1)
+    assert L.nf4q_quantize(None, 0, R(e), None) == 0
+    assert L.nf4q_dequantize(R(e), None, None) == 0
+
+
+def test_workspace_size(L):
+    assert L.nf4q_double_quant_workspace_bytes(1 << 20) >= 64
