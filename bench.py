@@ -1,0 +1,535 @@
+#!/usr/bin/env python
+"""Benchmark of the NF4 quantize -> double quant -> dequantize -> GEMV path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One STEP is one pass of the whole decode-side path over the Llama-7B decode
+workload: for each of the three weights [4096x4096], [11008x4096] and
+[4096x11008] (bf16 N(0, 0.02) with 0.1 % outliers, seeds 10-12; x ~ N(0, 1)
+bf16, M = 1): nf4q_quantize (absmax + codes + packing), nf4q_double_quant,
+nf4q_dequantize (bf16 out) and nf4q_gemv.  Inputs are resident in HBM when
+the timed region starts; L2 is flushed (256 MiB write) before every step,
+outside the step's events.  `value` is the step's algorithmic bytes divided
+by its device time (CUDA events), summed over ranks.
+
+The same run also times, on their own workloads, the prefill GEMM (14336x4096
+weight, M = 64..2048, TFLOP/s), the GEMV alone with L2 flushed before each
+launch (all three decode weights, and the 28672x8192 weight at M = 1..16 with
+NF4 and FP4 codes), and the 32-layer Llama-3-8B-shaped stack (whole-stack
+quantize + double quant, and one decode token through its 224 GEMVs).
+
+Multi-GPU: one process per GPU under torchrun; every rank runs the same
+workload on its own GPU (replicas: the path has no exchange step), time is
+the max over ranks, value the sum.  `--impl reference` times the CPU oracle
+on a bounded sample of the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NF4 GEMV effective weight GB/s and % of HBM peak; NF4 GEMM TFLOP/s"
+WORKLOAD = ("Llama-7B decode shapes [4096x4096], [11008x4096], [4096x11008], bf16 "
+            "N(0,0.02) + 0.1% outliers, x bf16 N(0,1) M=1; step = quantize + double "
+            "quant + dequantize + GEMV per weight")
+NS_HBM_GBS = 8000.0   # the "~8 TB/s" HBM figure the target is stated against
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sust=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sust=1400.0, src="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (100 ms) while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.path is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ byte counts
+def nbytes_state(n_elem):
+    nb = n_elem // 64
+    nd = (nb + 255) // 256
+    return n_elem // 2 + nb + 4 * nd + 4     # packed + absmax_q + scale2 + offset
+
+
+def kernel_bytes(N, K, M=1):
+    n = N * K
+    nb = n // 64
+    nd = (nb + 255) // 256
+    return {
+        "quantize": 2 * n + n // 2 + 4 * nb,
+        "double_quant": 4 * nb + nb + 4 * nd + 4,
+        "dequantize": nbytes_state(n) + 2 * n,
+        "gemv": nbytes_state(n) + 2 * M * K + 2 * M * N,
+    }
+
+
+# ------------------------------------------------------------------ our path
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import dequant_matmul_quantize_b300 as nq
+    import synth
+    from dequant_matmul_quantize_b300 import build
+    build.build()
+    L = nq.lib()
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    R = ctypes.byref
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what} failed with status {st}")
+
+    # ---- the decode workload
+    mats = []
+    for i in range(3):
+        w, x = synth.llama7b_decode(i, device=dev)
+        N, K = w.shape
+        qw = nq.QuantizedWeight.empty(N, K, device=dev)
+        ws = nq.dq_workspace(N * K // 64, dev)
+        out = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+        y = torch.empty(1, N, dtype=torch.bfloat16, device=dev)
+        mats.append(dict(w=w, x=x, N=N, K=K, qw=qw, s=qw.struct(), ws=ws, out=out, y=y,
+                         bytes=kernel_bytes(N, K)))
+    names = ["quantize", "double_quant", "dequantize", "gemv"]
+    launches_per_step = 3 * (1 + 2 + 1 + 1)   # quantize, 2 DQ kernels, dequant, gemv
+
+    def launch(m, k):
+        s = m["s"]
+        if k == 0:
+            check(L.nf4q_quantize(m["w"].data_ptr(), nq.IN_BF16, R(s), sp), "quantize")
+        elif k == 1:
+            check(L.nf4q_double_quant(R(s), m["ws"].data_ptr(), m["ws"].numel(), sp), "dq")
+        elif k == 2:
+            check(L.nf4q_dequantize(R(s), m["out"].data_ptr(), sp), "dequantize")
+        else:
+            check(L.nf4q_gemv(R(s), m["x"].data_ptr(), 1, m["y"].data_ptr(), sp), "gemv")
+
+    def step(evs=None):
+        j = 0
+        for m in mats:
+            for k in range(4):
+                if evs is not None:
+                    evs[j].record(stream)
+                launch(m, k)
+                j += 1
+        if evs is not None:
+            evs[j].record(stream)
+
+    step_bytes = sum(sum(m["bytes"].values()) for m in mats)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    per_step = [[E() for _ in range(13)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush()
+            step(per_step[i])
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - t0
+    clocks = clk.summary()
+    kern_ms = {n: 0.0 for n in names}
+    step_ms = []
+    for evs in per_step:
+        tot = 0.0
+        for j in range(12):
+            dt = evs[j].elapsed_time(evs[j + 1])
+            kern_ms[names[j % 4]] += dt
+            tot += dt
+        step_ms.append(tot)
+    dev_ms = sum(step_ms)
+    dev_ms_max = max_over_ranks(dev_ms)
+    ms_per_step = dev_ms_max / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # roofline of the kernel with the largest share of the step
+    dom = max(kern_ms, key=kern_ms.get)
+    dom_bytes = sum(m["bytes"][dom] for m in mats)      # per step, 3 launches
+    dom_ms = kern_ms[dom] / args.steps                  # per step
+    launches_dom = 3
+    achieved = (dom_bytes / launches_dom) / (dom_ms / launches_dom * 1e-3) / 1e9
+    roofline = {"kernel": "nf4q_" + dom, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+                "peak_source": peaks["src"] + " HBM copy bandwidth",
+                "bytes_per_launch": dom_bytes // launches_dom, "traffic": None,
+                "share_of_step": round(kern_ms[dom] / dev_ms, 3)}
+    breakdown = {n: {"ms_per_step": round(kern_ms[n] / args.steps, 4),
+                     "GB/s": round(sum(m["bytes"][n] for m in mats)
+                                   / (kern_ms[n] / args.steps * 1e-3) / 1e9, 1),
+                     "share": round(kern_ms[n] / dev_ms, 3)} for n in names}
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "bytes_per_step": step_bytes,
+                   "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "breakdown": breakdown,
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+        "clocks": clocks,
+    }
+
+    # ---- e2e: host buffers, copies inside the timed region
+    host_w = [m["w"].cpu().pin_memory() for m in mats]
+    host_x = [m["x"].cpu().pin_memory() for m in mats]
+    host_y = [torch.empty(1, m["N"], dtype=torch.bfloat16).pin_memory() for m in mats]
+    h2d = sum(t.numel() * 2 for t in host_w) + sum(t.numel() * 2 for t in host_x)
+    d2h = sum(t.numel() * 2 for t in host_y)
+
+    def e2e_step():
+        for m, hw, hx, hy in zip(mats, host_w, host_x, host_y):
+            m["w"].copy_(hw, non_blocking=True)
+            m["x"].copy_(hx, non_blocking=True)
+            for k in range(4):
+                launch(m, k)
+            hy.copy_(m["y"], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = E(), E()
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+    result["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1),
+                     "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                     "api": "C ABI via the ctypes binding, pinned host buffers"}
+
+    if not args.no_extras:
+        result.update(run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream))
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_sample()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
+    """GEMV alone (L2 flushed before each launch), prefill GEMM, and the
+    Llama-3-8B stack.  Each timed with CUDA events per launch."""
+    out = {}
+    sp = stream.cuda_stream
+    R = ctypes.byref
+    reps = 10
+
+    def timed(fn, n=reps, do_flush=True):
+        ts = []
+        for _ in range(2):
+            fn()
+        for _ in range(n):
+            if do_flush:
+                flush()
+            a, b = E(), E()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    # GEMV alone on the three decode weights
+    gem = []
+    tot_b, tot_ms = 0, 0.0
+    for i in range(3):
+        w, x = synth.llama7b_decode(i, device=dev)
+        qw = nq.quantize(w)
+        y = torch.empty(1, w.shape[0], dtype=torch.bfloat16, device=dev)
+        s = qw.struct()
+        ms = timed(lambda: L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), sp))
+        b = kernel_bytes(*w.shape)["gemv"]
+        gem.append({"shape": list(w.shape), "us": round(ms * 1e3, 2),
+                    "GB/s": round(b / (ms * 1e-3) / 1e9, 1)})
+        tot_b += b
+        tot_ms += ms
+        del w, qw
+    gbs = tot_b / (tot_ms * 1e-3) / 1e9
+    out["gemv"] = {"workload": "Llama-7B decode weights, M=1, L2 flushed before each launch",
+                   "GB/s": round(gbs, 1), "frac_measured_hbm": round(gbs / peaks["hbm"], 4),
+                   "frac_8TBps": round(gbs / NS_HBM_GBS, 4), "per_weight": gem}
+
+    # 70B-MLP weight, M sweep, NF4 and FP4
+    w = synth.mlp70b_weight(device=dev)
+    sweep = []
+    for code in ("nf4", "fp4"):
+        qw = nq.quantize(w, code)
+        s = qw.struct()
+        for M in (1, 4, 8, 16):
+            x = synth.mlp70b_x(M, device=dev)
+            y = torch.empty(M, w.shape[0], dtype=torch.bfloat16, device=dev)
+            ms = timed(lambda: L.nf4q_gemv(R(s), x.data_ptr(), M, y.data_ptr(), sp))
+            b = kernel_bytes(*w.shape, M=M)["gemv"]
+            sweep.append({"code": code, "M": M, "us": round(ms * 1e3, 2),
+                          "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                          "frac_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)})
+        del qw
+    del w
+    out["gemv_70b_mlp"] = {"workload": "28672x8192 bf16 N(0,0.015), L2 flushed", "points": sweep}
+
+    # prefill GEMM
+    w = synth.prefill_weight(device=dev)
+    qw = nq.quantize(w)
+    s = qw.struct()
+    pts = []
+    for M in (16, 32, 64, 256, 512, 2048):
+        x = synth.prefill_x(M, device=dev)
+        y = torch.empty(M, w.shape[0], dtype=torch.bfloat16, device=dev)
+        fn = (lambda: L.nf4q_gemm(R(s), x.data_ptr(), M, y.data_ptr(), sp))
+        ms = timed(fn)
+        fl = 2.0 * M * w.shape[0] * w.shape[1]
+        tf = fl / (ms * 1e-3) / 1e12
+        ms_gemv = None
+        if M <= 16:
+            ms_gemv = timed(lambda: L.nf4q_gemv(R(s), x.data_ptr(), M, y.data_ptr(), sp))
+        # the two-kernel alternative: dequantize, then cuBLAS bf16
+        deq = torch.empty_like(w)
+        def two():
+            L.nf4q_dequantize(R(s), deq.data_ptr(), sp)
+            torch.matmul(x, deq.T, out=y)
+        ms_two = timed(two)
+        pts.append({"M": M, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                    "frac_bf16_burst": round(tf / peaks["bf16"], 4),
+                    "us_dequant_plus_cublas": round(ms_two * 1e3, 1),
+                    **({"us_gemv": round(ms_gemv * 1e3, 1)} if ms_gemv else {})})
+        del deq
+    out["gemm"] = {"workload": "prefill 14336x4096 NF4 weight, X bf16 [M x 4096]",
+                   "points": pts, "peak_bf16_tflops": peaks["bf16"],
+                   "peak_source": peaks["src"] + " cuBLAS bf16 burst"}
+    del w, qw
+
+    # Llama-3-8B stack: whole-stack quantize + double quant, one decode token
+    if not args.no_stack:
+        stack = []
+        tot_n = 0
+        for layer in range(synth.LLAMA3_8B_LAYERS):
+            for mid in range(7):
+                w = synth.llama3_8b_matrix(layer, mid, device=dev)
+                x = synth.llama3_8b_x(layer, mid, device=dev)
+                qw = nq.QuantizedWeight.empty(*w.shape, device=dev)
+                ws = nq.dq_workspace(w.numel() // 64, dev)
+                y = torch.empty(1, w.shape[0], dtype=torch.bfloat16, device=dev)
+                stack.append((w, x, qw, qw.struct(), ws, y))
+                tot_n += w.numel()
+
+        def quant_all():
+            for w, x, qw, s, ws, y in stack:
+                L.nf4q_quantize(w.data_ptr(), nq.IN_BF16, R(s), sp)
+                L.nf4q_double_quant(R(s), ws.data_ptr(), ws.numel(), sp)
+
+        def token():
+            for w, x, qw, s, ws, y in stack:
+                L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), sp)
+
+        qms = timed(quant_all, n=3)
+        qbytes = sum(kernel_bytes(*t[0].shape)["quantize"] + kernel_bytes(*t[0].shape)["double_quant"]
+                     for t in stack)
+        tms = timed(token, n=5)
+        tbytes = sum(kernel_bytes(*t[0].shape)["gemv"] for t in stack)
+        out["llama3_8b_stack"] = {
+            "workload": "32 layers x {q,k,v,o,gate,up,down}, 6.98e9 weights, bf16 N(0,0.02)",
+            "quantize_dq_ms": round(qms, 3), "quantize_dq_GB/s": round(qbytes / (qms * 1e-3) / 1e9, 1),
+            "decode_token_ms": round(tms, 4), "decode_token_GB/s": round(tbytes / (tms * 1e-3) / 1e9, 1),
+            "decode_gemv_launches": len(stack)}
+        del stack
+    return out
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+def _limit_threads():
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(1)
+    except Exception:
+        return None
+
+
+def oracle_sample(rows=1024):
+    """The oracle's whole path on the first `rows` rows of the [4096x4096]
+    decode weight: quantize, double quant, dequantize, fp64 GEMV.  Returns
+    (seconds, algorithmic bytes of the same work on the GPU path)."""
+    import numpy as np
+    import torch
+    import synth
+    from oracle import nf4_oracle as o
+    w, x = synth.llama7b_decode(0, device="cpu")
+    w = w[:rows].float().numpy()
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    r = o.quantize_full(w)
+    o.matmul_ref(xb, r["w_hat"].reshape(w.shape))
+    dt = time.perf_counter() - t0
+    return dt, sum(kernel_bytes(rows, w.shape[1]).values())
+
+
+def cpu_baseline_sample():
+    lim = _limit_threads()
+    dt, b = oracle_sample(1024)
+    if lim is not None:
+        lim.unregister() if hasattr(lim, "unregister") else None
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": "rows 0..1023 of the 4096x4096 decode weight: quantize + double "
+                      "quant + dequantize + fp64 GEMV (NumPy, one thread)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    lim = _limit_threads()
+    rows = 256
+    for _ in range(max(3, args.warmup)):
+        oracle_sample(rows)
+    tot, b = 0.0, 0
+    for _ in range(args.steps):
+        dt, bb = oracle_sample(rows)
+        tot += dt
+        b += bb
+    value = b / tot / 1e9
+    sample = (f"rows 0..{rows - 1} of the 4096x4096 decode weight per step: quantize + "
+              "double quant + dequantize + fp64 GEMV (NumPy, one thread)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="only the step and e2e")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 7B-weight stack")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
