@@ -320,4 +320,63 @@ nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear) {
   return NF4Q_OK;
 }
 
+// ---------------------------------------------------------------- no-alloc
+// Static scratch of nf4q_double_quant_noalloc.  In host code the symbol is
+// only a handle: its device address comes from cudaGetSymbolAddress, looked
+// up once per device with that device current.
+static __device__ __align__(256) unsigned char g_dq_noalloc_scratch[256];
+static_assert(sizeof(DqWorkspace) <= 256, "double-quant record must fit the static scratch");
+
+namespace {
+void* noalloc_scratch(nf4q_status* st) {
+  static void* addr[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *st = NF4Q_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dq_noalloc_scratch) != cudaSuccess || !p) {
+      *st = NF4Q_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *st = NF4Q_OK;
+  return addr[dev];
+}
+}  // namespace
+
+nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  const int64_t nb = wq->rows * wq->cols / kBlock;
+  if (!wq->absmax_q || !wq->scale2 || !wq->offset) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned4(wq->offset) || !aligned4(wq->scale2)) return NF4Q_ERR_ALIGNMENT;
+  if (nf4q_double_quant_workspace_bytes(nb) > sizeof(g_dq_noalloc_scratch))
+    return NF4Q_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (nb == 0) {
+    if (cudaMemsetAsync(wq->offset, 0, sizeof(float), s) != cudaSuccess) return NF4Q_ERR_CUDA;
+    return NF4Q_OK;
+  }
+  if (!wq->absmax) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(wq->absmax) || !aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;
+  void* ws = noalloc_scratch(&st);
+  if (st != NF4Q_OK) return st;
+  if (cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
+  const int64_t g1 = grid_for(nb, kDqSumThreads, static_cast<int64_t>(sm_count()) * 2);
+  dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb, static_cast<DqWorkspace*>(ws),
+                                             wq->offset);
+  if ((st = launch_status()) != NF4Q_OK) return st;
+  const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
+  const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
+  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset,
+                                                  wq->absmax_q, wq->scale2);
+  return launch_status();
+}
+
 }  // extern "C"

@@ -175,6 +175,28 @@ nf4q_status nf4q_matmul(const nf4q_weight* wq, const void* X, int64_t M,
  * wait gave up).  Synchronizes the device; `clear` != 0 resets the flags. */
 nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear);
 
+/* Double quantization without a caller-supplied workspace: the same
+ * computation and outputs as nf4q_double_quant, for callers that must not
+ * allocate device memory at all - e.g. code that runs with every byte of
+ * device memory already handed to a fixed pool, or that cannot afford
+ * cudaMalloc's implicit device synchronization on a latency-critical path,
+ * and so has nowhere to get the small workspace from.  (The bitsandbytes
+ * pages have no counterpart; this is an interface convenience only.)
+ *   Scratch: a 256-byte array in the library's static device memory, present
+ *   on every GPU the library is loaded on until the process exits.  The call
+ *   allocates nothing and calls no allocating routine.
+ *   Limit: the scratch holds one double-quant record, which serves any tensor
+ *   the library accepts (n_b = rows*cols/64 up to 2^31 - 1); a tensor whose
+ *   workspace would not fit is refused with NF4Q_ERR_UNSUPPORTED.
+ *   Set-up: the first call on each device looks up the scratch's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.
+ *   Sharing: every call on a device uses the same scratch; the call clears it
+ *   (cudaMemsetAsync on `stream`) before use.  Calls whose work overlaps on
+ *   the GPU (other streams, other threads) race on it and must be serialized
+ *   by the caller.  Other arguments and errors as nf4q_double_quant. */
+nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif
