@@ -2,132 +2,61 @@
 // cores ("bitsandbytes tutorial", sec. 3.4: the 4-bit weight is dequantized
 // to bf16 and an ordinary bf16 matmul with fp32 accumulation follows).
 //
-// One CTA computes a 128 x 256 tile of Y with tcgen05.mma (kind::f16, bf16
-// operands, fp32 accumulator in tensor memory), K in steps of 64:
-//   warp 0      TMA producer: the X tile (128 x 64 bf16, 128-byte swizzle)
-//               and the packed W tile (256 rows x 32 bytes, 32-byte swizzle)
-//               of each stage, one mbarrier with the transaction byte count.
-//   warp 1      allocates 256 TMEM columns; one lane issues the four
-//               128x256x16 MMAs of a stage and commits them to the stage's
-//               "empty" barrier, and after the last stage to "acc_full".
-//   warps 2..9  dequantize: thread r rebuilds row r of the W tile,
-//               w_hat = bf16(code[nibble] * s_b) exactly as nf4_dequantize,
-//               into the K-major 128-byte-swizzled layout the MMA reads,
-//               then fence.proxy.async and arrive on the stage's "b_full".
-//               After the main loop the same warps drain TMEM (tcgen05.ld),
-//               round to bf16 and store Y.
-// Every wait is bounded (about 2 s of %globaltimer); a wait that gives up
-// sets bit 0 of the device error word and the CTA winds down: it waits
-// (bounded) for its own TMA copies and MMAs, frees its TMEM and returns.
+// One CTA computes a 256 x BN tile of Y as two 128 x BN halves that share
+// every dequantized W tile (so each weight is rebuilt once per 256 rows of
+// X), with tcgen05.mma (kind::f16, bf16 operands, two fp32 accumulators in
+// tensor memory), K in steps of 64:
+//   warp 0      TMA producer: the two X tiles (128 x 64 bf16 each, 128-byte
+//               swizzle) and the packed W tile (BN rows x 32 bytes, 32-byte
+//               swizzle) of a stage, one mbarrier with the byte count.
+//   warp 1      allocates 512 TMEM columns; one lane issues the 2 x 4
+//               128xBNx16 MMAs of a stage and commits them to the stage's
+//               "empty" barrier, after the last stage to "acc_full".
+//   warps 2..9  dequantize: thread r rebuilds row r of the W tile with the
+//               register byte tables of lut.cuh (bit-exact w_hat) into the
+//               K-major 128-byte-swizzled layout the MMA reads, then
+//               fence.proxy.async and arrive on the stage's "b_full".
+//               Afterwards warps 2-5 drain accumulator 0 and warps 6-9
+//               accumulator 1 (tcgen05.ld), round to bf16 and store Y.
+// BN (128..256) is picked per shape so the tile count fills whole waves of
+// the SMs.  Every wait is bounded (1 s of %globaltimer); a wait that gives up
+// sets bit 0 of the device error word and the CTA winds down: its other
+// waits stop, its TMA copies and MMAs are drained (bounded), its TMEM freed.
 // No multicast: every CTA loads its own tiles.
 #pragma once
 
-#include <cuda.h>
-
 #include "common.cuh"
+#include "lut.cuh"
+#include "tma.cuh"
 
 namespace nf4q {
 
-constexpr int kGemmBM = 128;
-constexpr int kGemmBN = 256;
+constexpr int kGemmBM = 128;   // rows per accumulator (two per CTA)
 constexpr int kGemmBK = 64;
-constexpr int kGemmStages = 3;
 constexpr int kGemmThreads = 320;
 constexpr int kGemmATile = kGemmBM * kGemmBK * 2;    // 16 KB
-constexpr int kGemmBTile = kGemmBN * kGemmBK * 2;    // 32 KB
-constexpr int kGemmPTile = kGemmBN * kGemmBK / 2;    // 8 KB
-constexpr int kGemmTmemCols = 256;
-constexpr size_t kGemmSmemBytes =
-    1024 + kGemmStages * (kGemmATile + kGemmBTile + kGemmPTile) + 1024 + 16 * 32 * 4;
+constexpr int kGemmTmemCols = 512;
 
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+template <int BN>
+struct GemmCfg {
+  static constexpr int kBTile = BN * kGemmBK * 2;     // bf16 W tile
+  static constexpr int kPTile = BN * kGemmBK / 2;     // packed W tile
+  static constexpr int kAStages = 4;                  // TMA stages: 2 X tiles + packed W
+  static constexpr int kAStage = 2 * kGemmATile + kPTile;
+  static constexpr int kBStages =                     // dequantized W stages
+      (kAStages * kAStage + 3 * kBTile + 2048 <= 232448 - 1024) ? 3 : 2;
+  static constexpr size_t kSmem = 1024 + kAStages * kAStage + kBStages * kBTile + 1024;
+  static_assert(kPTile % 1024 == 0 && kBTile % 1024 == 0, "1 KB alignment of tiles");
+  static_assert(kSmem <= 232448, "shared memory");
+};
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
-
-// Bounded wait for the phase of the given parity.  Gives up (false) after
-// the time limit, or as soon as another thread of the CTA has given up
-// (`abort` in shared memory), so a stuck CTA winds down quickly.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile uint32_t* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      *abort = 1u;
-      atomicOr(&g_device_error, 1u);
-      return false;
-    }
-  }
-}
-
-// Bounded wait that ignores the CTA abort flag: used before the CTA exits,
-// to let its own TMA copies and MMAs finish.
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) {
-      atomicOr(&g_device_error, 1u);
-      return;
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0,
-                                            int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
+// Scale inputs of one W row for 16 consecutive k-steps (64-blocks): the 16
+// absmax_q bytes (or fp32 absmax) and their scale2, loaded a group ahead.
+struct ScaleGroup {
+  uint4 q;          // 16 int8 codes of the scales
+  float s2a, s2b;   // scale2 of the first block and of the block after the
+  int split;        // first k-step (0..16) whose block uses s2b
+};
 
 // K-major operand in the 128-byte swizzled layout: rows of 128 bytes, 8-row
 // groups 1024 bytes apart.  Shared-memory matrix descriptor fields: start
@@ -178,40 +107,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // ------------------------------------------------------------ the kernel
+template <int CODE, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
             const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
             uint16_t* __restrict__ Y, int M, int N, int K,
             const __grid_constant__ CodeValues C) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int SA = Cfg::kAStages, SB = Cfg::kBStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sA = base;
-  const uint32_t sB = sA + kGemmStages * kGemmATile;
-  const uint32_t sP = sB + kGemmStages * kGemmBTile;
-  const uint32_t sBar = sP + kGemmStages * kGemmPTile;   // 1 KB of barriers
-  uint8_t* gB = gbase + (sB - base);
-  const uint8_t* gP = gbase + (sP - base);
+  auto sA = [&](int s, int h) { return base + s * Cfg::kAStage + h * kGemmATile; };
+  auto sP = [&](int s) { return base + s * Cfg::kAStage + 2 * kGemmATile; };
+  auto sB = [&](int s) { return base + SA * Cfg::kAStage + s * Cfg::kBTile; };
+  const uint32_t sBar = base + SA * Cfg::kAStage + SB * Cfg::kBTile;   // 1 KB of barriers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sBar - base) + 512);
   volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(gbase + (sBar - base) + 516);
-  float* s_code = reinterpret_cast<float*>(gbase + (sBar - base) + 1024);
+  // full: TMA landed; aempty: MMA done with the TMA slot;
+  // bfull: dequantized tile written; bempty: MMA done with the B slot
   auto full_bar = [&](int s) { return sBar + 8u * s; };
-  auto bfull_bar = [&](int s) { return sBar + 8u * (kGemmStages + s); };
-  auto empty_bar = [&](int s) { return sBar + 8u * (2 * kGemmStages + s); };
-  const uint32_t acc_bar = sBar + 8u * (3 * kGemmStages);
+  auto aempty_bar = [&](int s) { return sBar + 8u * (SA + s); };
+  auto bfull_bar = [&](int s) { return sBar + 8u * (2 * SA + s); };
+  auto bempty_bar = [&](int s) { return sBar + 8u * (2 * SA + SB + s); };
+  const uint32_t acc_bar = sBar + 8u * (2 * SA + 2 * SB);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kGemmBN, m0 = blockIdx.y * kGemmBM;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (2 * kGemmBM);
   const int KT = K / kGemmBK;
 
-  for (int i = threadIdx.x; i < 16 * 32; i += blockDim.x) s_code[i] = C.v[i >> 5];
   if (threadIdx.x == 0) {
     *abort = 0u;
-    for (int s = 0; s < kGemmStages; ++s) {
+    for (int s = 0; s < SA; ++s) {
       mbar_init(full_bar(s), 1);
+      mbar_init(aempty_bar(s), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
       mbar_init(bfull_bar(s), 8);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(bempty_bar(s), 1);
     }
     mbar_init(acc_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -235,97 +169,127 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
       int issued = 0;
       for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kGemmStages;
-        const uint32_t ph = (kt / kGemmStages) & 1;
-        if (!mbar_wait(empty_bar(s), ph ^ 1, abort)) break;
-        mbar_arrive_expect_tx(full_bar(s), kGemmATile + kGemmPTile);
-        tma_load_2d(sA + s * kGemmATile, &tmap_x, kt * kGemmBK, m0, full_bar(s));
-        tma_load_2d(sP + s * kGemmPTile, &tmap_w, kt * (kGemmBK / 2), n0, full_bar(s));
+        const int s = kt % SA;
+        const uint32_t ph = (kt / SA) & 1;
+        if (!mbar_wait(aempty_bar(s), ph ^ 1, abort)) break;
+        mbar_arrive_expect_tx(full_bar(s), 2 * kGemmATile + Cfg::kPTile);
+        tma_load_2d(sA(s, 0), &tmap_x, kt * kGemmBK, m0, full_bar(s));
+        tma_load_2d(sA(s, 1), &tmap_x, kt * kGemmBK, m0 + kGemmBM, full_bar(s));
+        tma_load_2d(sP(s), &tmap_w, kt * (kGemmBK / 2), n0, full_bar(s));
         issued = kt + 1;
       }
       // wind-down: make sure no copy is still landing in this CTA's smem
-      for (int kt = (issued > kGemmStages ? issued - kGemmStages : 0); kt < issued; ++kt)
-        mbar_wait_drain(full_bar(kt % kGemmStages), (kt / kGemmStages) & 1);
+      for (int kt = (issued > SA ? issued - SA : 0); kt < issued; ++kt)
+        mbar_wait_drain(full_bar(kt % SA), (kt / SA) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(kGemmBM, kGemmBN);
+      constexpr uint32_t idesc = make_idesc_bf16(kGemmBM, BN);
       for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kGemmStages;
-        const uint32_t ph = (kt / kGemmStages) & 1;
-        if (!mbar_wait(full_bar(s), ph, abort)) break;
-        if (!mbar_wait(bfull_bar(s), ph, abort)) break;
+        const int sa = kt % SA, sb = kt % SB;
+        if (!mbar_wait(full_bar(sa), (kt / SA) & 1, abort)) break;
+        if (!mbar_wait(bfull_bar(sb), (kt / SB) & 1, abort)) break;
         tc_fence_after();
-        const uint32_t a0 = sA + s * kGemmATile, b0 = sB + s * kGemmBTile;
 #pragma unroll
         for (int k = 0; k < kGemmBK / 16; ++k) {
-          mma_bf16(tmem, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), idesc,
-                   (kt > 0 || k > 0) ? 1u : 0u);
+          const uint64_t bdesc = smem_desc_sw128(sB(sb) + 32 * k);
+          const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
+          mma_bf16(tmem, smem_desc_sw128(sA(sa, 0) + 32 * k), bdesc, idesc, acc);
+          mma_bf16(tmem + 256, smem_desc_sw128(sA(sa, 1) + 32 * k), bdesc, idesc, acc);
         }
-        mma_commit(empty_bar(s));
+        mma_commit(aempty_bar(sa));
+        mma_commit(bempty_bar(sb));
       }
       mma_commit(acc_bar);  // fires once every MMA issued above has completed
     }
   } else {
-    // ---------------- dequantize producers (256 threads, one W row each)
+    // ---------------- dequantize producers (one W row per thread)
     const int r = threadIdx.x - 64;
+    const bool active = r < BN;
     const int n = n0 + r;
-    const bool row_ok = n < N;
-    const int64_t row_block0 = static_cast<int64_t>(n) * (K / kBlock);
-    const float* code = s_code + lane;
-    float s_next = (row_ok && KT > 0) ? block_scale(sv, row_block0) : 0.f;
-    bool ok = true;
-    for (int kt = 0; kt < KT && ok; ++kt) {
-      const int s = kt % kGemmStages;
-      const uint32_t ph = (kt / kGemmStages) & 1;
-      const float sc = s_next;
-      if (row_ok && kt + 1 < KT) s_next = block_scale(sv, row_block0 + kt + 1);
-      // B slot s is free once the MMAs of the previous round on it are done
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_bar(s), ph ^ 1, abort) &&
-                                       mbar_wait(full_bar(s), ph, abort))) {
-        ok = false;
-        break;
+    const bool row_ok = active && n < N;
+    const int kblocks = K / kBlock;
+    const int64_t row_block0 = static_cast<int64_t>(n) * kblocks;
+    // scales are read 16 k-steps at a time, one group ahead
+    const bool vec_q = sv.double_quant && (kblocks & 15) == 0;
+    auto load_group = [&](ScaleGroup& g, int kt0) {
+      g.q = make_uint4(0, 0, 0, 0);
+      g.s2a = g.s2b = 0.f;
+      g.split = 16;
+      if (!row_ok || kt0 >= KT || !sv.double_quant) return;
+      const int64_t b0 = row_block0 + kt0;
+      if (vec_q) {
+        g.q = __ldg(reinterpret_cast<const uint4*>(sv.absmax_q + b0));
+      } else {
+        uint32_t w[4] = {0, 0, 0, 0};
+        for (int j = 0; j < 16 && kt0 + j < KT; ++j)
+          w[j >> 2] |= (static_cast<uint32_t>(static_cast<uint8_t>(__ldg(sv.absmax_q + b0 + j))))
+                       << (8 * (j & 3));
+        g.q = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      const uint8_t* prow = gP + s * kGemmPTile + r * 32;
-      const int sw = (r >> 2) & 1;  // 32-byte swizzle of the TMA tile
-      const uint4 p0 = *reinterpret_cast<const uint4*>(prow + ((0 ^ sw) << 4));
-      const uint4 p1 = *reinterpret_cast<const uint4*>(prow + ((1 ^ sw) << 4));
-      const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-      uint8_t* brow = gB + s * kGemmBTile + r * 128;
+      g.s2a = __ldg(sv.scale2 + (b0 >> 8));
+      const int64_t nextd = ((b0 >> 8) + 1) << 8;   // first block of the next 256
+      g.split = static_cast<int>(nextd - b0 < 16 ? nextd - b0 : 16);
+      if (g.split < 16 && kt0 + g.split < KT) g.s2b = __ldg(sv.scale2 + (nextd >> 8));
+    };
+    const float off = sv.double_quant ? __ldg(sv.offset) : 0.f;
+    ScaleGroup gcur, gnext;
+    load_group(gcur, 0);
+    load_group(gnext, 16);
+    for (int kt = 0; kt < KT; ++kt) {
+      const int sa = kt % SA, sb = kt % SB;
+      const int j = kt & 15;
+      if (j == 0 && kt > 0) {
+        gcur = gnext;
+        load_group(gnext, kt + 16);
+      }
+      float sc;
+      if (sv.double_quant) {
+        const uint32_t qw = j < 8 ? (j < 4 ? gcur.q.x : gcur.q.y) : (j < 12 ? gcur.q.z : gcur.q.w);
+        const float q = static_cast<float>(static_cast<int8_t>((qw >> (8 * (j & 3))) & 0xFFu));
+        sc = __fmaf_rn(q, j < gcur.split ? gcur.s2a : gcur.s2b, off);
+      } else {
+        sc = row_ok ? __ldg(sv.absmax + row_block0 + kt) : 0.f;
+      }
+      RowTable<CODE> T;
+      build_table<CODE>(T, sc, C);
+      // B slot sb is free once the MMAs of the previous round on it are done
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bempty_bar(sb), ((kt / SB) & 1) ^ 1, abort) &&
+                                       mbar_wait(full_bar(sa), (kt / SA) & 1, abort)))
+        break;
+      if (active) {
+        const uint8_t* prow = gbase + (sP(sa) - base) + r * 32;
+        const int sw = (r >> 2) & 1;  // 32-byte swizzle of the TMA tile
+        const uint4 p0 = *reinterpret_cast<const uint4*>(prow + ((0 ^ sw) << 4));
+        const uint4 p1 = *reinterpret_cast<const uint4*>(prow + ((1 ^ sw) << 4));
+        const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        uint8_t* brow = gbase + (sB(sb) - base) + r * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // chunk c = elements 8c..8c+7 = packed word c
-        const uint32_t p = words[c];
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t nib = (p >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 0xFu;
-          f[i] = __fmul_rn(code[nib * 32], sc);
+        for (int c = 0; c < 8; ++c) {  // chunk c = elements 8c..8c+7 = packed word c
+          uint32_t o[4];
+          dequant_word<CODE>(T, words[c], o);
+          *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        uint4 o;
-        o.x = pack_bf16x2(f[0], f[1]);
-        o.y = pack_bf16x2(f[2], f[3]);
-        o.z = pack_bf16x2(f[4], f[5]);
-        o.w = pack_bf16x2(f[6], f[7]);
-        *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bfull_bar(s));
+      if (lane == 0) mbar_arrive(bfull_bar(sb));
     }
     // ---------------- epilogue: TMEM -> bf16 -> Y
     if (__all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
       tc_fence_after();
-      const int q = warp & 3;        // TMEM lane quarter this warp may read
-      const int h = (warp - 2) >> 2;  // column half
-      const int m = m0 + q * 32 + lane;
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col = h * 128 + cc * 32;
+      const int q = warp & 3;          // TMEM lane quarter this warp may read
+      const int h = (warp - 2) >> 2;   // accumulator (M half)
+      const int m = m0 + h * kGemmBM + q * 32 + lane;
+      uint16_t* yrow = Y + static_cast<int64_t>(m) * N + n0;
+      const bool vec = (N & 7) == 0;
+#pragma unroll 1
+      for (int col = 0; col < BN; col += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col, v);
+        tmem_ld32(tmem + h * 256 + (static_cast<uint32_t>(q * 32) << 16) + col, v);
         if (m < M) {
-          uint16_t* yrow = Y + static_cast<int64_t>(m) * N + n0 + col;
           const int ncols = min(32, N - (n0 + col));
-          if (ncols == 32 && (N & 7) == 0) {
+          if (ncols == 32 && vec) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint4 o;
@@ -333,14 +297,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
               o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
               o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
               o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-              *reinterpret_cast<uint4*>(yrow + 8 * j) = o;
+              *reinterpret_cast<uint4*>(yrow + col + 8 * j) = o;
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               if (j < ncols) {
                 const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
-                yrow[j] = *reinterpret_cast<const uint16_t*>(&b);
+                yrow[col + j] = *reinterpret_cast<const uint16_t*>(&b);
               }
             }
           }
@@ -360,72 +324,87 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
   }
 }
 
-// ------------------------------------------------------------ host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
-inline EncodeTiledFn encode_tiled_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
+// Pick BN so that the number of 256 x BN tiles fills whole waves of the SMs.
+inline int gemm_pick_bn(int64_t M, int64_t N, int sms) {
+  const int cands[5] = {256, 224, 192, 160, 128};
+  const int64_t mt = (M + 2 * kGemmBM - 1) / (2 * kGemmBM);
+  int best = 256;
+  double best_eff = -1.0;
+  for (int bn : cands) {
+    const int64_t tiles = mt * ((N + bn - 1) / bn);
+    const int64_t rounds = (tiles + sms - 1) / sms;
+    // useful columns / columns the rounds could have computed
+    const double eff = static_cast<double>(N) * mt / (static_cast<double>(rounds) * sms * bn);
+    if (eff > best_eff + 1e-9) { best_eff = eff; best = bn; }
   }
-  return fn;
+  return best;
 }
 
-inline nf4q_status gemm_launch(const nf4q_weight* wq, const ScaleView& sv,
-                               const CodeValues& C, const void* X, int64_t M, void* Y,
-                               cudaStream_t stream, int /*sms*/) {
+template <int CODE, int BN>
+inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, const ScaleView& sv,
+                                  const CodeValues& C, int64_t M, void* Y, cudaStream_t stream) {
+  using Cfg = GemmCfg<BN>;
   const int64_t N = wq->rows, K = wq->cols;
-  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return NF4Q_ERR_CUDA;
-  CUtensorMap tx, tw;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {kGemmBK, kGemmBM};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return NF4Q_ERR_CUDA;
-  }
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[2] = {kGemmBK / 2, kGemmBN};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return NF4Q_ERR_CUDA;
-  }
+  CUtensorMap tw;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint32_t box[2] = {kGemmBK / 2, BN};
+  cuuint32_t es[2] = {1, 1};
+  if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return NF4Q_ERR_CUDA;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kGemmSmemBytes)) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_kernel<CODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Cfg::kSmem)) != cudaSuccess)
       return NF4Q_ERR_CUDA;
     attr_set[dev] = true;
   }
-  if ((M + kGemmBM - 1) / kGemmBM > 65535) return NF4Q_ERR_UNSUPPORTED;
-  dim3 grid(static_cast<unsigned>((N + kGemmBN - 1) / kGemmBN),
-            static_cast<unsigned>((M + kGemmBM - 1) / kGemmBM));
-  gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(
+  dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
+            static_cast<unsigned>((M + 2 * kGemmBM - 1) / (2 * kGemmBM)));
+  gemm_kernel<CODE, BN><<<grid, kGemmThreads, Cfg::kSmem, stream>>>(
       tx, tw, sv, static_cast<uint16_t*>(Y), static_cast<int>(M), static_cast<int>(N),
       static_cast<int>(K), C);
   return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
+}
+
+template <int CODE>
+inline nf4q_status gemm_launch_code(const CUtensorMap& tx, const nf4q_weight* wq,
+                                    const ScaleView& sv, const CodeValues& C, int64_t M, void* Y,
+                                    cudaStream_t stream, int bn) {
+  switch (bn) {
+    case 224: return gemm_launch_bn<CODE, 224>(tx, wq, sv, C, M, Y, stream);
+    case 192: return gemm_launch_bn<CODE, 192>(tx, wq, sv, C, M, Y, stream);
+    case 160: return gemm_launch_bn<CODE, 160>(tx, wq, sv, C, M, Y, stream);
+    case 128: return gemm_launch_bn<CODE, 128>(tx, wq, sv, C, M, Y, stream);
+    default: return gemm_launch_bn<CODE, 256>(tx, wq, sv, C, M, Y, stream);
+  }
+}
+
+inline nf4q_status gemm_launch(const nf4q_weight* wq, const ScaleView& sv,
+                               const CodeValues& C, const void* X, int64_t M, void* Y,
+                               cudaStream_t stream, int sms) {
+  const int64_t N = wq->rows, K = wq->cols;
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
+  if ((M + 2 * kGemmBM - 1) / (2 * kGemmBM) > 65535) return NF4Q_ERR_UNSUPPORTED;
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return NF4Q_ERR_CUDA;
+  CUtensorMap tx;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {kGemmBK, kGemmBM};
+  cuuint32_t es[2] = {1, 1};
+  if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box,
+          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return NF4Q_ERR_CUDA;
+  const int bn = gemm_pick_bn(M, N, sms);
+  return wq->code == 0 ? gemm_launch_code<0>(tx, wq, sv, C, M, Y, stream, bn)
+                       : gemm_launch_code<1>(tx, wq, sv, C, M, Y, stream, bn);
 }
 
 }  // namespace nf4q

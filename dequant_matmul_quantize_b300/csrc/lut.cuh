@@ -1,0 +1,91 @@
+// Exact bf16 dequantization of packed 4-bit codes with register tables.
+//
+// For one (row, 64-block) the 16 values w_hat_j = bf16(fp32(code_j * s_b))
+// - bit for bit what nf4_dequantize writes ("bitsandbytes tutorial", sec.
+// 3.4) - are built once and split into a table of high bytes and one of low
+// bytes (4 + 4 registers of 4 one-byte entries; FP4 keeps the 8 magnitudes,
+// 2 + 2 registers, and takes the sign from bit 3).  Four codes are then
+// looked up with byte permutes (prmt) on the low 3 bits of each nibble, a
+// select on bit 3, and two permutes that interleave high and low bytes into
+// two bf16x2 registers.  About 2.6 integer-pipe instructions per weight.
+#pragma once
+
+#include "common.cuh"
+
+namespace nf4q {
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lop_select(uint32_t if1, uint32_t if0, uint32_t m) {
+  uint32_t r;  // (if1 & m) | (if0 & ~m)
+  asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(r) : "r"(if1), "r"(if0), "r"(m));
+  return r;
+}
+
+// (a0 * s, a1 * s), each rounded to nearest: one packed f32x2 multiply.
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float s, float& r0, float& r1) {
+  uint64_t a, b, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(b) : "f"(s));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
+}
+
+// Byte tables of one (row, block): H[i] / L[i] hold the high / low bytes of
+// w_hat for codes 4i .. 4i+3 (NF4 uses 4+4 registers; FP4 2+2, magnitudes).
+template <int CODE>
+struct RowTable {
+  uint32_t H[CODE == 0 ? 4 : 2];
+  uint32_t L[CODE == 0 ? 4 : 2];
+};
+
+template <int CODE>
+__device__ __forceinline__ void build_table(RowTable<CODE>& T, float s, const CodeValues& C) {
+#pragma unroll
+  for (int i = 0; i < (CODE == 0 ? 4 : 2); ++i) {
+    float f0, f1, f2, f3;
+    mul2_rn(C.v[4 * i + 0], C.v[4 * i + 1], s, f0, f1);
+    mul2_rn(C.v[4 * i + 2], C.v[4 * i + 3], s, f2, f3);
+    const uint32_t p0 = pack_bf16x2(f0, f1);
+    const uint32_t p1 = pack_bf16x2(f2, f3);
+    T.H[i] = prmt(p0, p1, 0x7531);
+    T.L[i] = prmt(p0, p1, 0x6420);
+  }
+}
+
+// Four codes -> two bf16x2 registers.  `sel` holds the four nibbles with
+// bit 3 cleared (low 16 bits), `m` the per-byte 0xFF/0x00 mask of bit 3.
+// Byte j of a lookup belongs to nibble j; nibble 2i+1 is element 2i of the
+// word (high nibble first), so the interleave puts elements (0,1) and (2,3)
+// of these four into the low/high halves of the two outputs.
+template <int CODE>
+__device__ __forceinline__ void lookup4(const RowTable<CODE>& T, uint32_t sel, uint32_t m,
+                                        uint32_t& r01, uint32_t& r23) {
+  uint32_t h, l;
+  if (CODE == 0) {
+    h = lop_select(prmt(T.H[2], T.H[3], sel), prmt(T.H[0], T.H[1], sel), m);
+    l = lop_select(prmt(T.L[2], T.L[3], sel), prmt(T.L[0], T.L[1], sel), m);
+  } else {  // FP4: magnitude lookup, bit 3 flips the sign
+    h = prmt(T.H[0], T.H[1], sel) ^ (m & 0x80808080u);
+    l = prmt(T.L[0], T.L[1], sel);
+  }
+  r01 = prmt(l, h, 0x4051);
+  r23 = prmt(l, h, 0x6273);
+}
+
+// One packed word (8 consecutive codes of one row) -> four bf16x2 registers
+// holding elements (0,1), (2,3), (4,5), (6,7).
+template <int CODE>
+__device__ __forceinline__ void dequant_word(const RowTable<CODE>& T, uint32_t w,
+                                             uint32_t (&r)[4]) {
+  const uint32_t s7 = w & 0x77777777u;
+  const uint32_t w4 = w << 4;
+  lookup4<CODE>(T, s7, prmt(w, w4, 0x9D8C), r[0], r[1]);
+  lookup4<CODE>(T, s7 >> 16, prmt(w, w4, 0xBFAE), r[2], r[3]);
+}
+
+}  // namespace nf4q

@@ -13,6 +13,7 @@
 #include "double_quant.cuh"
 #include "gemm.cuh"
 #include "gemv.cuh"
+#include "gemv_mma.cuh"
 #include "quantize.cuh"
 
 namespace nf4q {
@@ -74,12 +75,29 @@ nf4q_status check_scales(const nf4q_weight* wq) {
   if (!aligned16(wq->packed)) return NF4Q_ERR_ALIGNMENT;
   if (wq->double_quant) {
     if (!wq->absmax_q || !wq->scale2 || !wq->offset) return NF4Q_ERR_INVALID_ARG;
-    if (!aligned4(wq->scale2) || !aligned4(wq->offset)) return NF4Q_ERR_ALIGNMENT;
+    if (!aligned16(wq->absmax_q) || !aligned4(wq->scale2) || !aligned4(wq->offset))
+      return NF4Q_ERR_ALIGNMENT;
   } else {
     if (!wq->absmax) return NF4Q_ERR_INVALID_ARG;
     if (!aligned4(wq->absmax)) return NF4Q_ERR_ALIGNMENT;
   }
   return NF4Q_OK;
+}
+
+// Opt the GEMV kernels in to more than 48 KB of dynamic shared memory
+// (once per device).
+bool gemv_attr_ready() {
+  static bool done[kMaxDevices] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (done[dev]) return true;
+  const int bytes = static_cast<int>(gemv_smem_bytes(16, 2));
+  bool ok = cudaFuncSetAttribute(gemv_mma_kernel<0, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+            cudaFuncSetAttribute(gemv_mma_kernel<0, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+            cudaFuncSetAttribute(gemv_mma_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+            cudaFuncSetAttribute(gemv_mma_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+  done[dev] = ok;
+  return ok;
 }
 
 ScaleView scale_view(const nf4q_weight* wq) {
@@ -263,22 +281,43 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   }
   if ((st = check_scales(wq)) != NF4Q_OK) return st;
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
-  const int64_t grid = grid_for(wq->rows, kGemvSimpleThreads / 32,
-                                static_cast<int64_t>(sm_count()) * 8);
-  const uint32_t* pk = reinterpret_cast<const uint32_t*>(wq->packed);
+  if (wq->rows > (1ll << 30) || wq->cols > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
+  const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
+  // 16 rows per CTA; its warps split K so the grid holds ~24 warps per SM
+  const int NT = M > 8 ? 2 : 1;
+  const int nchunks = (K + kGemvChunk - 1) / kGemvChunk;
+  const int tiles = (N + kGemvRows - 1) / kGemvRows;
+  const int target = sm_count() * 24;
+  int ks = std::max(1, std::min(std::min(16, nchunks), (target + tiles - 1) / tiles));
+  const int per = (nchunks + ks - 1) / ks;
+  ks = (nchunks + per - 1) / per;
+  const size_t smem = gemv_smem_bytes(ks, NT);
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return NF4Q_ERR_CUDA;
+  CUtensorMap tw;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    cuuint32_t box[2] = {kGemvChunk / 2, kGemvRows};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return NF4Q_ERR_CUDA;
+  }
+  if (!gemv_attr_ready()) return NF4Q_ERR_CUDA;
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   uint16_t* yp = static_cast<uint16_t*>(y);
   const ScaleView sv = scale_view(wq);
   const CodeValues C = code_values(wq->code);
-#define NF4Q_GEMV_SIMPLE(MT)                                                  \
-  gemv_simple_kernel<MT><<<grid, kGemvSimpleThreads, 0, s>>>(pk, sv, xp, yp, \
-                                                             wq->rows, wq->cols, M, C)
-  if (M <= 1) NF4Q_GEMV_SIMPLE(1);
-  else if (M <= 2) NF4Q_GEMV_SIMPLE(2);
-  else if (M <= 4) NF4Q_GEMV_SIMPLE(4);
-  else if (M <= 8) NF4Q_GEMV_SIMPLE(8);
-  else NF4Q_GEMV_SIMPLE(16);
-#undef NF4Q_GEMV_SIMPLE
+#define NF4Q_GEMV_MMA(CODE, NTT) \
+  gemv_mma_kernel<CODE, NTT><<<tiles, 32 * ks, smem, s>>>(tw, sv, xp, yp, N, K, M, per, C)
+  if (wq->code == NF4Q_CODE_NF4) {
+    if (NT == 1) NF4Q_GEMV_MMA(0, 1); else NF4Q_GEMV_MMA(0, 2);
+  } else {
+    if (NT == 1) NF4Q_GEMV_MMA(1, 1); else NF4Q_GEMV_MMA(1, 2);
+  }
+#undef NF4Q_GEMV_MMA
   return launch_status();
 }
 
