@@ -15,6 +15,12 @@ constexpr int kDqBlock = 256;   // absmax values per double-quant block
 // Sticky device error word (bit 0: a pipeline wait gave up).
 __device__ uint32_t g_device_error;
 
+// The 16 code values (float32, indexed by code); 8-byte aligned so that
+// consecutive pairs can be read as one 64-bit operand.
+struct __align__(8) CodeValues {
+  float v[16];
+};
+
 // Everything a dequantizer needs to rebuild one block's scale.
 struct ScaleView {
   const int8_t* absmax_q;

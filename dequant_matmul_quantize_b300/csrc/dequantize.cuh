@@ -15,10 +15,6 @@ namespace nf4q {
 
 constexpr int kDequantThreads = 256;
 
-struct CodeValues {
-  float v[16];
-};
-
 template <int U>
 __global__ void __launch_bounds__(kDequantThreads)
 dequantize_kernel(const uint32_t* __restrict__ packed, ScaleView sv,

@@ -9,13 +9,14 @@
 //     accumulates the fp64 sum, the largest value and the smallest non-zero
 //     value (as bit patterns; non-negative floats order like integers).  The
 //     last CTA to finish checks whether fp64 addition was exact for this
-//     tensor (all values are multiples of the smallest one's ulp, and the
+//     tensor (all values are multiples of the smallest one's ulp and the
 //     total stays below 2^53 such ulps), which makes the sum independent of
-//     the order of the additions.  If it was not (absmax values spread over
-//     more than ~29 binades), that CTA re-adds all values exactly as
-//     per-exponent integer mantissa sums.  Either way the exact sum becomes a
-//     320-bit integer (sum * 2^149), which is divided by n_b and rounded to
-//     float32 (nearest, ties to even) with integer arithmetic.
+//     the order of the additions; it then rounds the fp64 quotient to float32,
+//     with the exact remainder deciding the one case where that could round
+//     twice (a quotient exactly on a float32 midpoint).  Otherwise (absmax
+//     values spread over more than ~29 binades) that CTA re-adds all values
+//     exactly as per-exponent integer mantissa sums into a 320-bit integer
+//     (sum * 2^149), divides by n_b and rounds with integer arithmetic.
 //   pass 2 (dq_quant_kernel): one warp per 256-block.
 #pragma once
 
@@ -23,15 +24,13 @@
 
 namespace nf4q {
 
-constexpr int kDqSumThreads = 512;
-constexpr int kDqQuantThreads = 256;
 
 // Layout of the double-quant workspace (cleared before pass 1).
 struct DqWorkspace {
-  double sum;           // fp64 sum of all absmax values
-  uint32_t max_bits;    // largest value, as bits
+  double sum;             // fp64 sum of all absmax values
+  uint32_t max_bits;      // largest value, as bits
   uint32_t inv_min_bits;  // ~(smallest non-zero value, as bits)
-  uint32_t ticket;      // CTAs finished
+  uint32_t ticket;        // CTAs finished
   uint32_t pad[11];
 };
 static_assert(sizeof(DqWorkspace) == 64, "workspace layout");
@@ -90,6 +89,30 @@ __device__ float big_round_mean(const uint32_t (&A)[kLimbs], uint32_t n) {
   return __uint_as_float((static_cast<uint32_t>(be) << 23) | (mant & 0x7FFFFFu));
 }
 
+// Float32 nearest (ties to even) to S / n for an exact fp64 sum S.
+__device__ __forceinline__ float dq_mean_from_exact_sum(double gsum, uint32_t n) {
+  const double dn = static_cast<double>(n);
+  const double q = gsum / dn;
+  float f = static_cast<float>(q);
+  if (static_cast<double>(f) != q) {
+    const float up = __uint_as_float(__float_as_uint(f) + 1u);
+    const float dn_f = f > 0.f ? __uint_as_float(__float_as_uint(f) - 1u) : 0.f;
+    const float other = static_cast<double>(f) < q ? up : dn_f;
+    const double mid = (static_cast<double>(f) + static_cast<double>(other)) * 0.5;
+    if (mid == q) {  // quotient exactly on a midpoint: the remainder decides
+      const double rem = fma(-q, dn, gsum);
+      const float lo = fminf(f, other), hi = fmaxf(f, other);
+      if (rem > 0.0) f = hi;
+      else if (rem < 0.0) f = lo;
+      else f = (__float_as_uint(lo) & 1u) ? hi : lo;
+    }
+  }
+  return f;
+}
+
+constexpr int kDqSumThreads = 512;
+constexpr int kDqQuantThreads = 256;
+
 // ---------------------------------------------------------------- pass 1
 __global__ void __launch_bounds__(kDqSumThreads)
 dq_sum_kernel(const float* __restrict__ absmax, int64_t nb,
@@ -101,15 +124,20 @@ dq_sum_kernel(const float* __restrict__ absmax, int64_t nb,
 
   double sum = 0.0;
   uint32_t mx = 0, imn = 0;  // imn = ~min over non-zero values
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-       i < nb; i += stride) {
-    const float a = __ldg(absmax + i);
+  auto add = [&](float a) {
     const uint32_t bits = __float_as_uint(a) & 0x7FFFFFFFu;
     sum += static_cast<double>(__uint_as_float(bits));
     mx = max(mx, bits);
     if (bits) imn = max(imn, ~bits);
+  };
+  const int64_t nvec = nb / 4;  // absmax is 16-byte aligned
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += stride) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(absmax) + i);
+    add(v.x); add(v.y); add(v.z); add(v.w);
   }
+  if (blockIdx.x == 0 && threadIdx.x < (nb & 3)) add(__ldg(absmax + nvec * 4 + threadIdx.x));
   for (int o = 16; o > 0; o >>= 1) {
     sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
     mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
@@ -155,22 +183,15 @@ dq_sum_kernel(const float* __restrict__ absmax, int64_t nb,
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    uint32_t A[kLimbs];
-    for (int i = 0; i < kLimbs; ++i) A[i] = 0u;
     if (exact) {
-      // gsum = m * 2^(ex - 1075); A = gsum * 2^149 = m << (ex - 926)
-      const uint64_t db = static_cast<uint64_t>(__double_as_longlong(gsum));
-      int ex = static_cast<int>((db >> 52) & 0x7FF);
-      uint64_t m = db & ((1ull << 52) - 1);
-      if (ex) m |= 1ull << 52; else ex = 1;
-      const int sh = ex - 926;
-      if (sh >= 0) big_add_shifted(A, m, sh);
-      else big_add_shifted(A, m >> (-sh), 0);  // exact: sum is a multiple of 2^-149
+      *offset = nb == 0 ? 0.f : dq_mean_from_exact_sum(gsum, n);
     } else {
+      uint32_t A[kLimbs];
+      for (int i = 0; i < kLimbs; ++i) A[i] = 0u;
       for (int e = 1; e < 255; ++e)
         if (s_hist[e]) big_add_shifted(A, s_hist[e], e - 1);
+      *offset = big_round_mean(A, n);
     }
-    *offset = nb == 0 ? 0.f : big_round_mean(A, n);
   }
 }
 
@@ -187,12 +208,21 @@ dq_quant_kernel(const float* __restrict__ absmax, int64_t nb,
   const float off = __ldg(offset);
   for (int64_t d = warp0; d < nd; d += nwarps) {
     const int64_t i0 = d * kDqBlock + lane * 8;
+    float a[8];
+    if (i0 + 8 <= nb) {  // absmax is 16-byte aligned and i0 % 8 == 0
+      const float4 v0 = __ldg(reinterpret_cast<const float4*>(absmax + i0));
+      const float4 v1 = __ldg(reinterpret_cast<const float4*>(absmax + i0) + 1);
+      a[0] = v0.x; a[1] = v0.y; a[2] = v0.z; a[3] = v0.w;
+      a[4] = v1.x; a[5] = v1.y; a[6] = v1.z; a[7] = v1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = i0 + i < nb ? __ldg(absmax + i0 + i) : off;
+    }
     float c[8];
     float m = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int64_t idx = i0 + i;
-      c[i] = idx < nb ? __fsub_rn(__ldg(absmax + idx), off) : 0.f;
+      c[i] = __fsub_rn(a[i], off);  // 0 for the padding of a partial block
       m = fmaxf(m, fabsf(c[i]));
     }
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));

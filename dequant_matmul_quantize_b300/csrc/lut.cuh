@@ -26,13 +26,12 @@ __device__ __forceinline__ uint32_t lop_select(uint32_t if1, uint32_t if0, uint3
   return r;
 }
 
-// (a0 * s, a1 * s), each rounded to nearest: one packed f32x2 multiply.
-__device__ __forceinline__ void mul2_rn(float a0, float a1, float s, float& r0, float& r1) {
-  uint64_t a, b, d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(b) : "f"(s));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
+// (c0 * s, c1 * s) for a pair of code values, each product rounded to
+// nearest: one packed f32x2 multiply.
+__device__ __forceinline__ uint64_t mul2_rn(uint64_t c01, uint64_t ss) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(c01), "l"(ss));
+  return d;
 }
 
 // Byte tables of one (row, block): H[i] / L[i] hold the high / low bytes of
@@ -45,13 +44,17 @@ struct RowTable {
 
 template <int CODE>
 __device__ __forceinline__ void build_table(RowTable<CODE>& T, float s, const CodeValues& C) {
+  uint64_t ss;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
+  const uint64_t* cv = reinterpret_cast<const uint64_t*>(C.v);
 #pragma unroll
   for (int i = 0; i < (CODE == 0 ? 4 : 2); ++i) {
-    float f0, f1, f2, f3;
-    mul2_rn(C.v[4 * i + 0], C.v[4 * i + 1], s, f0, f1);
-    mul2_rn(C.v[4 * i + 2], C.v[4 * i + 3], s, f2, f3);
-    const uint32_t p0 = pack_bf16x2(f0, f1);
-    const uint32_t p1 = pack_bf16x2(f2, f3);
+    const uint64_t d0 = mul2_rn(cv[2 * i], ss), d1 = mul2_rn(cv[2 * i + 1], ss);
+    uint32_t p0, p1;  // bf16x2 of codes 4i, 4i+1 and 4i+2, 4i+3
+    asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.bf16x2.f32 %0, b, a;\n}"
+        : "=r"(p0) : "l"(d0));
+    asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.bf16x2.f32 %0, b, a;\n}"
+        : "=r"(p1) : "l"(d1));
     T.H[i] = prmt(p0, p1, 0x7531);
     T.L[i] = prmt(p0, p1, 0x6420);
   }

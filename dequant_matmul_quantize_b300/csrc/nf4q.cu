@@ -100,6 +100,39 @@ bool gemv_attr_ready() {
   return ok;
 }
 
+// Opt the quantize kernels in to their dynamic shared memory (once per device).
+bool quantize_attr_ready() {
+  static bool done[kMaxDevices] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (done[dev]) return true;
+  const int b0 = static_cast<int>(quantize_smem_bytes(0)), b1 = static_cast<int>(quantize_smem_bytes(1));
+  const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  bool ok = cudaFuncSetAttribute(quantize_kernel<0, true, 2>, A, b0) == cudaSuccess &&
+            cudaFuncSetAttribute(quantize_kernel<0, false, 2>, A, b0) == cudaSuccess &&
+            cudaFuncSetAttribute(quantize_kernel<1, true, 2>, A, b1) == cudaSuccess &&
+            cudaFuncSetAttribute(quantize_kernel<1, false, 2>, A, b1) == cudaSuccess;
+  done[dev] = ok;
+  return ok;
+}
+
+// Resident CTAs per SM of the quantize kernel (registers and shared memory),
+// so the grid-stride grid is exactly one full wave.
+int quantize_ctas_per_sm(int code) {
+  static int cache[kMaxDevices][2] = {{0}};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (cache[dev][code] == 0) {
+    int n = 0;
+    const size_t smem = quantize_smem_bytes(code);
+    cudaError_t e = code == 0
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<0, true, 2>, kQuantThreads, smem)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<1, true, 2>, kQuantThreads, smem);
+    cache[dev][code] = (e == cudaSuccess && n > 0) ? n : 1;
+  }
+  return cache[dev][code];
+}
+
 ScaleView scale_view(const nf4q_weight* wq) {
   ScaleView sv;
   sv.absmax_q = wq->absmax_q;
@@ -188,16 +221,18 @@ nf4q_status nf4q_quantize(const void* w, int32_t in_dtype, const nf4q_weight* wq
   if (!T.ok) return NF4Q_ERR_UNSUPPORTED;
   QuantParams P;
   const int c = wq->code;
-  for (int i = 0; i < kLutEntries; ++i) P.lut[i] = T.lut[c][i];
+  for (int i = 0; i < kLutEntries; ++i) {
+    P.lut_t[i] = T.lut_t[c][i];
+    P.lut_lo[i] = T.lut_lo[c][i];
+    P.lut_dl[i] = T.lut_dl[c][i];
+  }
   for (int i = 0; i < 15; ++i) P.thr[i] = i < T.nthr[c] ? T.thr[c][i] : 2.0f;
-  P.nthr = T.nthr[c];
-  P.lut_scale = T.lut_scale[c];
-  P.lut_bias = T.lut_bias[c] + kMagic;
+  if (!quantize_attr_ready()) return NF4Q_ERR_CUDA;
   const int64_t n_units = n / 8;
   constexpr int U = 2;
   const int64_t grid = grid_for(n_units, 32 * U * (kQuantThreads / 32),
-                                static_cast<int64_t>(sm_count()) * 2);
-  const size_t smem = kLutEntries * 32 * sizeof(uint32_t);
+                                static_cast<int64_t>(sm_count()) * quantize_ctas_per_sm(c));
+  const size_t smem = quantize_smem_bytes(c);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t* packed = reinterpret_cast<uint32_t*>(wq->packed);
   if (c == NF4Q_CODE_NF4) {
@@ -213,6 +248,28 @@ nf4q_status nf4q_quantize(const void* w, int32_t in_dtype, const nf4q_weight* wq
   }
   return launch_status();
 }
+
+}  // extern "C"
+
+namespace nf4q {
+namespace {
+// Both passes of the double quantization, on a cleared workspace record.
+nf4q_status dq_launch(const nf4q_weight* wq, int64_t nb, void* ws, cudaStream_t s) {
+  if (cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
+  const int64_t g1 = grid_for(nb / 4, kDqSumThreads, static_cast<int64_t>(sm_count()));
+  dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb, static_cast<DqWorkspace*>(ws),
+                                             wq->offset);
+  if (cudaGetLastError() != cudaSuccess) return NF4Q_ERR_CUDA;
+  const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
+  const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
+  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset, wq->absmax_q,
+                                                  wq->scale2);
+  return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
+}
+}  // namespace
+}  // namespace nf4q
+
+extern "C" {
 
 size_t nf4q_double_quant_workspace_bytes(int64_t n_b) {
   (void)n_b;
@@ -235,16 +292,7 @@ nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
   if (!aligned16(wq->absmax) || !aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;
   if (!workspace || workspace_bytes < sizeof(DqWorkspace)) return NF4Q_ERR_WORKSPACE;
   if (!aligned16(workspace)) return NF4Q_ERR_ALIGNMENT;
-  if (cudaMemsetAsync(workspace, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
-  const int64_t g1 = grid_for(nb, kDqSumThreads, static_cast<int64_t>(sm_count()) * 2);
-  dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb,
-                                             static_cast<DqWorkspace*>(workspace), wq->offset);
-  if ((st = launch_status()) != NF4Q_OK) return st;
-  const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
-  const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
-  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset,
-                                                  wq->absmax_q, wq->scale2);
-  return launch_status();
+  return dq_launch(wq, nb, workspace, s);
 }
 
 nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
@@ -283,11 +331,11 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
   if (wq->rows > (1ll << 30) || wq->cols > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
   const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
-  // 16 rows per CTA; its warps split K so the grid holds ~24 warps per SM
+  // 32 rows per CTA; its warps split K so the grid holds ~16 warps per SM
   const int NT = M > 8 ? 2 : 1;
   const int nchunks = (K + kGemvChunk - 1) / kGemvChunk;
-  const int tiles = (N + kGemvRows - 1) / kGemvRows;
-  const int target = sm_count() * 24;
+  const int tiles = (N + kGemvRows * kGemvR - 1) / (kGemvRows * kGemvR);
+  const int target = sm_count() * 16;
   int ks = std::max(1, std::min(std::min(16, nchunks), (target + tiles - 1) / tiles));
   const int per = (nchunks + ks - 1) / ks;
   ks = (nchunks + per - 1) / per;
@@ -298,7 +346,7 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[2] = {kGemvChunk / 2, kGemvRows};
+    cuuint32_t box[2] = {kGemvChunk / 2, kGemvRows * kGemvR};
     cuuint32_t es[2] = {1, 1};
     if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -406,16 +454,7 @@ nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream) {
   if (!aligned16(wq->absmax) || !aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;
   void* ws = noalloc_scratch(&st);
   if (st != NF4Q_OK) return st;
-  if (cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
-  const int64_t g1 = grid_for(nb, kDqSumThreads, static_cast<int64_t>(sm_count()) * 2);
-  dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb, static_cast<DqWorkspace*>(ws),
-                                             wq->offset);
-  if ((st = launch_status()) != NF4Q_OK) return st;
-  const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
-  const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
-  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset,
-                                                  wq->absmax_q, wq->scale2);
-  return launch_status();
+  return dq_launch(wq, nb, ws, s);
 }
 
 }  // extern "C"

@@ -8,18 +8,23 @@
 // absmax is a 3-step butterfly.  Each warp pass covers U*256 elements.
 //
 // Code search.  The exact rule is on wn = fp32(w / absmax) (IEEE division):
-// code = #{ j : wn > T_j } over the round-down midpoints T_j.  The kernel
-// does not divide per element.  It forms q = fp32(w * fp32(1 / absmax)),
-// which is within 2^-22 of wn, and looks q up in a 259-bin table (bin =
-// nearest integer of q*128 + 129 for NF4, |q|*256 + 1 for FP4): every bin
-// is narrower than the gap between decision points, so at most one T is in
-// reach and code = base(bin) + (q > T).  When q lies within 2^-19 of that T
-// the two could disagree, so the unit is recomputed with the exact division
-// and a plain count over all T_j; so are blocks whose absmax is below 2^-126
-// (where 1/absmax would overflow) or zero.  The result is therefore exactly
-// the rule, the fast path only saves work.  The bin table is replicated once
-// per lane in shared memory (entry e of lane l at word e*32 + l), so the
-// data-dependent lookups of a warp never collide on a bank.
+// code = #{ j : wn > T_j } over the round-down midpoints T_j (FP4: on |wn|,
+// plus the sign).  The kernel does not divide per element.  It forms
+// q = fp32(w * r) with r an approximate reciprocal of absmax (relative error
+// at most 2^-22), which is within 2^-21 of wn, and looks q up
+// in 259-bin tables (bin = nearest integer of q*128 + 129): every bin is
+// narrower than the gap between decision points (FP4's are mirrored onto the
+// signed value), so at most one point T is in reach and
+// code = lo(bin) + (q > T) * dl(bin).  When q lies within 2^-19 of that T the
+// two could disagree, so the unit is recomputed with the exact division and
+// a plain count over all T_j; so are blocks whose absmax is zero, below
+// 2^-126 or above 2^126 (1/absmax not a normal number) or not finite.  The result is therefore
+// exactly the rule; the fast path only saves work.  The tables are
+// replicated once per lane in shared memory (entry e of lane l at word
+// e*32 + l), so the data-dependent lookups of a warp never collide on a
+// bank, and the per-element work is spread over the FMA pipe (bin, address,
+// packing), the load pipe (table reads) and the integer pipe (compare bit,
+// near test).
 #pragma once
 
 #include "common.cuh"
@@ -31,34 +36,48 @@ constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23
 constexpr uint32_t kMagicBits = 0x4B400000u;
 constexpr float kNearEps = 1.9073486328125e-06f;  // 2^-19
 constexpr float kTinyScale = 1.17549435e-38f;     // 2^-126
+constexpr float kHugeScale = 8.50705917e37f;      // 2^126
+constexpr int kLutWords = kLutEntries * 32;       // one table, replicated per lane
 
 struct QuantParams {
-  float lut[kLutEntries];
-  float thr[15];
-  int nthr;
-  float lut_scale;
-  float lut_bias;  // already includes kMagic
+  float lut_t[kLutEntries];     // decision point within reach of each bin
+  int32_t lut_lo[kLutEntries];  // code below it
+  int32_t lut_dl[kLutEntries];  // change of code across it (FP4 only)
+  float thr[15];                // exact-path decision points
 };
 
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int lds_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Fast code of one element: bin lookup (2 or 3 shared loads) and a compare.
+// `lane_tab` is this lane's column of the tables minus the magic offset of
+// the bin computation, so that the address is one multiply-add.  The code is
+// added into `word` at nibble shift `sh` with multiply-adds.
 template <int CODE>
-__device__ __forceinline__ uint32_t code_fast(float q, const uint32_t* lut,
-                                              float scale, float bias,
-                                              bool& near) {
-  const float v = CODE == 0 ? q : fabsf(q);
-  const float y = __fmaf_rn(v, scale, bias);
-  uint32_t b = __float_as_uint(y) - kMagicBits;
-  b = min(b, static_cast<uint32_t>(kLutEntries - 1));  // non-finite inputs
-  const uint32_t e = lut[b * 32];
-  const float d = __fsub_rn(__uint_as_float(e & ~0xFu), v);
+__device__ __forceinline__ void code_fast(float q, uint32_t lane_tab, bool& near, uint32_t& word,
+                                          int sh) {
+  const float y = __fmaf_rn(q, 128.0f, 129.0f + kMagic);
+  const uint32_t a = __float_as_uint(y) * 128u + lane_tab;
+  const float t = lds_f32(a);
+  const int lo = lds_s32(a + kLutWords * 4);
+  const float d = __fsub_rn(t, q);
   near |= fabsf(d) <= kNearEps;
-  uint32_t c = (e & 0xFu) + (__float_as_uint(d) >> 31);
-  if (CODE == 1) c |= (q < 0.f && c != 0u) ? 8u : 0u;
-  return c;
+  const int bit = static_cast<int>(__float_as_uint(d) >> 31);  // q > t
+  const int dl = CODE == 0 ? 1 : lds_s32(a + 2 * kLutWords * 4);
+  const int c = bit * dl + lo;
+  word += static_cast<uint32_t>(c) * (1u << sh);
 }
 
 template <int CODE>
-__device__ __forceinline__ uint32_t code_exact(float w, float a,
-                                               const QuantParams& P) {
+__device__ __forceinline__ uint32_t code_exact(float w, float a, const QuantParams& P) {
   const float q = a == 0.f ? 0.f : __fdiv_rn(w, a);
   const float v = CODE == 0 ? q : fabsf(q);
   uint32_t c = 0;
@@ -106,19 +125,29 @@ __device__ __forceinline__ void load_unit(const void* base, int64_t unit,
   }
 }
 
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;  // NaN if either is NaN, so a non-finite block is always seen
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 template <int CODE, bool BF16IN, int U>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_kernel(const void* __restrict__ w, uint32_t* __restrict__ packed,
                 float* __restrict__ absmax, int64_t n_units,
                 const __grid_constant__ QuantParams P) {
-  extern __shared__ uint32_t s_lut[];  // kLutEntries * 32 words
-  for (int i = threadIdx.x; i < kLutEntries * 32; i += blockDim.x)
-    s_lut[i] = __float_as_uint(P.lut[i >> 5]);
+  extern __shared__ uint32_t s_lut[];  // [tables][kLutEntries][32]
+  for (int i = threadIdx.x; i < kLutWords; i += blockDim.x) {
+    const int e = i >> 5;
+    s_lut[i] = __float_as_uint(P.lut_t[e]);
+    s_lut[kLutWords + i] = static_cast<uint32_t>(P.lut_lo[e]);
+    if (CODE == 1) s_lut[2 * kLutWords + i] = static_cast<uint32_t>(P.lut_dl[e]);
+  }
   __syncthreads();
 
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t* lut = s_lut + lane;
-  const float scale = P.lut_scale, bias = P.lut_bias;
+  const uint32_t lane_tab = static_cast<uint32_t>(__cvta_generic_to_shared(s_lut)) + lane * 4u -
+                            kMagicBits * 128u;
   const int64_t gwarp =
       (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -141,26 +170,33 @@ quantize_kernel(const void* __restrict__ w, uint32_t* __restrict__ packed,
     for (int u = 0; u < U; ++u) {
       float m = fabsf(v[u][0]);
 #pragma unroll
-      for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(v[u][i]));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+      for (int i = 1; i < 8; ++i) m = max_nan(m, fabsf(v[u][i]));
+      m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
       amax[u] = m;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t unit = base + u * 32 + lane;
       const float a = amax[u];
-      const bool tiny = !(a >= kTinyScale);
-      const float r = tiny ? 0.f : __frcp_rn(a);
+      // 2^-126 <= a <= 2^126: the reciprocal is a normal number (the
+      // approximate one flushes subnormal results), |w * rcp(a)| <= 1 + 2^-21
+      // and every bin index is inside the table; anything else (zero, tiny,
+      // huge or non-finite absmax) takes the exact path
+      const bool ok = a >= kTinyScale && a <= kHugeScale;
       bool near = false;
       uint32_t word = 0;
+      if (ok) {
+        // Approximate reciprocal (relative error <= 2^-22): q stays within
+        // 2^-21 of the exact quotient, inside the 2^-19 exact-fallback window.
+        float r;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float q = __fmul_rn(v[u][i], r);
-        word |= code_fast<CODE>(q, lut, scale, bias, near) << nib_shift(i);
+        for (int i = 0; i < 8; ++i)
+          code_fast<CODE>(__fmul_rn(v[u][i], r), lane_tab, near, word, nib_shift(i));
       }
-      if (near || tiny)
+      if (near || !ok)
         word = encode_unit_exact<CODE>(v[u][0], v[u][1], v[u][2], v[u][3],
                                        v[u][4], v[u][5], v[u][6], v[u][7], a, P);
       if (unit < n_units) {
@@ -169,6 +205,10 @@ quantize_kernel(const void* __restrict__ w, uint32_t* __restrict__ packed,
       }
     }
   }
+}
+
+inline size_t quantize_smem_bytes(int code) {
+  return static_cast<size_t>(code == 0 ? 2 : 3) * kLutWords * 4;
 }
 
 }  // namespace nf4q

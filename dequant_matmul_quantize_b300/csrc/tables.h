@@ -14,7 +14,8 @@
 // Encoder decision points: for neighbouring levels c_j < c_{j+1} the exact
 // midpoint (c_j + c_{j+1}) / 2 (exact in double) is rounded DOWN to float32.
 // For a float32 value v, "v > T_j" then holds exactly when v is nearer to
-// c_{j+1} than to c_j, and an exact tie stays with c_j.
+// c_{j+1} than to c_j, and an exact tie stays with c_j.  (FP4 applies its 7
+// points to |v|.)
 #pragma once
 
 #include <cmath>
@@ -30,11 +31,13 @@ struct HostTables {
   float values[2][16];   // [code kind][code]
   float thr[2][15];      // decision points (NF4: 15 on wn; FP4: 7 on |wn|)
   int nthr[2];
-  // Bin table of the fast encoder: entry b holds the only decision point
-  // within reach of bin b (or 2.0f when there is none), with the number of
-  // decision points below the bin stored in its low 4 bits.
-  float lut[2][kLutEntries];
-  float lut_scale[2], lut_bias[2];
+  // Bin tables of the fast encoder, over the signed normalized value for
+  // both codes: entry b holds the only decision point within reach of bin b
+  // (2.0f when there is none), the code just below it and the change of code
+  // across it.
+  float lut_t[2][kLutEntries];
+  int32_t lut_lo[2][kLutEntries];
+  int32_t lut_dl[2][kLutEntries];
   bool ok;
 };
 
@@ -70,26 +73,54 @@ inline void sort16(double* v) {
 
 }  // namespace detail
 
-// Fill one bin table.  Bin b receives every value v with
-// rn_int(v * scale + bias) == b, i.e. v in [(b - .5 - bias)/scale,
-// (b + .5 - bias)/scale]; a margin of a quarter bin absorbs rounding.
-inline bool build_lut(const float* thr, int n, float scale, float bias,
-                      float* lut) {
-  const double m = 0.25 / scale;
+// Exact code of a float32 value under the decision points (host copy of the
+// rule the kernels implement; used to label the bins).
+inline int code_of(const HostTables& T, int code, double v) {
+  if (code == 0) {
+    int c = 0;
+    for (int j = 0; j < 15; ++j) c += v > T.thr[0][j] ? 1 : 0;
+    return c;
+  }
+  const double a = v < 0 ? -v : v;
+  int m = 0;
+  for (int j = 0; j < 7; ++j) m += a > T.thr[1][j] ? 1 : 0;
+  return m | ((v < 0 && m) ? 8 : 0);
+}
+
+// Fill the bin tables of one code.  Bin b receives every value v with
+// rn_int(v * 128 + 129) == b, i.e. v in [(b - 129.5)/128, (b - 128.5)/128];
+// a margin of a quarter bin on both sides absorbs rounding.  The decision
+// points on the signed value are +-T_j (FP4) or T_j (NF4); all are more than
+// two bins apart, so a bin holds at most one.
+inline bool build_lut(HostTables& T, int code) {
+  double pts[15];
+  int np = 0;
+  if (code == 0) {
+    for (int j = 0; j < 15; ++j) pts[np++] = T.thr[0][j];
+  } else {
+    for (int j = 6; j >= 0; --j) pts[np++] = -static_cast<double>(T.thr[1][j]);
+    for (int j = 0; j < 7; ++j) pts[np++] = T.thr[1][j];
+  }
+  const double m = 0.25 / 128.0;
   for (int b = 0; b < kLutEntries; ++b) {
-    double lo = (b - 0.5 - bias) / scale - m;
-    double hi = (b + 0.5 - bias) / scale + m;
-    int base = 0, inside = -1, count_inside = 0;
-    for (int j = 0; j < n; ++j) {
-      if (thr[j] < lo) ++base;
-      else if (thr[j] <= hi) { inside = j; ++count_inside; }
+    const double lo = (b - 129.5) / 128.0 - m, hi = (b - 128.5) / 128.0 + m;
+    int inside = -1, count = 0;
+    for (int j = 0; j < np; ++j)
+      if (pts[j] >= lo && pts[j] <= hi) { inside = j; ++count; }
+    if (count > 1) return false;
+    if (inside < 0) {
+      T.lut_t[code][b] = 2.0f;
+      T.lut_lo[code][b] = code_of(T, code, 0.5 * (lo + hi));
+      T.lut_dl[code][b] = 0;
+    } else {
+      const double p = pts[inside];
+      const float pf = static_cast<float>(p);
+      T.lut_t[code][b] = pf;
+      const int below = code_of(T, code, std::nextafter(p, -1e9));
+      const int above = code_of(T, code, std::nextafter(p, 1e9));
+      T.lut_lo[code][b] = below;
+      T.lut_dl[code][b] = above - below;
     }
-    if (count_inside > 1 || base > 15) return false;
-    float t = inside >= 0 ? thr[inside] : 2.0f;
-    uint32_t bits;
-    std::memcpy(&bits, &t, 4);
-    bits = (bits & ~0xFu) | static_cast<uint32_t>(base);
-    std::memcpy(&lut[b], &bits, 4);
   }
   return true;
 }
@@ -125,11 +156,8 @@ inline HostTables build_host_tables() {
     T.thr[1][j] = detail::round_down_f32(
         (static_cast<double>(T.values[1][j]) + T.values[1][j + 1]) * 0.5);
   T.nthr[1] = 7;
-  // ---- bin tables: NF4 over wn in [-1, 1], FP4 over |wn| in [0, 1]
-  T.lut_scale[0] = 128.0f; T.lut_bias[0] = 129.0f;
-  T.lut_scale[1] = 256.0f; T.lut_bias[1] = 1.0f;
-  T.ok = build_lut(T.thr[0], 15, 128.0f, 129.0f, T.lut[0]) &&
-         build_lut(T.thr[1], 7, 256.0f, 1.0f, T.lut[1]);
+  // ---- bin tables over the signed normalized value
+  T.ok = build_lut(T, 0) && build_lut(T, 1);
   return T;
 }
 
