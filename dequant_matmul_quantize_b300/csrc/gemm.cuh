@@ -12,12 +12,14 @@
 //   warp 1      allocates 512 TMEM columns; one lane issues the 2 x 4
 //               128xBNx16 MMAs of a stage and commits them to the stage's
 //               "empty" barrier, after the last stage to "acc_full".
-//   warps 2..9  dequantize: thread r rebuilds row r of the W tile with the
-//               register byte tables of lut.cuh (bit-exact w_hat) into the
-//               K-major 128-byte-swizzled layout the MMA reads, then
+//   warps 2..17 dequantize, as two groups of 8 warps taking alternate
+//               k-steps (one group alone cannot keep the ALUs busy): thread
+//               r of a group rebuilds row r of the W tile with the register
+//               byte tables of lut.cuh (bit-exact w_hat) into the K-major
+//               128-byte-swizzled layout the MMA reads, then
 //               fence.proxy.async and arrive on the stage's "b_full".
-//               Afterwards warps 2-5 drain accumulator 0 and warps 6-9
-//               accumulator 1 (tcgen05.ld), round to bf16 and store Y.
+//               Afterwards the 16 warps drain the two accumulators
+//               (tcgen05.ld), round to bf16 and store Y.
 // BN (128..256) is picked per shape so the tile count fills whole waves of
 // the SMs.  Every wait is bounded (1 s of %globaltimer); a wait that gives up
 // sets bit 0 of the device error word and the CTA winds down: its other
@@ -33,7 +35,7 @@ namespace nf4q {
 
 constexpr int kGemmBM = 128;   // rows per accumulator (two per CTA)
 constexpr int kGemmBK = 64;
-constexpr int kGemmThreads = 320;
+constexpr int kGemmThreads = 576;  // TMA warp, MMA warp, 2 x 8 dequant warps
 constexpr int kGemmATile = kGemmBM * kGemmBK * 2;    // 16 KB
 constexpr int kGemmTmemCols = 512;
 
@@ -203,8 +205,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       mma_commit(acc_bar);  // fires once every MMA issued above has completed
     }
   } else {
-    // ---------------- dequantize producers (one W row per thread)
-    const int r = threadIdx.x - 64;
+    // ---------------- dequantize producers: two groups of 8 warps take
+    // alternate k-steps; thread r of a group rebuilds W row r
+    const int idx = threadIdx.x - 64;
+    const int grp = idx >> 8;
+    const int r = idx & 255;
     const bool active = r < BN;
     const int n = n0 + r;
     const bool row_ok = active && n < N;
@@ -221,11 +226,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       if (vec_q) {
         g.q = __ldg(reinterpret_cast<const uint4*>(sv.absmax_q + b0));
       } else {
-        uint32_t w[4] = {0, 0, 0, 0};
-        for (int j = 0; j < 16 && kt0 + j < KT; ++j)
-          w[j >> 2] |= (static_cast<uint32_t>(static_cast<uint8_t>(__ldg(sv.absmax_q + b0 + j))))
-                       << (8 * (j & 3));
-        g.q = make_uint4(w[0], w[1], w[2], w[3]);
+        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t v = kt0 + j < KT
+              ? static_cast<uint32_t>(static_cast<uint8_t>(__ldg(sv.absmax_q + b0 + j))) : 0u;
+          const uint32_t sh = v << (8 * (j & 3));
+          if (j < 4) w0 |= sh; else if (j < 8) w1 |= sh; else if (j < 12) w2 |= sh; else w3 |= sh;
+        }
+        g.q = make_uint4(w0, w1, w2, w3);
       }
       g.s2a = __ldg(sv.scale2 + (b0 >> 8));
       const int64_t nextd = ((b0 >> 8) + 1) << 8;   // first block of the next 256
@@ -236,12 +245,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
     ScaleGroup gcur, gnext;
     load_group(gcur, 0);
     load_group(gnext, 16);
-    for (int kt = 0; kt < KT; ++kt) {
+    for (int kt = grp; kt < KT; kt += 2) {
       const int sa = kt % SA, sb = kt % SB;
       const int j = kt & 15;
-      if (j == 0 && kt > 0) {
+      if (kt >= 16 && j == grp) {  // first k-step of this thread in a new group of 16
         gcur = gnext;
-        load_group(gnext, kt + 16);
+        load_group(gnext, kt - j + 16);
       }
       float sc;
       if (sv.double_quant) {
@@ -275,16 +284,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       __syncwarp();
       if (lane == 0) mbar_arrive(bfull_bar(sb));
     }
-    // ---------------- epilogue: TMEM -> bf16 -> Y
+    // ---------------- epilogue: TMEM -> bf16 -> Y (16 warps: accumulator,
+    // TMEM lane quarter, and every other 32-column chunk)
     if (__all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
       tc_fence_after();
-      const int q = warp & 3;          // TMEM lane quarter this warp may read
-      const int h = (warp - 2) >> 2;   // accumulator (M half)
+      const int q = warp & 3;                 // TMEM lane quarter this warp may read
+      const int h = ((warp - 2) >> 2) & 1;    // accumulator (M half)
+      const int c0 = ((warp - 2) >> 3) * 32;  // first column chunk
       const int m = m0 + h * kGemmBM + q * 32 + lane;
       uint16_t* yrow = Y + static_cast<int64_t>(m) * N + n0;
       const bool vec = (N & 7) == 0;
 #pragma unroll 1
-      for (int col = 0; col < BN; col += 32) {
+      for (int col = c0; col < BN; col += 64) {
         uint32_t v[32];
         tmem_ld32(tmem + h * 256 + (static_cast<uint32_t>(q * 32) << 16) + col, v);
         if (m < M) {
