@@ -35,7 +35,6 @@ namespace nf4q {
 
 constexpr int kGemmBM = 128;   // rows per accumulator (two per CTA)
 constexpr int kGemmBK = 64;
-constexpr int kGemmThreads = 576;  // TMA warp, MMA warp, 2 x 8 dequant warps
 constexpr int kGemmATile = kGemmBM * kGemmBK * 2;    // 16 KB
 constexpr int kGemmTmemCols = 512;
 
@@ -48,6 +47,11 @@ struct GemmCfg {
   static constexpr int kBStages =                     // dequantized W stages
       (kAStages * kAStage + 3 * kBTile + 2048 <= 232448 - 1024) ? 3 : 2;
   static constexpr size_t kSmem = 1024 + kAStages * kAStage + kBStages * kBTile + 1024;
+  // One group of 8 dequant warps per B stage: group g produces the k-steps
+  // kt % kBStages == g, always into stage g, so no producer can run more than
+  // one mbarrier phase ahead of the MMA on its stage.
+  static constexpr int kGroups = kBStages;
+  static constexpr int kThreads = 64 + kGroups * 256;   // + TMA warp and MMA warp
   static_assert(kPTile % 1024 == 0 && kBTile % 1024 == 0, "1 KB alignment of tiles");
   static_assert(kSmem <= 232448, "shared memory");
 };
@@ -110,7 +114,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // ------------------------------------------------------------ the kernel
 template <int CODE, int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
             const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
             uint16_t* __restrict__ Y, int M, int N, int K,
@@ -245,10 +249,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
     ScaleGroup gcur, gnext;
     load_group(gcur, 0);
     load_group(gnext, 16);
-    for (int kt = grp; kt < KT; kt += 2) {
+    for (int kt = grp; kt < KT; kt += Cfg::kGroups) {
       const int sa = kt % SA, sb = kt % SB;
       const int j = kt & 15;
-      if (kt >= 16 && j == grp) {  // first k-step of this thread in a new group of 16
+      if (kt >= 16 && j < Cfg::kGroups) {  // first k-step of this thread in a new group of 16
         gcur = gnext;
         load_group(gnext, kt - j + 16);
       }
@@ -286,7 +290,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
     // ---------------- epilogue: TMEM -> bf16 -> Y (16 warps: accumulator,
     // TMEM lane quarter, and every other 32-column chunk)
-    if (__all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
+    if (warp < 18 && __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
       tc_fence_after();
       const int q = warp & 3;                 // TMEM lane quarter this warp may read
       const int h = ((warp - 2) >> 2) & 1;    // accumulator (M half)
@@ -377,7 +381,7 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
   }
   dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
             static_cast<unsigned>((M + 2 * kGemmBM - 1) / (2 * kGemmBM)));
-  gemm_kernel<CODE, BN><<<grid, kGemmThreads, Cfg::kSmem, stream>>>(
+  gemm_kernel<CODE, BN><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(
       tx, tw, sv, static_cast<uint16_t*>(Y), static_cast<int>(M), static_cast<int>(N),
       static_cast<int>(K), C);
   return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
