@@ -86,9 +86,11 @@ template <int CODE>
 __device__ __forceinline__ void dequant_word(const RowTable<CODE>& T, uint32_t w,
                                              uint32_t (&r)[4]) {
   const uint32_t s7 = w & 0x77777777u;
-  const uint32_t w4 = w << 4;
+  // the two shifts as multiplies, which run on the FMA pipe
+  const uint32_t w4 = w * 16u;
+  const uint32_t s7h = __umulhi(s7, 0x10000u);  // s7 >> 16
   lookup4<CODE>(T, s7, prmt(w, w4, 0x9D8C), r[0], r[1]);
-  lookup4<CODE>(T, s7 >> 16, prmt(w, w4, 0xBFAE), r[2], r[3]);
+  lookup4<CODE>(T, s7h, prmt(w, w4, 0xBFAE), r[2], r[3]);
 }
 
 }  // namespace nf4q

@@ -12,7 +12,6 @@
 #include "dequantize.cuh"
 #include "double_quant.cuh"
 #include "gemm.cuh"
-#include "gemv.cuh"
 #include "gemv_mma.cuh"
 #include "quantize.cuh"
 
@@ -84,20 +83,31 @@ nf4q_status check_scales(const nf4q_weight* wq) {
   return NF4Q_OK;
 }
 
-// Opt the GEMV kernels in to more than 48 KB of dynamic shared memory
-// (once per device).
+// The GEMV instantiations: code (NF4, FP4) x (NT, R) in {(1, 1), (2, 2)}.
+using GemvKernelFn = void (*)(CUtensorMap, ScaleView, const uint16_t*, uint16_t*, int, int, int,
+                              int, int, CodeValues);
+GemvKernelFn gemv_kernel(int code, int NT) {
+  if (code == 0) return NT == 1 ? gemv_mma_kernel<0, 1, 1> : gemv_mma_kernel<0, 2, 2>;
+  return NT == 1 ? gemv_mma_kernel<1, 1, 1> : gemv_mma_kernel<1, 2, 2>;
+}
+
+// Opt the GEMV kernels in to their largest dynamic shared memory (once per
+// device).
 bool gemv_attr_ready() {
   static bool done[kMaxDevices] = {false};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return true;
-  const int bytes = static_cast<int>(gemv_smem_bytes(16, 2));
-  bool ok = cudaFuncSetAttribute(gemv_mma_kernel<0, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-            cudaFuncSetAttribute(gemv_mma_kernel<0, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-            cudaFuncSetAttribute(gemv_mma_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-            cudaFuncSetAttribute(gemv_mma_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
-  done[dev] = ok;
-  return ok;
+  const int bytes = static_cast<int>(gemv_smem_bytes(2, 2, kGemvMaxStages, kGemvMaxSplit));
+  for (int code = 0; code < 2; ++code)
+    for (int nt = 1; nt <= 2; ++nt)
+      if (cudaFuncSetAttribute(gemv_kernel(code, nt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bytes) != cudaSuccess)
+        return false;
+  done[dev] = true;
+  return true;
 }
 
 // Opt the quantize kernels in to their dynamic shared memory (once per device).
@@ -331,41 +341,58 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
   if (wq->rows > (1ll << 30) || wq->cols > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
   const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
-  // 32 rows per CTA; its warps split K so the grid holds ~16 warps per SM
-  const int NT = M > 8 ? 2 : 1;
-  const int nchunks = (K + kGemvChunk - 1) / kGemvChunk;
-  const int tiles = (N + kGemvRows * kGemvR - 1) / (kGemvRows * kGemvR);
-  const int target = sm_count() * 16;
-  int ks = std::max(1, std::min(std::min(16, nchunks), (target + tiles - 1) / tiles));
-  const int per = (nchunks + ks - 1) / ks;
-  ks = (nchunks + per - 1) / per;
-  const size_t smem = gemv_smem_bytes(ks, NT);
+  if (!gemv_attr_ready()) return NF4Q_ERR_CUDA;
+  // M <= 8: one 8-column MMA tile and 16 rows per CTA; M > 8: two column
+  // tiles and 32 rows, so each x fragment serves twice as many weights.
+  const int NT = M > 8 ? 2 : 1, R = NT;
+  const int code = wq->code == NF4Q_CODE_NF4 ? 0 : 1;
+  const int64_t tiles = (N + kGemvRows * R - 1) / (kGemvRows * R);
+  const int nseg = (K + kGemvSeg - 1) / kGemvSeg;
+  const int nchunks = (nseg + kGemvWarps - 1) / kGemvWarps;
+  // K split over a cluster: the smallest that gives every SM at least four
+  // CTAs (16 warps); the ring has two stages, which leaves room for eight
+  // CTAs per SM (measured best on 4096^2 .. 28672x8192 weights).
+  int split = 1;
+  while (split < std::min(kGemvMaxSplit, nchunks) &&
+         tiles * split < static_cast<int64_t>(kGemvMinCtasPerSm) * sm_count())
+    split *= 2;
+  const int per = (nchunks + split - 1) / split;
+  split = (nchunks + per - 1) / per;  // CTAs that get chunks
+  const int stages = std::min(kGemvStages, per);
+  const size_t smem = gemv_smem_bytes(R, NT, stages, split);
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return NF4Q_ERR_CUDA;
   CUtensorMap tw;
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[2] = {kGemvChunk / 2, kGemvRows * kGemvR};
+    cuuint32_t box[2] = {kGemvSeg / 2, static_cast<cuuint32_t>(kGemvRows * R)};
     cuuint32_t es[2] = {1, 1};
     if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return NF4Q_ERR_CUDA;
   }
-  if (!gemv_attr_ready()) return NF4Q_ERR_CUDA;
+  if (tiles * split > 0x7FFFFFFF) return NF4Q_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * split));
+  cfg.blockDim = dim3(kGemvWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = split > 1 ? 1 : 0;
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   uint16_t* yp = static_cast<uint16_t*>(y);
   const ScaleView sv = scale_view(wq);
   const CodeValues C = code_values(wq->code);
-#define NF4Q_GEMV_MMA(CODE, NTT) \
-  gemv_mma_kernel<CODE, NTT><<<tiles, 32 * ks, smem, s>>>(tw, sv, xp, yp, N, K, M, per, C)
-  if (wq->code == NF4Q_CODE_NF4) {
-    if (NT == 1) NF4Q_GEMV_MMA(0, 1); else NF4Q_GEMV_MMA(0, 2);
-  } else {
-    if (NT == 1) NF4Q_GEMV_MMA(1, 1); else NF4Q_GEMV_MMA(1, 2);
-  }
-#undef NF4Q_GEMV_MMA
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel(code, NT), tw, sv, xp, yp, N, K, static_cast<int>(M),
+                         per, stages, C) != cudaSuccess)
+    return NF4Q_ERR_CUDA;
   return launch_status();
 }
 
