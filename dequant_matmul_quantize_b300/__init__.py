@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
         "nf4q_quantize": (i32, [vp, i32, W, vp]),
         "nf4q_double_quant_workspace_bytes": (sz, [i64]),
         "nf4q_double_quant": (i32, [W, vp, sz, vp]),
+        "nf4q_quantize_dq": (i32, [vp, i32, W, vp, sz, vp]),
         "nf4q_dequantize": (i32, [W, vp, vp]),
         "nf4q_gemv": (i32, [W, vp, i32, vp, vp]),
         "nf4q_gemm": (i32, [W, vp, i64, vp, vp]),
@@ -195,14 +196,27 @@ def double_quant_into(qw: QuantizedWeight, workspace: Optional[torch.Tensor] = N
         ctypes.byref(s), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
+def quantize_dq_into(qw: QuantizedWeight, w: torch.Tensor,
+                     workspace: Optional[torch.Tensor] = None, stream=None):
+    """nf4q_quantize_dq: quantize and double-quantize w into qw in one call."""
+    assert w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols)
+    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16}[w.dtype]
+    if workspace is None:
+        workspace = dq_workspace(qw.absmax.numel(), qw.absmax.device)
+    s = qw.struct()
+    _check("nf4q_quantize_dq", lib().nf4q_quantize_dq(
+        _ptr(w), dt, ctypes.byref(s), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
 def quantize(w: torch.Tensor, code: str = "nf4", double_quant: bool = True,
              workspace: Optional[torch.Tensor] = None, stream=None) -> QuantizedWeight:
     """Quantize a [rows x cols] fp32/bf16 CUDA weight (cols % 64 == 0)."""
     rows, cols = w.shape
     qw = QuantizedWeight.empty(rows, cols, code, double_quant, w.device)
-    quantize_into(qw, w, stream)
     if double_quant:
-        double_quant_into(qw, workspace, stream)
+        quantize_dq_into(qw, w, workspace, stream)
+    else:
+        quantize_into(qw, w, stream)
     return qw
 
 

@@ -2,65 +2,77 @@
 // bf16 ("bitsandbytes tutorial", sec. 3.4: weights kept in 4 bits are
 // turned back into the 16-bit compute dtype before the matmul).
 //
-// w_hat = bf16_rn(fp32(code_value[code] * s_b)).  One thread handles units
-// of 4 packed bytes = 8 elements and writes 16 bytes of bf16; 8 consecutive
-// lanes share a 64-block.  The 16 code values sit in shared memory, one copy
-// per lane (value j of lane l at word j*32 + l), so the data-dependent
-// lookups never collide on a bank.
+// w_hat = bf16_rn(fp32(code_value[code] * s_b)).  One lane owns one 64-block:
+// it reads the block's 32 packed bytes and its scale, builds the 16 values
+// w_hat_j of the block once as register byte tables (the GEMV's lookup,
+// lut.cuh), and turns each 32-bit word of codes into four bf16x2 registers
+// with byte permutes - about three instructions per weight, against the
+// HBM budget of roughly fourteen.  A warp's 32 blocks (4 KB of bf16) go to a
+// shared-memory tile laid out with the 128-byte swizzle (so the 16-byte
+// stores of eight consecutive lanes hit distinct banks), and one TMA store
+// writes the tile out; two tiles per warp alternate so the store of one
+// overlaps the work on the next.
 #pragma once
 
 #include "common.cuh"
+#include "lut.cuh"
+#include "tma.cuh"
 
 namespace nf4q {
 
-constexpr int kDequantThreads = 256;
+constexpr int kDequantWarps = 8;
+constexpr int kDequantThreads = kDequantWarps * 32;
+constexpr uint32_t kDequantTileBytes = 32 * kBlock * 2;  // 32 blocks of bf16
+constexpr size_t kDequantSmemBytes = 1024 + 2 * kDequantWarps * kDequantTileBytes;
+constexpr int kDequantCtasPerSm = 3;  // 65 KB of staging each
 
-template <int U>
+// Output tensor map: [n_blocks rows][64 bf16], box {64, 32}, 128-byte swizzle.
+template <int CODE>
 __global__ void __launch_bounds__(kDequantThreads)
-dequantize_kernel(const uint32_t* __restrict__ packed, ScaleView sv,
-                  uint4* __restrict__ out, int64_t n_units,
+dequantize_kernel(const uint4* __restrict__ packed, ScaleView sv,
+                  const __grid_constant__ CUtensorMap tmap_out, int64_t n_blocks,
                   const __grid_constant__ CodeValues C) {
-  __shared__ float s_code[16 * 32];
-  for (int i = threadIdx.x; i < 16 * 32; i += blockDim.x) s_code[i] = C.v[i >> 5];
-  __syncthreads();
-  const uint32_t lane = threadIdx.x & 31u;
-  const float* code = s_code + lane;
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // thread t handles units t, t + nthreads, ... in groups of U
-  for (int64_t u0 = tid; u0 < n_units; u0 += nthreads * U) {
-    uint32_t word[U];
-    float s[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t unit = u0 + static_cast<int64_t>(u) * nthreads;
-      word[u] = unit < n_units ? ld_stream_u32(packed + unit) : 0u;
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+  const uint32_t bufs = base + warp * 2 * kDequantTileBytes;
+  const int64_t n_tiles = (n_blocks + 31) / 32;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kDequantWarps;
+  int parity = 0;
+  for (int64_t tile = static_cast<int64_t>(blockIdx.x) * kDequantWarps + warp; tile < n_tiles;
+       tile += nwarps, parity ^= 1) {
+    const int64_t b = tile * 32 + lane;
+    uint4 p0 = make_uint4(0u, 0u, 0u, 0u), p1 = p0;
+    float s = 0.f;
+    if (b < n_blocks) {
+      p0 = ld_stream_u4(packed + 2 * b);
+      p1 = ld_stream_u4(packed + 2 * b + 1);
+      s = block_scale(sv, b);
     }
+    RowTable<CODE> T;
+    build_table<CODE>(T, s, C);
+    const uint32_t buf = bufs + parity * kDequantTileBytes;
+    // the store issued from this buffer two tiles ago must have read it
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    const uint32_t row = buf + lane * 128;
+    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t unit = u0 + static_cast<int64_t>(u) * nthreads;
-      s[u] = unit < n_units ? block_scale(sv, unit >> 3) : 0.f;
+    for (int k = 0; k < 8; ++k) {
+      uint32_t r[4];
+      dequant_word<CODE>(T, words[k], r);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((k ^ (lane & 7)) << 4)),
+                   "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                   : "memory");
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t unit = u0 + static_cast<int64_t>(u) * nthreads;
-      if (unit >= n_units) continue;
-      const uint32_t p = word[u];
-      float f[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        // element i: byte i/2, high nibble for even i
-        const uint32_t nib = (p >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 0xFu;
-        f[i] = __fmul_rn(code[nib * 32], s[u]);
-      }
-      uint4 o;
-      o.x = pack_bf16x2(f[0], f[1]);
-      o.y = pack_bf16x2(f[2], f[3]);
-      o.z = pack_bf16x2(f[4], f[5]);
-      o.w = pack_bf16x2(f[6], f[7]);
-      st_u4(out + unit, o);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&tmap_out, buf, 0, static_cast<int>(tile * 32));
+      bulk_commit();
     }
   }
+  if (lane == 0) bulk_wait_all();
 }
 
 }  // namespace nf4q

@@ -5,18 +5,16 @@
 //
 // The mean is the float32 nearest to the EXACT mean, whatever the order in
 // which the GPU adds things up:
-//   pass 1 (dq_sum_kernel): every CTA adds its values in fp64 and atomically
-//     accumulates the fp64 sum, the largest value and the smallest non-zero
-//     value (as bit patterns; non-negative floats order like integers).  The
-//     last CTA to finish checks whether fp64 addition was exact for this
-//     tensor (all values are multiples of the smallest one's ulp and the
-//     total stays below 2^53 such ulps), which makes the sum independent of
-//     the order of the additions; it then rounds the fp64 quotient to float32,
-//     with the exact remainder deciding the one case where that could round
-//     twice (a quotient exactly on a float32 midpoint).  Otherwise (absmax
-//     values spread over more than ~29 binades) that CTA re-adds all values
-//     exactly as per-exponent integer mantissa sums into a 320-bit integer
-//     (sum * 2^149), divides by n_b and rounds with integer arithmetic.
+//   pass 1 (dq_sum_kernel, or fused into the quantize kernel): every value
+//     a in [2^-32, 2^8) is the integer a * 2^55 < 2^63 exactly; threads add
+//     these integers in 128 bits, CTAs combine theirs with 64-bit atomics
+//     (carry propagated by hand), so the total is exact and independent of
+//     the order.  A non-zero value outside that range (or not finite) raises
+//     a flag.  The last CTA to finish divides the exact total by n_b with
+//     integer arithmetic and rounds to float32 (ties to even); if the flag
+//     is up it first re-adds all values exactly as per-exponent integer
+//     mantissa sums into a 320-bit integer instead.  Integer work only: the
+//     fp64 units of this GPU are far too slow to sit in the quantize loop.
 //   pass 2 (dq_quant_kernel): one warp per 256-block.
 #pragma once
 
@@ -27,13 +25,14 @@ namespace nf4q {
 
 // Layout of the double-quant workspace (cleared before pass 1).
 struct DqWorkspace {
-  double sum;             // fp64 sum of all absmax values
-  uint32_t max_bits;      // largest value, as bits
-  uint32_t inv_min_bits;  // ~(smallest non-zero value, as bits)
-  uint32_t ticket;        // CTAs finished
-  uint32_t pad[11];
+  unsigned long long lo;   // total of a * 2^55 over in-range values,
+  unsigned long long hi;   //   low and high 64 bits
+  uint32_t out_of_range;   // some non-zero value outside [2^-32, 2^8)
+  uint32_t ticket;         // CTAs finished
+  uint32_t pad[10];
 };
 static_assert(sizeof(DqWorkspace) == 64, "workspace layout");
+constexpr int kDqFixShift = 55;  // fixed point: a * 2^55
 
 // ---------------------------------------------------------------- big ints
 constexpr int kLimbs = 10;  // 320 bits: sum * 2^149 < 2^32 * 2^128 * 2^149
@@ -89,93 +88,84 @@ __device__ float big_round_mean(const uint32_t (&A)[kLimbs], uint32_t n) {
   return __uint_as_float((static_cast<uint32_t>(be) << 23) | (mant & 0x7FFFFFu));
 }
 
-// Float32 nearest (ties to even) to S / n for an exact fp64 sum S.
-__device__ __forceinline__ float dq_mean_from_exact_sum(double gsum, uint32_t n) {
-  const double dn = static_cast<double>(n);
-  const double q = gsum / dn;
-  float f = static_cast<float>(q);
-  if (static_cast<double>(f) != q) {
-    const float up = __uint_as_float(__float_as_uint(f) + 1u);
-    const float dn_f = f > 0.f ? __uint_as_float(__float_as_uint(f) - 1u) : 0.f;
-    const float other = static_cast<double>(f) < q ? up : dn_f;
-    const double mid = (static_cast<double>(f) + static_cast<double>(other)) * 0.5;
-    if (mid == q) {  // quotient exactly on a midpoint: the remainder decides
-      const double rem = fma(-q, dn, gsum);
-      const float lo = fminf(f, other), hi = fmaxf(f, other);
-      if (rem > 0.0) f = hi;
-      else if (rem < 0.0) f = lo;
-      else f = (__float_as_uint(lo) & 1u) ? hi : lo;
-    }
-  }
-  return f;
-}
-
 constexpr int kDqSumThreads = 512;
 constexpr int kDqQuantThreads = 256;
 
-// ---------------------------------------------------------------- pass 1
-__global__ void __launch_bounds__(kDqSumThreads)
-dq_sum_kernel(const float* __restrict__ absmax, int64_t nb,
-              DqWorkspace* __restrict__ ws, float* __restrict__ offset) {
-  __shared__ double s_sum[kDqSumThreads / 32];
-  __shared__ uint32_t s_max[kDqSumThreads / 32], s_imin[kDqSumThreads / 32];
-  __shared__ bool s_last;
-  __shared__ unsigned long long s_hist[256];
+// Running exact sum of one thread over absmax values (fixed point 2^-55,
+// 128 bits) and the out-of-range flag.
+// a * 2^55 as an integer (0 for a == 0); false if a is non-zero and outside
+// [2^-32, 2^8) (or not finite).
+__device__ __forceinline__ bool dq_fixed(float a, unsigned long long& A) {
+  const uint32_t bits = __float_as_uint(a) & 0x7FFFFFFFu;
+  const uint32_t e = bits >> 23;  // a = 1.m * 2^(e - 127)
+  A = 0ull;
+  if (bits == 0u) return true;
+  if (e < 95u || e > 134u) return false;
+  A = static_cast<unsigned long long>((bits & 0x7FFFFFu) | 0x800000u) << (e - 95u);
+  return true;
+}
 
-  double sum = 0.0;
-  uint32_t mx = 0, imn = 0;  // imn = ~min over non-zero values
-  auto add = [&](float a) {
-    const uint32_t bits = __float_as_uint(a) & 0x7FFFFFFFu;
-    sum += static_cast<double>(__uint_as_float(bits));
-    mx = max(mx, bits);
-    if (bits) imn = max(imn, ~bits);
-  };
-  const int64_t nvec = nb / 4;  // absmax is 16-byte aligned
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
-       i += stride) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(absmax) + i);
-    add(v.x); add(v.y); add(v.z); add(v.w);
+struct DqStats {
+  unsigned long long lo = 0, hi = 0;
+  bool oor = false;
+  __device__ __forceinline__ void add(float a) {
+    unsigned long long A;
+    if (!dq_fixed(a, A)) { oor = true; return; }
+    lo += A;
+    hi += lo < A ? 1ull : 0ull;
   }
-  if (blockIdx.x == 0 && threadIdx.x < (nb & 3)) add(__ldg(absmax + nvec * 4 + threadIdx.x));
+};
+
+// Combines the sums of all threads of the CTA into the workspace and takes
+// a ticket; true (in every thread) in the last CTA to finish.  Every
+// thread's earlier global writes are visible grid-wide before the ticket.
+template <int NWARPS>
+__device__ __forceinline__ bool dq_commit(DqStats st, DqWorkspace* ws) {
+  __shared__ unsigned long long s_lo[NWARPS], s_hi[NWARPS];
+  __shared__ int s_oor[NWARPS];
+  __shared__ bool s_last;
   for (int o = 16; o > 0; o >>= 1) {
-    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    imn = max(imn, __shfl_xor_sync(0xFFFFFFFFu, imn, o));
+    const unsigned long long l2 = __shfl_xor_sync(0xFFFFFFFFu, st.lo, o);
+    const unsigned long long h2 = __shfl_xor_sync(0xFFFFFFFFu, st.hi, o);
+    st.lo += l2;
+    st.hi += h2 + (st.lo < l2 ? 1ull : 0ull);
   }
+  const int oor = __any_sync(0xFFFFFFFFu, st.oor);
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) { s_sum[wid] = sum; s_max[wid] = mx; s_imin[wid] = imn; }
+  if (lane == 0) { s_lo[wid] = st.lo; s_hi[wid] = st.hi; s_oor[wid] = oor; }
+  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int k = 1; k < kDqSumThreads / 32; ++k) {
-      sum += s_sum[k]; mx = max(mx, s_max[k]); imn = max(imn, s_imin[k]);
+    int any = s_oor[0];
+    for (int k = 1; k < NWARPS; ++k) {
+      st.lo += s_lo[k];
+      st.hi += s_hi[k] + (st.lo < s_lo[k] ? 1ull : 0ull);
+      any |= s_oor[k];
     }
-    atomicAdd(&ws->sum, sum);
-    atomicMax(&ws->max_bits, mx);
-    atomicMax(&ws->inv_min_bits, imn);
+    const unsigned long long old = atomicAdd(&ws->lo, st.lo);
+    atomicAdd(&ws->hi, st.hi + (old + st.lo < old ? 1ull : 0ull));
+    if (any) atomicOr(&ws->out_of_range, 1u);
     __threadfence();
     const uint32_t t = atomicAdd(&ws->ticket, 1u);
     s_last = (t == gridDim.x - 1);
   }
   __syncthreads();
-  if (!s_last) return;
+  return s_last;
+}
+
+// Run by every thread of the last CTA: *offset = the float32 nearest to the
+// exact mean of the nb values at absmax.
+__device__ __noinline__ void dq_finalize(const float* __restrict__ absmax, int64_t nb,
+                                        DqWorkspace* __restrict__ ws,
+                                        float* __restrict__ offset) {
+  __shared__ unsigned long long s_hist[256];
   __threadfence();
-
-  // ---- last CTA: exactness check, optional exact re-sum, rounding
-  const uint32_t gmax = atomicAdd(&ws->max_bits, 0u);
-  const uint32_t gmin = ~atomicAdd(&ws->inv_min_bits, 0u);
-  const double gsum = atomicAdd(&ws->sum, 0.0);
-  const int e_hi = max(static_cast<int>(gmax >> 23), 1);
-  const int e_lo = max(static_cast<int>(gmin >> 23), 1);
-  const uint32_t n = static_cast<uint32_t>(nb);
-  const int log2n = n <= 1 ? 0 : 32 - __clz(n - 1);
-  const bool exact = gmax == 0u || (e_hi < 255 && log2n + (e_hi - e_lo) + 24 <= 53);
-
-  if (!exact) {
+  const bool oor = atomicAdd(&ws->out_of_range, 0u) != 0u;
+  if (oor) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) s_hist[i] = 0ull;
     __syncthreads();
     for (int64_t i = threadIdx.x; i < nb; i += blockDim.x) {
-      const uint32_t bits = __float_as_uint(__ldg(absmax + i)) & 0x7FFFFFFFu;
+      const uint32_t bits = __float_as_uint(__ldcg(absmax + i)) & 0x7FFFFFFFu;
       const uint32_t e = min(bits >> 23, 254u);
       const uint32_t m = e ? ((bits & 0x7FFFFFu) | 0x800000u) : bits;
       atomicAdd(&s_hist[max(e, 1u)], static_cast<unsigned long long>(m));
@@ -183,16 +173,33 @@ dq_sum_kernel(const float* __restrict__ absmax, int64_t nb,
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    if (exact) {
-      *offset = nb == 0 ? 0.f : dq_mean_from_exact_sum(gsum, n);
-    } else {
-      uint32_t A[kLimbs];
-      for (int i = 0; i < kLimbs; ++i) A[i] = 0u;
+    uint32_t A[kLimbs];  // sum * 2^149
+    for (int i = 0; i < kLimbs; ++i) A[i] = 0u;
+    if (oor) {
       for (int e = 1; e < 255; ++e)
         if (s_hist[e]) big_add_shifted(A, s_hist[e], e - 1);
-      *offset = big_round_mean(A, n);
+    } else {
+      big_add_shifted(A, atomicAdd(&ws->lo, 0ull), 149 - kDqFixShift);
+      big_add_shifted(A, atomicAdd(&ws->hi, 0ull), 149 - kDqFixShift + 64);
     }
+    *offset = big_round_mean(A, static_cast<uint32_t>(nb));
   }
+}
+
+// ---------------------------------------------------------------- pass 1
+__global__ void __launch_bounds__(kDqSumThreads)
+dq_sum_kernel(const float* __restrict__ absmax, int64_t nb,
+              DqWorkspace* __restrict__ ws, float* __restrict__ offset) {
+  DqStats st;
+  const int64_t nvec = nb / 4;  // absmax is 16-byte aligned
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += stride) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(absmax) + i);
+    st.add(v.x); st.add(v.y); st.add(v.z); st.add(v.w);
+  }
+  if (blockIdx.x == 0 && threadIdx.x < (nb & 3)) st.add(__ldg(absmax + nvec * 4 + threadIdx.x));
+  if (dq_commit<kDqSumThreads / 32>(st, ws)) dq_finalize(absmax, nb, ws, offset);
 }
 
 // ---------------------------------------------------------------- pass 2

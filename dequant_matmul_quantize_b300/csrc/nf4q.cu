@@ -110,6 +110,33 @@ bool gemv_attr_ready() {
   return true;
 }
 
+// Opt the dequantize kernels in to their dynamic shared memory (once per
+// device).
+bool dequantize_attr_ready() {
+  static bool done[kMaxDevices] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (done[dev]) return true;
+  const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  const int b = static_cast<int>(kDequantSmemBytes);
+  done[dev] = cudaFuncSetAttribute(dequantize_kernel<0>, A, b) == cudaSuccess &&
+              cudaFuncSetAttribute(dequantize_kernel<1>, A, b) == cudaSuccess;
+  return done[dev];
+}
+
+using QuantKernelFn = void (*)(const void*, uint2*, float*, int64_t, QuantParams,
+                               DqWorkspace*, float*);
+
+// The quantize instantiation for a code, input type and fused double-quant pass.
+QuantKernelFn quantize_kernel_for(int code, int bf16, int dq) {
+  if (code == 0) {
+    if (bf16) return dq ? quantize_kernel<0, true, true> : quantize_kernel<0, true, false>;
+    return dq ? quantize_kernel<0, false, true> : quantize_kernel<0, false, false>;
+  }
+  if (bf16) return dq ? quantize_kernel<1, true, true> : quantize_kernel<1, true, false>;
+  return dq ? quantize_kernel<1, false, true> : quantize_kernel<1, false, false>;
+}
+
 // Opt the quantize kernels in to their dynamic shared memory (once per device).
 bool quantize_attr_ready() {
   static bool done[kMaxDevices] = {false};
@@ -118,10 +145,12 @@ bool quantize_attr_ready() {
   if (done[dev]) return true;
   const int b0 = static_cast<int>(quantize_smem_bytes(0)), b1 = static_cast<int>(quantize_smem_bytes(1));
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  bool ok = cudaFuncSetAttribute(quantize_kernel<0, true, 2>, A, b0) == cudaSuccess &&
-            cudaFuncSetAttribute(quantize_kernel<0, false, 2>, A, b0) == cudaSuccess &&
-            cudaFuncSetAttribute(quantize_kernel<1, true, 2>, A, b1) == cudaSuccess &&
-            cudaFuncSetAttribute(quantize_kernel<1, false, 2>, A, b1) == cudaSuccess;
+  bool ok = true;
+  for (int k = 0; k < 8; ++k) {
+    const int code = k >> 2;
+    ok = ok && cudaFuncSetAttribute(quantize_kernel_for(code, (k >> 1) & 1, k & 1), A,
+                                    code == 0 ? b0 : b1) == cudaSuccess;
+  }
   done[dev] = ok;
   return ok;
 }
@@ -135,9 +164,8 @@ int quantize_ctas_per_sm(int code) {
   if (cache[dev][code] == 0) {
     int n = 0;
     const size_t smem = quantize_smem_bytes(code);
-    cudaError_t e = code == 0
-        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<0, true, 2>, kQuantThreads, smem)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<1, true, 2>, kQuantThreads, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, quantize_kernel_for(code, 1, 1), kQuantThreads, smem);
     cache[dev][code] = (e == cudaSuccess && n > 0) ? n : 1;
   }
   return cache[dev][code];
@@ -217,13 +245,18 @@ nf4q_status nf4q_thresholds(int32_t code, float* out, int32_t* count) {
   return NF4Q_OK;
 }
 
-nf4q_status nf4q_quantize(const void* w, int32_t in_dtype, const nf4q_weight* wq,
-                          void* stream) {
-  nf4q_status st = check_shape(wq);
-  if (st != NF4Q_OK) return st;
-  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16) return NF4Q_ERR_INVALID_ARG;
+
+}  // extern "C"
+
+namespace nf4q {
+namespace {
+// Both passes of the double quantization, on a cleared workspace record.
+// Quantize launch after the argument checks common to both entry points
+// (n > 0).  ws != nullptr: fused first double-quant pass into ws (cleared
+// here) and wq->offset.
+nf4q_status quantize_launch(const void* w, int32_t in_dtype, const nf4q_weight* wq, void* ws,
+                            cudaStream_t s) {
   const int64_t n = wq->rows * wq->cols;
-  if (n == 0) return NF4Q_OK;
   if (!w || !wq->packed || !wq->absmax) return NF4Q_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(wq->packed) || !aligned16(wq->absmax))
     return NF4Q_ERR_ALIGNMENT;
@@ -238,48 +271,47 @@ nf4q_status nf4q_quantize(const void* w, int32_t in_dtype, const nf4q_weight* wq
   }
   for (int i = 0; i < 15; ++i) P.thr[i] = i < T.nthr[c] ? T.thr[c][i] : 2.0f;
   if (!quantize_attr_ready()) return NF4Q_ERR_CUDA;
-  const int64_t n_units = n / 8;
-  constexpr int U = 2;
-  const int64_t grid = grid_for(n_units, 32 * U * (kQuantThreads / 32),
+  const int64_t n_units = n / 16;  // 16 elements per lane and unit
+  const int64_t grid = grid_for(n_units, kQuantThreads,
                                 static_cast<int64_t>(sm_count()) * quantize_ctas_per_sm(c));
-  const size_t smem = quantize_smem_bytes(c);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t* packed = reinterpret_cast<uint32_t*>(wq->packed);
-  if (c == NF4Q_CODE_NF4) {
-    if (in_dtype == NF4Q_IN_BF16)
-      quantize_kernel<0, true, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
-    else
-      quantize_kernel<0, false, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
-  } else {
-    if (in_dtype == NF4Q_IN_BF16)
-      quantize_kernel<1, true, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
-    else
-      quantize_kernel<1, false, U><<<grid, kQuantThreads, smem, s>>>(w, packed, wq->absmax, n_units, P);
-  }
+  if (ws && cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
+  quantize_kernel_for(c, in_dtype == NF4Q_IN_BF16, ws != nullptr)<<<grid, kQuantThreads,
+                                                                    quantize_smem_bytes(c), s>>>(
+      w, reinterpret_cast<uint2*>(wq->packed), wq->absmax, n_units, P,
+      static_cast<DqWorkspace*>(ws), wq->offset);
   return launch_status();
 }
 
-}  // extern "C"
+// Second double-quant pass: int8 codes and per-256 scales from the mean.
+nf4q_status dq_quant_launch(const nf4q_weight* wq, int64_t nb, cudaStream_t s) {
+  const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
+  const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
+  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset, wq->absmax_q,
+                                                  wq->scale2);
+  return launch_status();
+}
 
-namespace nf4q {
-namespace {
-// Both passes of the double quantization, on a cleared workspace record.
 nf4q_status dq_launch(const nf4q_weight* wq, int64_t nb, void* ws, cudaStream_t s) {
   if (cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
   const int64_t g1 = grid_for(nb / 4, kDqSumThreads, static_cast<int64_t>(sm_count()));
   dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb, static_cast<DqWorkspace*>(ws),
                                              wq->offset);
   if (cudaGetLastError() != cudaSuccess) return NF4Q_ERR_CUDA;
-  const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
-  const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
-  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset, wq->absmax_q,
-                                                  wq->scale2);
-  return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
+  return dq_quant_launch(wq, nb, s);
 }
 }  // namespace
 }  // namespace nf4q
 
 extern "C" {
+
+nf4q_status nf4q_quantize(const void* w, int32_t in_dtype, const nf4q_weight* wq,
+                          void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16) return NF4Q_ERR_INVALID_ARG;
+  if (wq->rows * wq->cols == 0) return NF4Q_OK;
+  return quantize_launch(w, in_dtype, wq, nullptr, static_cast<cudaStream_t>(stream));
+}
 
 size_t nf4q_double_quant_workspace_bytes(int64_t n_b) {
   (void)n_b;
@@ -305,6 +337,26 @@ nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
   return dq_launch(wq, nb, workspace, s);
 }
 
+nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight* wq,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16) return NF4Q_ERR_INVALID_ARG;
+  if (wq->double_quant != 1) return NF4Q_ERR_INVALID_ARG;
+  if (!wq->absmax_q || !wq->scale2 || !wq->offset) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned4(wq->offset) || !aligned4(wq->scale2)) return NF4Q_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t nb = wq->rows * wq->cols / kBlock;
+  if (nb == 0)
+    return cudaMemsetAsync(wq->offset, 0, sizeof(float), s) == cudaSuccess ? NF4Q_OK
+                                                                          : NF4Q_ERR_CUDA;
+  if (!aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < sizeof(DqWorkspace)) return NF4Q_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NF4Q_ERR_ALIGNMENT;
+  if ((st = quantize_launch(w, in_dtype, wq, workspace, s)) != NF4Q_OK) return st;
+  return dq_quant_launch(wq, nb, s);
+}
+
 nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
   nf4q_status st = check_shape(wq);
   if (st != NF4Q_OK) return st;
@@ -314,13 +366,32 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
   if (!out) return NF4Q_ERR_INVALID_ARG;
   if (!aligned16(out)) return NF4Q_ERR_ALIGNMENT;
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
-  const int64_t n_units = n / 8;
-  constexpr int U = 4;
-  const int64_t grid = grid_for(n_units, static_cast<int64_t>(kDequantThreads) * U,
-                                static_cast<int64_t>(sm_count()) * 8);
-  dequantize_kernel<U><<<grid, kDequantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint32_t*>(wq->packed), scale_view(wq),
-      static_cast<uint4*>(out), n_units, code_values(wq->code));
+  if (!dequantize_attr_ready()) return NF4Q_ERR_CUDA;
+  const int64_t n_blocks = n / kBlock;
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return NF4Q_ERR_CUDA;
+  CUtensorMap tout;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kBlock), static_cast<cuuint64_t>(n_blocks)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kBlock * 2)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlock), 32};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return NF4Q_ERR_CUDA;
+  }
+  const int64_t n_tiles = (n_blocks + 31) / 32;
+  const int64_t grid = grid_for(n_tiles, kDequantWarps,
+                                static_cast<int64_t>(sm_count()) * kDequantCtasPerSm);
+  const uint4* pk = reinterpret_cast<const uint4*>(wq->packed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (wq->code == NF4Q_CODE_NF4)
+    dequantize_kernel<0><<<grid, kDequantThreads, kDequantSmemBytes, s>>>(
+        pk, scale_view(wq), tout, n_blocks, code_values(wq->code));
+  else
+    dequantize_kernel<1><<<grid, kDequantThreads, kDequantSmemBytes, s>>>(
+        pk, scale_view(wq), tout, n_blocks, code_values(wq->code));
   return launch_status();
 }
 

@@ -3,39 +3,41 @@
 // blocks, sec. 3.2 NF4 levels; FP4 per "bitsandbytes introduction",
 // sec. 一 item 7).
 //
-// Work unit: 8 consecutive elements -> one 32-bit word of packed codes.  A
-// 64-block is 8 consecutive units, held by 8 consecutive lanes, so its
-// absmax is a 3-step butterfly.  Each warp pass covers U*256 elements.
+// Work unit: 16 consecutive elements -> two 32-bit words of packed codes.  A
+// 64-block is 4 consecutive units, held by 4 consecutive lanes, so its
+// absmax is a 2-step butterfly.
 //
 // Code search.  The exact rule is on wn = fp32(w / absmax) (IEEE division):
 // code = #{ j : wn > T_j } over the round-down midpoints T_j (FP4: on |wn|,
-// plus the sign).  The kernel does not divide per element.  It forms
-// q = fp32(w * r) with r an approximate reciprocal of absmax (relative error
-// at most 2^-22), which is within 2^-21 of wn, and looks q up
-// in 259-bin tables (bin = nearest integer of q*128 + 129): every bin is
-// narrower than the gap between decision points (FP4's are mirrored onto the
-// signed value), so at most one point T is in reach and
-// code = lo(bin) + (q > T) * dl(bin).  When q lies within 2^-19 of that T the
-// two could disagree, so the unit is recomputed with the exact division and
-// a plain count over all T_j; so are blocks whose absmax is zero, below
-// 2^-126 or above 2^126 (1/absmax not a normal number) or not finite.  The result is therefore
-// exactly the rule; the fast path only saves work.  The tables are
-// replicated once per lane in shared memory (entry e of lane l at word
-// e*32 + l), so the data-dependent lookups of a warp never collide on a
-// bank, and the per-element work is spread over the FMA pipe (bin, address,
-// packing), the load pipe (table reads) and the integer pipe (compare bit,
-// near test).
+// plus the sign).  The kernel does not divide per element.  With r an
+// approximate reciprocal of absmax (relative error at most 2^-22), the exact
+// product v r is within 2^-21 of wn.  One FMA on v r gives the bin of a
+// 259-entry table (bin = nearest integer of 128 v r + 129): every bin is
+// narrower than the gap between decision points (FP4's are mirrored onto
+// the signed value), so at most one point T is in reach, and
+// code = lo(bin) + [wn > T] * dl(bin) (dl = 1 for NF4).  A second FMA forms
+// e = (v r - T) 2^19 from the table's -T 2^19; if |e| <= 1 (v r within about
+// 2^-19 of T) the two sides of T could disagree and the unit is recomputed
+// with the exact division and a plain count over all T_j; so are blocks
+// whose absmax is zero, below 2^-100 (2^19 / absmax would overflow) or above
+// 2^126 (1/absmax not a normal number) or not finite.  Otherwise sat(e) is the compare bit exactly, and
+// lo + bit (one add on the table's float 2^23 + lo) is the code in the low
+// mantissa bits.  The result is therefore exactly the rule; the fast path
+// only saves work.  The eight codes of a word are packed by a multiply-add
+// chain (Horner) on those float bit patterns, and one addition removes the
+// 2^23 terms.  The tables are replicated once per lane in shared memory, so
+// the data-dependent lookups of a warp never collide on a bank.
 #pragma once
 
 #include "common.cuh"
+#include "double_quant.cuh"
 
 namespace nf4q {
 
 constexpr int kQuantThreads = 512;
 constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23
 constexpr uint32_t kMagicBits = 0x4B400000u;
-constexpr float kNearEps = 1.9073486328125e-06f;  // 2^-19
-constexpr float kTinyScale = 1.17549435e-38f;     // 2^-126
+constexpr float kTinyScale = 7.88860905e-31f;     // 2^-100
 constexpr float kHugeScale = 8.50705917e37f;      // 2^126
 constexpr int kLutWords = kLutEntries * 32;       // one table, replicated per lane
 
@@ -46,34 +48,46 @@ struct QuantParams {
   float thr[15];                // exact-path decision points
 };
 
-__device__ __forceinline__ float lds_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ int lds_s32(uint32_t a) {
-  int v;
-  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
+// Shared-memory tables, one copy per lane: entry e of lane l is the pair
+// {-T * 2^19, 2^23 + lo} at byte (e * 32 + l) * 8 (T the decision point in
+// reach of bin e, lo the code below it), and for FP4 the float code step dl
+// at byte kPairBytes + (e * 32 + l) * 4.
+constexpr uint32_t kPairBytes = kLutEntries * 32 * 8;
+constexpr float kTwo19 = 524288.0f;
+constexpr uint32_t kCodeMagicFix = 0x05000000u;  // -(2^23 bits * (16 + 1)) mod 2^32
+
+__device__ __forceinline__ float sat_add0(float e) {
+  float r;  // clamp to [0, 1]
+  asm("add.sat.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(e));
+  return r;
 }
 
-// Fast code of one element: bin lookup (2 or 3 shared loads) and a compare.
-// `lane_tab` is this lane's column of the tables minus the magic offset of
-// the bin computation, so that the address is one multiply-add.  The code is
-// added into `word` at nibble shift `sh` with multiply-adds.
+// Fast code of one element v of a block with approximate reciprocal scale
+// r (r128 = 128 r, r19 = 2^19 r, both exact): bin from v * r128, then
+// e = (v r - T) 2^19 in one FMA on the exact product v r.  |e| <= 1 flags the
+// unit for the exact path; otherwise sat(e) is the compare bit exactly.
+// `lane_tab` / `lane_dl` are this lane's table columns minus the magic
+// offset of the bin, so each address is one multiply-add.  Returns the code
+// as the bits of the float 2^23 + code.
 template <int CODE>
-__device__ __forceinline__ void code_fast(float q, uint32_t lane_tab, bool& near, uint32_t& word,
-                                          int sh) {
-  const float y = __fmaf_rn(q, 128.0f, 129.0f + kMagic);
-  const uint32_t a = __float_as_uint(y) * 128u + lane_tab;
-  const float t = lds_f32(a);
-  const int lo = lds_s32(a + kLutWords * 4);
-  const float d = __fsub_rn(t, q);
-  near |= fabsf(d) <= kNearEps;
-  const int bit = static_cast<int>(__float_as_uint(d) >> 31);  // q > t
-  const int dl = CODE == 0 ? 1 : lds_s32(a + 2 * kLutWords * 4);
-  const int c = bit * dl + lo;
-  word += static_cast<uint32_t>(c) * (1u << sh);
+__device__ __forceinline__ uint32_t code_fast(float v, float r128, float r19, uint32_t lane_tab,
+                                              uint32_t lane_dl, float& near) {
+  const float y = __fmaf_rn(v, r128, 129.0f + kMagic);
+  const uint32_t yb = __float_as_uint(y);
+  float ntp, lof;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(ntp), "=f"(lof) : "r"(yb * 256u + lane_tab));
+  const float e = __fmaf_rn(v, r19, ntp);
+  near = fminf(near, fabsf(e));  // <= 1: v r within about 2^-19 of T
+  const float bit = sat_add0(e);
+  float c;
+  if (CODE == 0) {
+    c = __fadd_rn(lof, bit);
+  } else {
+    float dl;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(dl) : "r"(yb * 128u + lane_dl));
+    c = __fmaf_rn(bit, dl, lof);
+  }
+  return __float_as_uint(c);
 }
 
 template <int CODE>
@@ -91,18 +105,6 @@ __device__ __forceinline__ uint32_t code_exact(float w, float a, const QuantPara
 // element 2j -> bits 7..4 of byte j, element 2j+1 -> bits 3..0.
 __device__ __forceinline__ constexpr int nib_shift(int i) {
   return 8 * (i >> 1) + ((i & 1) ? 0 : 4);
-}
-
-template <int CODE>
-__device__ __noinline__ uint32_t encode_unit_exact(float w0, float w1, float w2,
-                                                   float w3, float w4, float w5,
-                                                   float w6, float w7, float a,
-                                                   const QuantParams& P) {
-  const float w[8] = {w0, w1, w2, w3, w4, w5, w6, w7};
-  uint32_t word = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) word |= code_exact<CODE>(w[i], a, P) << nib_shift(i);
-  return word;
 }
 
 template <bool BF16IN>
@@ -125,90 +127,166 @@ __device__ __forceinline__ void load_unit(const void* base, int64_t unit,
   }
 }
 
+// Raw 16-byte loads of the 16 elements of unit `unit` (zeros if !live).
+template <bool BF16IN>
+__device__ __forceinline__ void load_raw(const void* base, int64_t unit, bool live,
+                                         uint4 (&raw)[BF16IN ? 2 : 4]) {
+#pragma unroll
+  for (int i = 0; i < (BF16IN ? 2 : 4); ++i)
+    raw[i] = live ? ld_stream_u4(static_cast<const uint4*>(base) + unit * (BF16IN ? 2 : 4) + i)
+                  : make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <bool BF16IN>
+__device__ __forceinline__ void unpack_raw(const uint4 (&raw)[BF16IN ? 2 : 4], float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < (BF16IN ? 2 : 4); ++i) {
+    const uint32_t q[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (BF16IN) {
+        v[8 * i + 2 * j] = bf16lo_to_f32(q[j]);
+        v[8 * i + 2 * j + 1] = bf16hi_to_f32(q[j]);
+      } else {
+        v[4 * i + j] = __uint_as_float(q[j]);
+      }
+    }
+  }
+}
+
+// The exact rule for the word (8 elements) `word` of the weight, reading
+// its elements again (rare: only words with a value near a decision point
+// or blocks with an extreme scale come here).
+template <int CODE, bool BF16IN>
+__device__ __noinline__ uint32_t encode_word_exact(const void* w, int64_t word, float a,
+                                                   const QuantParams& P) {
+  float v[8];
+  load_unit<BF16IN>(w, word, v);
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out |= code_exact<CODE>(v[i], a, P) << nib_shift(i);
+  return out;
+}
+
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;  // NaN if either is NaN, so a non-finite block is always seen
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
 
-template <int CODE, bool BF16IN, int U>
-__global__ void __launch_bounds__(kQuantThreads)
-quantize_kernel(const void* __restrict__ w, uint32_t* __restrict__ packed,
+// One lane handles units of 16 consecutive elements (two packed words); a
+// 64-block is four consecutive lanes, so its absmax is a 2-step butterfly.
+// DQ: also the first pass of double quantization - the absmax values are
+// summed exactly into `ws` and the last CTA writes their mean to `offset`
+// (double_quant.cuh).
+template <int CODE, bool BF16IN, bool DQ>
+__global__ void __launch_bounds__(kQuantThreads, 2)
+quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
                 float* __restrict__ absmax, int64_t n_units,
-                const __grid_constant__ QuantParams P) {
-  extern __shared__ uint32_t s_lut[];  // [tables][kLutEntries][32]
+                const __grid_constant__ QuantParams P, DqWorkspace* __restrict__ ws,
+                float* __restrict__ offset) {
+  extern __shared__ __align__(16) uint32_t s_lut[];  // pairs, then (FP4) steps
+  // DQ: exact running sum of each group leader's absmax values (a leader is
+  // the lane that stores a block's absmax), kept in shared memory to spare
+  // registers; and the out-of-range flag
+  __shared__ unsigned long long s_dq[DQ ? kQuantThreads / 4 : 1][2];
+  __shared__ int s_dq_oor;
+  if (DQ && (threadIdx.x & 3) == 0) s_dq[threadIdx.x >> 2][0] = s_dq[threadIdx.x >> 2][1] = 0ull;
+  if (DQ && threadIdx.x == 0) s_dq_oor = 0;
   for (int i = threadIdx.x; i < kLutWords; i += blockDim.x) {
     const int e = i >> 5;
-    s_lut[i] = __float_as_uint(P.lut_t[e]);
-    s_lut[kLutWords + i] = static_cast<uint32_t>(P.lut_lo[e]);
-    if (CODE == 1) s_lut[2 * kLutWords + i] = static_cast<uint32_t>(P.lut_dl[e]);
+    s_lut[2 * i] = __float_as_uint(-(P.lut_t[e] * kTwo19));
+    s_lut[2 * i + 1] = __float_as_uint(8388608.0f + static_cast<float>(P.lut_lo[e]));
+    if (CODE == 1) s_lut[2 * kLutWords + i] = __float_as_uint(static_cast<float>(P.lut_dl[e]));
   }
   __syncthreads();
 
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t lane_tab = static_cast<uint32_t>(__cvta_generic_to_shared(s_lut)) + lane * 4u -
-                            kMagicBits * 128u;
-  const int64_t gwarp =
-      (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const uint32_t tab = static_cast<uint32_t>(__cvta_generic_to_shared(s_lut));
+  const uint32_t lane_tab = tab + lane * 8u - kMagicBits * 256u;
+  const uint32_t lane_dl = tab + kPairBytes + lane * 4u - kMagicBits * 128u;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
 
-  for (int64_t base = gwarp * (32 * U); base < n_units;
-       base += nwarps * (32 * U)) {
-    float v[U][8];
+  // The raw input of the next unit is loaded before the current one is
+  // encoded, which doubles the bytes each lane keeps in flight.
+  constexpr int kRaw = BF16IN ? 2 : 4;  // 16-byte loads per unit
+  uint4 nxt[kRaw];
+  int64_t unit = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  load_raw<BF16IN>(w, unit, unit < n_units, nxt);
+  for (; unit - lane < n_units; unit += nthreads) {
+    const bool live = unit < n_units;
+    float v[16];
+    unpack_raw<BF16IN>(nxt, v);
+    load_raw<BF16IN>(w, unit + nthreads, unit + nthreads < n_units, nxt);
+    float a = fabsf(v[0]);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t unit = base + u * 32 + lane;
-      if (unit < n_units) {
-        load_unit<BF16IN>(w, unit, v[u]);
-      } else {
+    for (int i = 1; i < 16; ++i) a = max_nan(a, fabsf(v[i]));
+    a = max_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+    a = max_nan(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+    // 2^-100 <= a <= 2^126: the reciprocal is a normal number (the
+    // approximate one flushes subnormal results) and 2^19 r <= 2^119 is
+    // finite, so |v r| <= 1 + 2^-21 and every bin index is inside the
+    // table; anything else (zero, tiny, huge or non-finite absmax) takes
+    // the exact path
+    const bool ok = a >= kTinyScale && a <= kHugeScale;
+    uint32_t word[2] = {0u, 0u};
+    float near[2] = {2.0f, 2.0f};
+    if (ok) {
+      // Approximate reciprocal (relative error <= 2^-22): v r stays within
+      // 2^-21 of the exact quotient, inside the 2^-19 exact-fallback window.
+      float r;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+      const float r128 = r * 128.0f, r19 = r * kTwo19;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
+      for (int h = 0; h < 2; ++h) {
+        // Horner over the nibble order of the word: elements 6, 7, 4, 5,
+        // 2, 3, 0, 1 (element 2j is the high nibble of byte j); the 2^23
+        // of each code adds a constant that one addition removes
+        const float* vh = v + 8 * h;
+        uint32_t wd = code_fast<CODE>(vh[6], r128, r19, lane_tab, lane_dl, near[h]);
+#pragma unroll
+        for (int k = 1; k < 8; ++k) {
+          const int i = (6 - 2 * (k >> 1)) + (k & 1);
+          wd = wd * 16u + code_fast<CODE>(vh[i], r128, r19, lane_tab, lane_dl, near[h]);
+        }
+        word[h] = wd + kCodeMagicFix;
       }
     }
-    float amax[U];
+    if (live) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float m = fabsf(v[u][0]);
-#pragma unroll
-      for (int i = 1; i < 8; ++i) m = max_nan(m, fabsf(v[u][i]));
-      m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      m = max_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-      amax[u] = m;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t unit = base + u * 32 + lane;
-      const float a = amax[u];
-      // 2^-126 <= a <= 2^126: the reciprocal is a normal number (the
-      // approximate one flushes subnormal results), |w * rcp(a)| <= 1 + 2^-21
-      // and every bin index is inside the table; anything else (zero, tiny,
-      // huge or non-finite absmax) takes the exact path
-      const bool ok = a >= kTinyScale && a <= kHugeScale;
-      bool near = false;
-      uint32_t word = 0;
-      if (ok) {
-        // Approximate reciprocal (relative error <= 2^-22): q stays within
-        // 2^-21 of the exact quotient, inside the 2^-19 exact-fallback window.
-        float r;
-        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          code_fast<CODE>(__fmul_rn(v[u][i], r), lane_tab, near, word, nib_shift(i));
-      }
-      if (near || !ok)
-        word = encode_unit_exact<CODE>(v[u][0], v[u][1], v[u][2], v[u][3],
-                                       v[u][4], v[u][5], v[u][6], v[u][7], a, P);
-      if (unit < n_units) {
-        packed[unit] = word;
-        if ((lane & 7u) == 0u) absmax[unit >> 3] = a;
+      for (int h = 0; h < 2; ++h)
+        if (near[h] <= 1.0f || !ok) word[h] = encode_word_exact<CODE, BF16IN>(w, 2 * unit + h, a, P);
+      packed[unit] = make_uint2(word[0], word[1]);
+      if ((lane & 3u) == 0u) {
+        absmax[unit >> 2] = a;
+        if constexpr (DQ) {
+          unsigned long long A;
+          if (dq_fixed(a, A)) {
+            unsigned long long* acc = s_dq[threadIdx.x >> 2];
+            const unsigned long long lo = acc[0] + A;
+            acc[0] = lo;
+            if (lo < A) acc[1] += 1ull;
+          } else {
+            s_dq_oor = 1;
+          }
+        }
       }
     }
+  }
+  if constexpr (DQ) {
+    __syncthreads();
+    DqStats st;
+    if ((threadIdx.x & 3) == 0) {
+      st.lo = s_dq[threadIdx.x >> 2][0];
+      st.hi = s_dq[threadIdx.x >> 2][1];
+    }
+    st.oor = threadIdx.x == 0 && s_dq_oor != 0;
+    if (dq_commit<kQuantThreads / 32>(st, ws)) dq_finalize(absmax, n_units / 4, ws, offset);
   }
 }
 
 inline size_t quantize_smem_bytes(int code) {
-  return static_cast<size_t>(code == 0 ? 2 : 3) * kLutWords * 4;
+  return kPairBytes + (code == 0 ? 0 : static_cast<size_t>(kLutWords) * 4);
 }
 
 }  // namespace nf4q

@@ -144,6 +144,19 @@ size_t nf4q_double_quant_workspace_bytes(int64_t n_b);
 nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Blockwise quantization followed by double quantization, in one call (the
+ * stored form with double quant on, tutorial sec. 2.3, 3.2 and 3.3).  The
+ * results are bit for bit those of nf4q_quantize followed by
+ * nf4q_double_quant on the same arguments; the first double-quant pass (the
+ * exact mean) runs inside the quantize kernel, so only the per-256 pass is a
+ * second launch.
+ *   w, in_dtype  as for nf4q_quantize.
+ *   wq   wq->double_quant must be 1; writes packed, absmax, absmax_q,
+ *        scale2 and offset (alignments as for the two calls).
+ *   workspace  as for nf4q_double_quant (cleared by the call). */
+nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight* wq,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Dequantization to bf16 (tutorial sec. 3.4).
  *   out: device bf16 [rows x cols], 16-byte aligned.
  * s_b = fmaf(absmax_q[b], scale2[b/256], offset) with double quant, else

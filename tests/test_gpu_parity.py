@@ -168,6 +168,42 @@ def test_double_quant_degenerate_and_wide_range():
     _dq_direct(np.concatenate([np.full(3, 1e-45, np.float32), [3e38]]).astype(np.float32))
 
 
+def _weight_with_absmax(absmax: np.ndarray, seed: int) -> np.ndarray:
+    """One row whose 64-blocks have exactly the given absmax values."""
+    rng = np.random.default_rng(seed)
+    blocks = rng.uniform(-1, 1, (absmax.size, 64)).astype(np.float32)
+    blocks *= absmax[:, None]
+    blocks[:, 0] = absmax
+    return blocks.reshape(1, -1)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("code", ["nf4", "fp4"])
+def test_quantize_dq_fused_matches_two_calls(code, dtype):
+    """nf4q_quantize_dq == nf4q_quantize + nf4q_double_quant, bit for bit,
+    including absmax sets that take the exact re-sum path of the mean."""
+    rng = np.random.default_rng(5)
+    cases = [np.abs(rng.standard_normal(3000) * 0.05).astype(np.float32),
+             np.full(700, 0.125, np.float32),
+             np.zeros(300, np.float32)]
+    wide = (10.0 ** rng.uniform(-30, 30, 4000)).astype(np.float32)
+    wide[::7] = 0
+    cases.append(wide)
+    for i, am in enumerate(cases):
+        w = torch.from_numpy(_weight_with_absmax(am, i)).to(dtype).cuda()
+        fused = nq.quantize(w, code)                       # the fused entry point
+        two = nq.QuantizedWeight.empty(w.shape[0], w.shape[1], code, True, w.device)
+        nq.quantize_into(two, w)
+        nq.double_quant_into(two)
+        torch.cuda.synchronize()
+        a, b = gpu_state(fused), gpu_state(two)
+        for k in a:
+            assert_bits_equal(a[k], b[k], f"{code} case {i} {k}")
+        ref = oracle_state(as_f32(w), code)
+        for k in ("packed", "absmax", "absmax_q", "scale2", "offset"):
+            assert_bits_equal(a[k], ref[k], f"{code} case {i} {k} vs oracle")
+
+
 # ---------------------------------------------------------------- GEMV
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 12, 16])
 @pytest.mark.parametrize("shape", [(37, 320), (256, 1024), (129, 4160)])
