@@ -153,6 +153,35 @@ __device__ __forceinline__ bool dq_commit(DqStats st, DqWorkspace* ws) {
   return s_last;
 }
 
+// Float32 nearest (ties to even) to (hi * 2^64 + lo) * 2^-55 / n, when that
+// quotient is at least 2^-31 (so floor(S / n) has 25 bits or more and the
+// remainder only feeds the sticky bit); otherwise returns false.  S / n is
+// below 2^63 because every summand is.
+__device__ __forceinline__ bool dq_round_fixed(unsigned long long lo, unsigned long long hi,
+                                               uint32_t n, float* out) {
+  const uint32_t limb[4] = {static_cast<uint32_t>(hi >> 32), static_cast<uint32_t>(hi),
+                            static_cast<uint32_t>(lo >> 32), static_cast<uint32_t>(lo)};
+  unsigned long long q = 0, r = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const unsigned long long cur = (r << 32) | limb[i];
+    const unsigned long long d = cur / n;
+    r = cur - d * n;
+    q = (q << 32) | d;  // the top limbs of the quotient are zero
+  }
+  const int p = 64 - __clzll(static_cast<long long>(q));  // bit length of q
+  if (p < 25) return false;
+  const int sh = p - 24;
+  unsigned long long mant = q >> sh;
+  const unsigned long long rest = q & ((1ull << sh) - 1ull);
+  const unsigned long long half = 1ull << (sh - 1);
+  if (rest > half || (rest == half && (r != 0 || (mant & 1ull))) ) ++mant;
+  int be = p + 71;  // biased exponent of q * 2^-55: (p - 1) - 55 + 127
+  if (mant == (1ull << 24)) { mant >>= 1; ++be; }
+  *out = __uint_as_float((static_cast<uint32_t>(be) << 23) | (static_cast<uint32_t>(mant) & 0x7FFFFFu));
+  return true;
+}
+
 // Run by every thread of the last CTA: *offset = the float32 nearest to the
 // exact mean of the nb values at absmax.
 __device__ __noinline__ void dq_finalize(const float* __restrict__ absmax, int64_t nb,
@@ -179,8 +208,14 @@ __device__ __noinline__ void dq_finalize(const float* __restrict__ absmax, int64
       for (int e = 1; e < 255; ++e)
         if (s_hist[e]) big_add_shifted(A, s_hist[e], e - 1);
     } else {
-      big_add_shifted(A, atomicAdd(&ws->lo, 0ull), 149 - kDqFixShift);
-      big_add_shifted(A, atomicAdd(&ws->hi, 0ull), 149 - kDqFixShift + 64);
+      const unsigned long long lo = atomicAdd(&ws->lo, 0ull), hi = atomicAdd(&ws->hi, 0ull);
+      float m;
+      if (dq_round_fixed(lo, hi, static_cast<uint32_t>(nb), &m)) {
+        *offset = m;
+        return;
+      }
+      big_add_shifted(A, lo, 149 - kDqFixShift);
+      big_add_shifted(A, hi, 149 - kDqFixShift + 64);
     }
     *offset = big_round_mean(A, static_cast<uint32_t>(nb));
   }
@@ -207,6 +242,10 @@ __global__ void __launch_bounds__(kDqQuantThreads)
 dq_quant_kernel(const float* __restrict__ absmax, int64_t nb,
                 const float* __restrict__ offset, int8_t* __restrict__ absmax_q,
                 float* __restrict__ scale2) {
+  // Launched as a programmatic dependent of the fused quantize kernel, this
+  // waits here until that grid has completed and its writes (absmax, the
+  // mean) are visible; launched normally it returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
   const int64_t warp0 =

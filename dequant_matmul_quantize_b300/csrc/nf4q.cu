@@ -283,11 +283,28 @@ nf4q_status quantize_launch(const void* w, int32_t in_dtype, const nf4q_weight* 
 }
 
 // Second double-quant pass: int8 codes and per-256 scales from the mean.
-nf4q_status dq_quant_launch(const nf4q_weight* wq, int64_t nb, cudaStream_t s) {
+// `dependent`: launched as a programmatic dependent of the kernel before it
+// on the stream (which signals griddepcontrol.launch_dependents), so its
+// launch overlaps that kernel's tail.
+nf4q_status dq_quant_launch(const nf4q_weight* wq, int64_t nb, cudaStream_t s,
+                            bool dependent) {
   const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
   const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
-  dq_quant_kernel<<<g2, kDqQuantThreads, 0, s>>>(wq->absmax, nb, wq->offset, wq->absmax_q,
-                                                  wq->scale2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(g2));
+  cfg.blockDim = dim3(kDqQuantThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  const float* am = wq->absmax;
+  const float* off = wq->offset;
+  if (cudaLaunchKernelEx(&cfg, dq_quant_kernel, am, nb, off, wq->absmax_q, wq->scale2) !=
+      cudaSuccess)
+    return NF4Q_ERR_CUDA;
   return launch_status();
 }
 
@@ -297,7 +314,7 @@ nf4q_status dq_launch(const nf4q_weight* wq, int64_t nb, void* ws, cudaStream_t 
   dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb, static_cast<DqWorkspace*>(ws),
                                              wq->offset);
   if (cudaGetLastError() != cudaSuccess) return NF4Q_ERR_CUDA;
-  return dq_quant_launch(wq, nb, s);
+  return dq_quant_launch(wq, nb, s, false);
 }
 }  // namespace
 }  // namespace nf4q
@@ -354,7 +371,7 @@ nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight*
   if (!workspace || workspace_bytes < sizeof(DqWorkspace)) return NF4Q_ERR_WORKSPACE;
   if (!aligned16(workspace)) return NF4Q_ERR_ALIGNMENT;
   if ((st = quantize_launch(w, in_dtype, wq, workspace, s)) != NF4Q_OK) return st;
-  return dq_quant_launch(wq, nb, s);
+  return dq_quant_launch(wq, nb, s, true);
 }
 
 nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {

@@ -274,6 +274,9 @@ quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
     }
   }
   if constexpr (DQ) {
+    // the second double-quant pass may start launching (it waits for this
+    // grid to complete before it reads anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
     DqStats st;
     if ((threadIdx.x & 3) == 0) {
