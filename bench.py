@@ -139,6 +139,27 @@ def kernel_bytes(N, K, M=1):
     return b
 
 
+# DRAM bytes (read + write) per call of each phase of the step, averaged over
+# the three weights, from one ncu capture of this script (the launch list in
+# profiles/ncu_launches_llama7b_decode_step.md).  They hold only for the
+# kernel sources they were measured on: `traffic` is reported as null as soon
+# as the digest of csrc/ differs.
+MEASURED_TRAFFIC = {"csrc_digest": "7eba4a0c1e7f835f",
+                    "quantize_dq": 75606665, "dequantize": 36956774, "gemv": 18426197}
+
+
+def csrc_digest() -> str:
+    import hashlib
+    d = os.path.join(ROOT, "dequant_matmul_quantize_b300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 # ------------------------------------------------------------------ our path
 def run_ours(args):
     import torch
@@ -258,15 +279,22 @@ def run_ours(args):
     dom_ms = kern_ms[dom] / args.steps                  # per step
     launches_dom = 3
     achieved = (dom_bytes / launches_dom) / (dom_ms / launches_dom * 1e-3) / 1e9
+    traffic_ok = csrc_digest() == MEASURED_TRAFFIC["csrc_digest"]
     roofline = {"kernel": "nf4q_" + dom, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                 "peak_source": peaks["src"] + " HBM copy bandwidth",
-                "bytes_per_launch": dom_bytes // launches_dom, "traffic": None,
+                "bytes_per_launch": dom_bytes // launches_dom,
+                "traffic": MEASURED_TRAFFIC.get(dom) if traffic_ok else None,
+                "traffic_note": "DRAM read+write per call from the ncu launch list; writes "
+                                "still in L2 when the kernel ends are not counted",
                 "share_of_step": round(kern_ms[dom] / dev_ms, 3)}
     breakdown = {n: {"ms_per_step": round(kern_ms[n] / args.steps, 4),
                      "GB/s": round(sum(m["bytes"][n] for m in mats)
                                    / (kern_ms[n] / args.steps * 1e-3) / 1e9, 1),
-                     "share": round(kern_ms[n] / dev_ms, 3)} for n in names}
+                     "share": round(kern_ms[n] / dev_ms, 3),
+                     "bytes_per_call": sum(m["bytes"][n] for m in mats) // 3,
+                     "traffic_per_call": MEASURED_TRAFFIC.get(n) if traffic_ok else None}
+                 for n in names}
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup),

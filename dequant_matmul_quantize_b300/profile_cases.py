@@ -1,0 +1,88 @@
+"""Single workloads for profiling one kernel at a time (ncu / nsight).
+
+    python -m dequant_matmul_quantize_b300.profile_cases CASE [CASE ...]
+
+Each case builds its seeded synthetic input, runs the library call twice
+(a warm-up and the one to capture) and synchronizes.  Cases:
+
+    quant11008   nf4q_quantize_dq then nf4q_dequantize, 11008x4096 decode weight
+    gemv70b      nf4q_gemv M=1 on the 28672x8192 weight (NF4)
+    gemv4096     nf4q_gemv M=1 on the 4096x4096 decode weight
+    gemv70b_m16  nf4q_gemv M=16 on the 28672x8192 weight (NF4)
+    gemm2048     nf4q_gemm M=2048 on the 14336x4096 prefill weight
+
+Kernel launches per case are listed so a capture can be aimed with ncu's
+-k / -s / -c options.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def _run(case: str, torch, nq, synth) -> None:
+    L = nq.lib()
+    R = ctypes.byref
+    dev = torch.device("cuda", 0)
+    sp = torch.cuda.current_stream().cuda_stream
+
+    def ok(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: status {st}")
+
+    if case == "quant11008":
+        w, _ = synth.llama7b_decode(1, device=dev)
+        N, K = w.shape
+        qw = nq.QuantizedWeight.empty(N, K, device=dev)
+        s = qw.struct()
+        ws = nq.dq_workspace(N * K // 64, dev)
+        out = torch.empty_like(w)
+        for _ in range(2):
+            ok(L.nf4q_quantize_dq(w.data_ptr(), nq.IN_BF16, R(s), ws.data_ptr(), ws.numel(), sp),
+               "quantize_dq")
+            ok(L.nf4q_dequantize(R(s), out.data_ptr(), sp), "dequantize")
+    elif case in ("gemv70b", "gemv70b_m16"):
+        M = 16 if case.endswith("m16") else 1
+        qw = nq.quantize(synth.mlp70b_weight(device=dev))
+        s = qw.struct()
+        x = synth.mlp70b_x(M, device=dev)
+        y = torch.empty(M, qw.rows, dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            ok(L.nf4q_gemv(R(s), x.data_ptr(), M, y.data_ptr(), sp), "gemv")
+    elif case == "gemv4096":
+        w, x = synth.llama7b_decode(0, device=dev)
+        qw = nq.quantize(w)
+        s = qw.struct()
+        y = torch.empty(1, qw.rows, dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            ok(L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), sp), "gemv")
+    elif case == "gemm2048":
+        qw = nq.quantize(synth.prefill_weight(device=dev))
+        s = qw.struct()
+        x = synth.prefill_x(2048, device=dev)
+        y = torch.empty(2048, qw.rows, dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            ok(L.nf4q_gemm(R(s), x.data_ptr(), 2048, y.data_ptr(), sp), "gemm")
+    else:
+        raise SystemExit(f"unknown case {case!r}; see the module docstring")
+    torch.cuda.synchronize()
+
+
+def main(argv) -> None:
+    import torch
+    import dequant_matmul_quantize_b300 as nq
+    import synth
+    if not argv:
+        raise SystemExit(__doc__)
+    for case in argv:
+        _run(case, torch, nq, synth)
+    print("ok")
+
+
+if __name__ == "__main__":
+    main(sys.argv[1:])
