@@ -160,14 +160,36 @@ def csrc_digest() -> str:
     return h.hexdigest()[:16]
 
 
+# ------------------------------------------------------------------ ranks
+def rank_env():
+    """(rank, world size, local rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(v: float, world: int, dist=None, device=None) -> float:
+    """The largest v over all ranks (an all-reduce MAX); v itself on one rank."""
+    if world == 1:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank (one replica per GPU, weak scaling) moves
+    bytes_per_rank_step per step, and the job's step time is the slowest
+    rank's."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ our path
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
@@ -187,12 +209,8 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def slowest(v):
+        return max_over_ranks(v, world, dist, dev)
 
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -269,9 +287,9 @@ def run_ours(args):
             tot += dt
         step_ms.append(tot)
     dev_ms = sum(step_ms)
-    dev_ms_max = max_over_ranks(dev_ms)
+    dev_ms_max = slowest(dev_ms)
     ms_per_step = dev_ms_max / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(world, step_bytes, ms_per_step)
 
     # roofline of the kernel with the largest share of the step
     dom = max(kern_ms, key=kern_ms.get)
@@ -335,8 +353,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
-    result["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1),
+    e2e_ms = slowest(e0.elapsed_time(e1)) / e2e_steps
+    result["e2e"] = {"value": round(job_throughput(world, step_bytes, e2e_ms), 1),
                      "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                      "api": "C ABI via the ctypes binding, pinned host buffers"}
@@ -564,8 +582,7 @@ def cpu_baseline_sample():
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank, world, _ = rank_env()
     if rank != 0:
         return
     lim = _limit_threads()

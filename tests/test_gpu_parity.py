@@ -204,6 +204,24 @@ def test_quantize_dq_fused_matches_two_calls(code, dtype):
             assert_bits_equal(a[k], ref[k], f"{code} case {i} {k} vs oracle")
 
 
+@pytest.mark.parametrize("shape", [(40, 64 * 33), (512, 1024)])
+def test_dequantize_unaligned_fp32_scales(shape):
+    """Without double quantization the fp32 absmax only has to be 4-byte
+    aligned; a scale array that is not 16-byte aligned takes the direct-load
+    path of the dequantizer and must give the same bits."""
+    w = synth.normal_weight(*shape, 0.02, seed=shape[0])
+    qw = nq.quantize(w.cuda(), "nf4", double_quant=False)
+    ref = nq.dequantize(qw)
+    nb = qw.absmax.numel()
+    buf = torch.empty(nb + 4, dtype=torch.float32, device=qw.absmax.device)
+    moved = buf[1:1 + nb]
+    moved.copy_(qw.absmax)
+    qw2 = nq.QuantizedWeight(qw.packed, moved, None, None, None, qw.rows, qw.cols, "nf4", False)
+    out = nq.dequantize(qw2)
+    torch.cuda.synchronize()
+    assert_bits_equal(bf16_bits(out).ravel(), bf16_bits(ref).ravel(), "dequant unaligned scales")
+
+
 # ---------------------------------------------------------------- GEMV
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 12, 16])
 @pytest.mark.parametrize("shape", [(37, 320), (256, 1024), (129, 4160)])
