@@ -94,6 +94,35 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return r
 
 
+# compute dtypes (the dequantized weights, x and y): tutorial section 四,
+# bnb_4bit_compute_dtype; bf16 is the default
+DT_BF16 = 0
+DT_F16 = 1
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """fp16 bit patterns (uint16) -> float32 (exact widening)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> fp16 bit patterns, round to nearest, ties to even, with
+    overflow to infinity and gradual underflow (NumPy's IEEE conversion)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    with np.errstate(over="ignore"):
+        return x.astype(np.float16).view(np.uint16)
+
+
+def to_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    """float32 -> bit patterns of the compute dtype."""
+    return f32_to_bf16_bits(x) if dtype == DT_BF16 else f32_to_f16_bits(x)
+
+
+def from_bits(bits: np.ndarray, dtype: int) -> np.ndarray:
+    """Bit patterns of the compute dtype -> float32 (exact)."""
+    return bf16_bits_to_f32(bits) if dtype == DT_BF16 else f16_bits_to_f32(bits)
+
+
 def round_fraction_to_f32(v: Fraction) -> np.float32:
     """Nearest float32 to the exact rational ``v`` (ties to even mantissa)."""
     if v == 0:
@@ -339,14 +368,15 @@ def block_scales(absmax_q=None, scale2=None, offset=None, absmax=None,
 
 
 def dequantize(packed: np.ndarray, scales: np.ndarray, code: int = CODE_NF4,
-               blocksize: int = BLOCKSIZE) -> np.ndarray:
-    """bf16 weights (uint16 bit patterns): w_hat = bf16(fp32(code[idx] * s_b))
-    (tutorial section 3.4: weights stored in 4 bits, dequantized to bf16)."""
+               blocksize: int = BLOCKSIZE, dtype: int = DT_BF16) -> np.ndarray:
+    """Weights in the compute dtype (uint16 bit patterns):
+    w_hat = round(fp32(code[idx] * s_b)) to bf16 or fp16 (tutorial section
+    3.4: weights stored in 4 bits, dequantized to the compute dtype)."""
     idx = unpack_nibbles(packed)
     table = code_table(code)
     s = np.repeat(np.asarray(scales, dtype=np.float32), blocksize)
     prod = (table[idx] * s).astype(np.float32)
-    return f32_to_bf16_bits(prod)
+    return to_bits(prod, dtype)
 
 
 def quantize_full(w, code=CODE_NF4, double_quant_on=True):
@@ -363,18 +393,28 @@ def quantize_full(w, code=CODE_NF4, double_quant_on=True):
 
 
 # ------------------------------------------------------------------ matmul
-def matmul_ref(x_bits: np.ndarray, w_hat_bits: np.ndarray):
-    """y_ref = x . w_hat^T in fp64 from bf16 inputs (section 3.4: dequantize
-    to bf16, then an ordinary matmul), and the per-output error scale
-    sum_k |x_k * w_hat_k|.  x [M, K], w_hat [N, K] as bf16 bit patterns."""
-    x = bf16_bits_to_f32(x_bits).astype(np.float64)
-    w = bf16_bits_to_f32(w_hat_bits).astype(np.float64)
+def matmul_ref(x_bits: np.ndarray, w_hat_bits: np.ndarray, dtype: int = DT_BF16):
+    """y_ref = x . w_hat^T in fp64 from compute-dtype inputs (section 3.4:
+    dequantize to the compute dtype, then an ordinary matmul), and the
+    per-output error scale sum_k |x_k * w_hat_k|.  x [M, K], w_hat [N, K] as
+    bit patterns of the compute dtype."""
+    x = from_bits(x_bits, dtype).astype(np.float64)
+    w = from_bits(w_hat_bits, dtype).astype(np.float64)
     return x @ w.T, np.abs(x) @ np.abs(w).T
 
 
-def matmul_tolerance(y_ref: np.ndarray, bound: np.ndarray) -> np.ndarray:
-    """|y - y_ref| <= 2e-3 * sum_k |x_k w_hat_k| + one bf16 ulp of y_ref."""
-    return 2e-3 * bound + ulp_bf16(y_ref)
+def ulp_f16(v: np.ndarray) -> np.ndarray:
+    """Spacing of fp16 numbers at |v| (2^(e-10) for 2^e <= |v| < 2^(e+1),
+    2^-24 below the normal range)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a >= 2.0 ** -14, 2.0 ** (e - 10), 2.0 ** -24)
+
+
+def matmul_tolerance(y_ref: np.ndarray, bound: np.ndarray, dtype: int = DT_BF16) -> np.ndarray:
+    """|y - y_ref| <= 2e-3 * sum_k |x_k w_hat_k| + one ulp of y_ref in the
+    compute dtype."""
+    return 2e-3 * bound + (ulp_bf16(y_ref) if dtype == DT_BF16 else ulp_f16(y_ref))
 
 
 def bits_per_parameter(n: int, k: int, double_quant_on: bool = True) -> float:

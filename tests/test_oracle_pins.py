@@ -48,6 +48,83 @@ def test_bf16_widen_is_exact():
     assert same.all()
 
 
+# ------------------------------------------------------------ fp16 compute dtype
+def _f16_grid():
+    """Every finite fp16 value, ascending, as exact float64 with its bits:
+    built from the IEEE half format definition (sign, 5-bit exponent with
+    bias 15, 10-bit fraction; exponent 0 = subnormal), not from a cast."""
+    vals, bits = [], []
+    for e in range(31):
+        for f in range(1024):
+            v = (f / 1024.0) * 2.0 ** -14 if e == 0 else (1 + f / 1024.0) * 2.0 ** (e - 15)
+            vals.append(v); bits.append((e << 10) | f)
+    pos_v, pos_b = np.array(vals), np.array(bits, dtype=np.uint32)
+    v = np.concatenate([-pos_v[::-1][:-1], pos_v])          # drop -0
+    b = np.concatenate([(pos_b[::-1][:-1] | 0x8000), pos_b]).astype(np.uint16)
+    return v, b
+
+
+def _f16_nearest_even(x64: np.ndarray) -> np.ndarray:
+    """Brute force round-to-nearest-even onto the fp16 grid with overflow to
+    infinity at |x| >= 65520 (the midpoint past the largest finite value)."""
+    v, b = _f16_grid()
+    out = np.empty(x64.shape, dtype=np.uint16)
+    for i, x in enumerate(x64):
+        if abs(x) >= 65520.0:
+            out[i] = 0x7C00 | (0x8000 if x < 0 else 0)
+            continue
+        j = np.searchsorted(v, x)
+        cands = [k for k in (j - 1, j) if 0 <= k < len(v)]
+        d = [abs(v[k] - x) for k in cands]
+        best = min(d)
+        ks = [k for k, dd in zip(cands, d) if dd == best]
+        k = ks[0] if len(ks) == 1 else min(ks, key=lambda q: b[q] & 1)  # even mantissa
+        out[i] = b[k]
+        if out[i] == 0 and np.signbit(x):   # rounding to zero keeps the sign
+            out[i] = 0x8000
+    return out
+
+
+def test_f16_rounding_matches_brute_force_grid():
+    x = np.concatenate([
+        RNG.standard_normal(3000).astype(np.float32) * np.float32(100.0),
+        (RNG.standard_normal(1000) * 1e-5).astype(np.float32),          # subnormal range
+        np.array([65504.0, 65519.0, 65520.0, 65536.0, 1e6, -65520.0, 0.0, -0.0,
+                  2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 1.0 + 2.0 ** -11,
+                  1.0 + 3 * 2.0 ** -11], dtype=np.float32)])
+    # exact midpoints between neighbouring fp16 values (representable in fp32)
+    v, _ = _f16_grid()
+    mids = ((v[:-1] + v[1:]) / 2)[::37].astype(np.float32)
+    x = np.concatenate([x, mids])
+    got, want = o.f32_to_f16_bits(x), _f16_nearest_even(x.astype(np.float64))
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(repr(x[i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def test_f16_widen_is_exact():
+    v, b = _f16_grid()
+    assert np.array_equal(o.f16_bits_to_f32(b).astype(np.float64), v)
+
+
+def test_dequant_f16_closed_form():
+    # unit scale: w_hat is the code value rounded once to fp16
+    t = o.nf4_code_table()
+    packed = o.pack_nibbles(np.arange(16, dtype=np.uint8).repeat(4))
+    got = o.f16_bits_to_f32(o.dequantize(packed, np.ones(1, np.float32), dtype=o.DT_F16))
+    want = np.array([np.float16(float(c)) for c in t.repeat(4)], dtype=np.float32)
+    assert np.array_equal(got, want)
+    # a scale that overflows fp16 gives infinities, as IEEE rounding does
+    big = o.f16_bits_to_f32(o.dequantize(packed, np.full(1, 1e5, np.float32), dtype=o.DT_F16))
+    assert np.isinf(big[-1]) and big[-1] > 0 and big[28] == 0.0
+
+
+def test_ulp_f16_spacing():
+    v, b = _f16_grid()
+    pos = v[v > 0][:-1]
+    nxt = v[v > 0][1:]
+    assert np.array_equal(o.ulp_f16(pos), nxt - pos)
+
+
 # ------------------------------------------------------------ fma / rounding
 def _exact_f32_round(v: Fraction) -> np.float32:
     """Brute force: scan the float32 neighbourhood and pick the nearest,
@@ -454,4 +531,12 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         @ o.bf16_bits_to_f32(wb).astype(np.float64)[:, ::-1].T, None))
     with pytest.raises(AssertionError):
         test_matmul_ref_against_torch_and_one_hot()
+    monkeypatch.undo()
+    # (5) fp16 rounding by truncation instead of to nearest
+    monkeypatch.setattr(o, "f32_to_f16_bits", lambda x: np.asarray(
+        [np.float16(np.float32(v)) if abs(np.float16(np.float32(v))) <= abs(v) else
+         np.nextafter(np.float16(np.float32(v)), np.float16(0)) for v in np.asarray(x, np.float32)],
+        dtype=np.float16).view(np.uint16))
+    with pytest.raises(AssertionError):
+        test_f16_rounding_matches_brute_force_grid()
     monkeypatch.undo()
