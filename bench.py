@@ -457,6 +457,17 @@ def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
                           "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
                           "frac_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)})
         del qw
+    # fp16 compute dtype (NF4 codes, fp16 x and y)
+    qw = nq.quantize(w, "nf4", compute_dtype="f16")
+    for M in (1, 16):
+        x = synth.mlp70b_x(M, device=dev).to(torch.float16)
+        y = torch.empty(M, w.shape[0], dtype=torch.float16, device=dev)
+        ms = gemv_timed(qw, x, M, y)
+        b = kernel_bytes(*w.shape, M=M)["gemv"]
+        sweep.append({"code": "nf4", "compute_dtype": "f16", "M": M, "us": round(ms * 1e3, 2),
+                      "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                      "frac_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)})
+    del qw
     del w
     out["gemv_70b_mlp"] = {"workload": "28672x8192 bf16 N(0,0.015), rotating copies > L2",
                            "points": sweep}
@@ -487,7 +498,20 @@ def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
                     "us_dequant_plus_cublas": round(ms_two * 1e3, 1),
                     **({"us_gemv": round(ms_gemv * 1e3, 1)} if ms_gemv else {})})
         del deq
-    out["gemm"] = {"workload": "prefill 14336x4096 NF4 weight, X bf16 [M x 4096]",
+    # fp16 compute dtype at M = 2048 (fp16 X and Y, f16 tcgen05 MMA); the
+    # bf16 peak stands in for fp16's (same nominal dense rate)
+    qh = nq.quantize(w, "nf4", compute_dtype="f16")
+    sh = qh.struct()
+    M = 2048
+    xh = synth.prefill_x(M, device=dev).to(torch.float16)
+    yh = torch.empty(M, w.shape[0], dtype=torch.float16, device=dev)
+    ms = timed(lambda: L.nf4q_gemm(R(sh), xh.data_ptr(), M, yh.data_ptr(), sp))
+    tf = 2.0 * M * w.shape[0] * w.shape[1] / (ms * 1e-3) / 1e12
+    pts.append({"M": M, "compute_dtype": "f16", "us": round(ms * 1e3, 1),
+                "TFLOP/s": round(tf, 1), "frac_bf16_burst": round(tf / peaks["bf16"], 4)})
+    del qh, xh, yh
+    out["gemm"] = {"workload": "prefill 14336x4096 NF4 weight, X bf16 [M x 4096] (and one "
+                               "fp16 point)",
                    "points": pts, "peak_bf16_tflops": peaks["bf16"],
                    "peak_source": peaks["src"] + " cuBLAS bf16 burst"}
     del w, qw

@@ -25,7 +25,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libnf4q.so")
 
 CODES = {"nf4": 0, "fp4": 1}
-IN_F32, IN_BF16 = 0, 1
+IN_F32, IN_BF16, IN_F16 = 0, 1, 2
+DTYPES = {"bf16": 0, "f16": 1}          # compute dtype codes of nf4q_weight
 BLOCKSIZE, DQ_BLOCKSIZE = 64, 256
 GEMV_MAX_M = 16
 
@@ -56,6 +57,7 @@ class NF4QWeight(ctypes.Structure):
         ("dq_blocksize", ctypes.c_int32),
         ("code", ctypes.c_int32),
         ("double_quant", ctypes.c_int32),
+        ("compute_dtype", ctypes.c_int32),
     ]
 
 
@@ -150,16 +152,22 @@ class QuantizedWeight:
     cols: int
     code: str = "nf4"
     double_quant: bool = True
+    compute_dtype: str = "bf16"
 
     def struct(self) -> NF4QWeight:
         return NF4QWeight(_ptr(self.packed), _ptr(self.absmax_q), _ptr(self.absmax),
                           _ptr(self.scale2), _ptr(self.offset), self.rows, self.cols,
                           BLOCKSIZE, DQ_BLOCKSIZE, CODES[self.code],
-                          1 if self.double_quant else 0)
+                          1 if self.double_quant else 0, DTYPES[self.compute_dtype])
+
+    @property
+    def torch_dtype(self):
+        """torch dtype of the dequantized weights, x and y."""
+        return torch.bfloat16 if self.compute_dtype == "bf16" else torch.float16
 
     @staticmethod
     def empty(rows: int, cols: int, code: str = "nf4", double_quant: bool = True,
-              device=None) -> "QuantizedWeight":
+              device=None, compute_dtype: str = "bf16") -> "QuantizedWeight":
         device = device or torch.device("cuda", torch.cuda.current_device())
         pb, nb, nd = sizes(rows, cols)
         u8 = dict(dtype=torch.uint8, device=device)
@@ -169,14 +177,15 @@ class QuantizedWeight:
             absmax_q=torch.empty(max(nb, 1), dtype=torch.int8, device=device)[:nb],
             scale2=torch.empty(max(nd, 1), dtype=torch.float32, device=device)[:nd],
             offset=torch.empty(1, dtype=torch.float32, device=device),
-            rows=rows, cols=cols, code=code, double_quant=double_quant)
+            rows=rows, cols=cols, code=code, double_quant=double_quant,
+            compute_dtype=compute_dtype)
 
 
 # ------------------------------------------------------------------ ops
 def quantize_into(qw: QuantizedWeight, w: torch.Tensor, stream=None):
     """nf4q_quantize: writes qw.packed and qw.absmax from w (fp32 or bf16)."""
     assert w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols)
-    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16}[w.dtype]
+    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16, torch.float16: IN_F16}[w.dtype]
     s = qw.struct()
     _check("nf4q_quantize", lib().nf4q_quantize(_ptr(w), dt, ctypes.byref(s), _stream(stream)))
 
@@ -200,7 +209,7 @@ def quantize_dq_into(qw: QuantizedWeight, w: torch.Tensor,
                      workspace: Optional[torch.Tensor] = None, stream=None):
     """nf4q_quantize_dq: quantize and double-quantize w into qw in one call."""
     assert w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols)
-    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16}[w.dtype]
+    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16, torch.float16: IN_F16}[w.dtype]
     if workspace is None:
         workspace = dq_workspace(qw.absmax.numel(), qw.absmax.device)
     s = qw.struct()
@@ -209,10 +218,13 @@ def quantize_dq_into(qw: QuantizedWeight, w: torch.Tensor,
 
 
 def quantize(w: torch.Tensor, code: str = "nf4", double_quant: bool = True,
-             workspace: Optional[torch.Tensor] = None, stream=None) -> QuantizedWeight:
-    """Quantize a [rows x cols] fp32/bf16 CUDA weight (cols % 64 == 0)."""
+             workspace: Optional[torch.Tensor] = None, stream=None,
+             compute_dtype: str = "bf16") -> QuantizedWeight:
+    """Quantize a [rows x cols] fp32/bf16/fp16 CUDA weight (cols % 64 == 0);
+    `compute_dtype` ("bf16" or "f16") is the dtype it will be dequantized and
+    multiplied in."""
     rows, cols = w.shape
-    qw = QuantizedWeight.empty(rows, cols, code, double_quant, w.device)
+    qw = QuantizedWeight.empty(rows, cols, code, double_quant, w.device, compute_dtype)
     if double_quant:
         quantize_dq_into(qw, w, workspace, stream)
     else:
@@ -223,18 +235,18 @@ def quantize(w: torch.Tensor, code: str = "nf4", double_quant: bool = True,
 def dequantize(qw: QuantizedWeight, out: Optional[torch.Tensor] = None,
                stream=None) -> torch.Tensor:
     if out is None:
-        out = torch.empty(qw.rows, qw.cols, dtype=torch.bfloat16, device=qw.packed.device)
+        out = torch.empty(qw.rows, qw.cols, dtype=qw.torch_dtype, device=qw.packed.device)
     s = qw.struct()
     _check("nf4q_dequantize", lib().nf4q_dequantize(ctypes.byref(s), _ptr(out), _stream(stream)))
     return out
 
 
 def _mm(name: str, qw: QuantizedWeight, x: torch.Tensor, out, stream):
-    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    assert x.is_cuda and x.dtype == qw.torch_dtype and x.is_contiguous()
     assert x.shape[-1] == qw.cols
     M = x.shape[0]
     if out is None:
-        out = torch.empty(M, qw.rows, dtype=torch.bfloat16, device=x.device)
+        out = torch.empty(M, qw.rows, dtype=qw.torch_dtype, device=x.device)
     s = qw.struct()
     _check(name, getattr(lib(), name)(ctypes.byref(s), _ptr(x), M, _ptr(out), _stream(stream)))
     return out

@@ -76,6 +76,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Two float32 -> packed fp16x2 (lo in the low half), each rounded to nearest
+// even (overflow to infinity).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Compute dtypes: 0 = bf16, 1 = fp16 (nf4q_compute_dtype).
+template <int DT>
+__device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
+  return DT == 0 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+template <int DT>
+__device__ __forceinline__ uint16_t round_to_dt(float v) {
+  return static_cast<uint16_t>(pack_x2<DT>(v, 0.f) & 0xFFFFu);
+}
+
+__device__ __forceinline__ float f16lo_to_f32(uint32_t v) {
+  float r;
+  asm("{\n .reg .b16 h;\n mov.b32 {h, _}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(r) : "r"(v));
+  return r;
+}
+__device__ __forceinline__ float f16hi_to_f32(uint32_t v) {
+  float r;
+  asm("{\n .reg .b16 h;\n mov.b32 {_, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(r) : "r"(v));
+  return r;
+}
+
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) {
   return __uint_as_float(v << 16);
 }

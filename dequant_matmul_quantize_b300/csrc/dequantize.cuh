@@ -1,8 +1,9 @@
 // nf4_dequantize: packed 4-bit codes + (double-quantized) block scales ->
-// bf16 ("bitsandbytes tutorial", sec. 3.4: weights kept in 4 bits are
-// turned back into the 16-bit compute dtype before the matmul).
+// the compute dtype, bf16 or fp16 ("bitsandbytes tutorial", sec. 3.4: weights
+// kept in 4 bits are turned back into the 16-bit compute dtype before the
+// matmul; sec. 四: bnb_4bit_compute_dtype).
 //
-// w_hat = bf16_rn(fp32(code_value[code] * s_b)).  One lane owns one 64-block:
+// w_hat = round(fp32(code_value[code] * s_b)) to the compute dtype.  One lane owns one 64-block:
 // it reads the block's 32 packed bytes and its scale, builds the 16 values
 // w_hat_j of the block once as register byte tables (the GEMV's lookup,
 // lut.cuh), and turns each 32-bit word of codes into four bf16x2 registers
@@ -27,7 +28,7 @@ constexpr size_t kDequantSmemBytes = 1024 + 2 * kDequantWarps * kDequantTileByte
 constexpr int kDequantCtasPerSm = 3;  // 65 KB of staging each
 
 // Output tensor map: [n_blocks rows][64 bf16], box {64, 32}, 128-byte swizzle.
-template <int CODE>
+template <int CODE, int DT>
 __global__ void __launch_bounds__(kDequantThreads)
 dequantize_kernel(const uint4* __restrict__ packed, ScaleView sv,
                   const __grid_constant__ CUtensorMap tmap_out, int64_t n_blocks,
@@ -50,7 +51,7 @@ dequantize_kernel(const uint4* __restrict__ packed, ScaleView sv,
       s = block_scale(sv, b);
     }
     RowTable<CODE> T;
-    build_table<CODE>(T, s, C);
+    build_table<CODE, DT>(T, s, C);
     const uint32_t buf = bufs + parity * kDequantTileBytes;
     // the store issued from this buffer two tiles ago must have read it
     if (lane == 0) bulk_wait_read<1>();

@@ -78,9 +78,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22,
 // M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and
+// B both bf16 (DT 0) or both fp16 (DT 1), K-major, N >> 3 and M >> 4.
+template <int DT>
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+  return (1u << 4) | ((DT == 0 ? 1u : 0u) << 7) | ((DT == 0 ? 1u : 0u) << 10) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -113,7 +116,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // ------------------------------------------------------------ the kernel
-template <int CODE, int BN>
+template <int CODE, int BN, int DT>
 __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
             const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
@@ -190,7 +193,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(kGemmBM, BN);
+      constexpr uint32_t idesc = make_idesc<DT>(kGemmBM, BN);
       for (int kt = 0; kt < KT; ++kt) {
         const int sa = kt % SA, sb = kt % SB;
         if (!mbar_wait(full_bar(sa), (kt / SA) & 1, abort)) break;
@@ -265,7 +268,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
         sc = row_ok ? __ldg(sv.absmax + row_block0 + kt) : 0.f;
       }
       RowTable<CODE> T;
-      build_table<CODE>(T, sc, C);
+      build_table<CODE, DT>(T, sc, C);
       // B slot sb is free once the MMAs of the previous round on it are done
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(bempty_bar(sb), ((kt / SB) & 1) ^ 1, abort) &&
                                        mbar_wait(full_bar(sa), (kt / SA) & 1, abort)))
@@ -308,19 +311,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-              o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-              o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-              o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+              o.x = pack_x2<DT>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+              o.y = pack_x2<DT>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+              o.z = pack_x2<DT>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+              o.w = pack_x2<DT>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
               *reinterpret_cast<uint4*>(yrow + col + 8 * j) = o;
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              if (j < ncols) {
-                const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
-                yrow[col + j] = *reinterpret_cast<const uint16_t*>(&b);
-              }
+              if (j < ncols) yrow[col + j] = round_to_dt<DT>(__uint_as_float(v[j]));
             }
           }
         }
@@ -362,7 +362,7 @@ inline int gemm_pick_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-template <int CODE, int BN>
+template <int CODE, int BN, int DT>
 inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, const ScaleView& sv,
                                   const CodeValues& C, int64_t M, void* Y, cudaStream_t stream) {
   using Cfg = GemmCfg<BN>;
@@ -381,29 +381,29 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel<CODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_kernel<CODE, BN, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::kSmem)) != cudaSuccess)
       return NF4Q_ERR_CUDA;
     attr_set[dev] = true;
   }
   dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
             static_cast<unsigned>((M + 2 * kGemmBM - 1) / (2 * kGemmBM)));
-  gemm_kernel<CODE, BN><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(
+  gemm_kernel<CODE, BN, DT><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(
       tx, tw, sv, static_cast<uint16_t*>(Y), static_cast<int>(M), static_cast<int>(N),
       static_cast<int>(K), C);
   return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
 }
 
-template <int CODE>
+template <int CODE, int DT>
 inline nf4q_status gemm_launch_code(const CUtensorMap& tx, const nf4q_weight* wq,
                                     const ScaleView& sv, const CodeValues& C, int64_t M, void* Y,
                                     cudaStream_t stream, int bn) {
   switch (bn) {
-    case 224: return gemm_launch_bn<CODE, 224>(tx, wq, sv, C, M, Y, stream);
-    case 192: return gemm_launch_bn<CODE, 192>(tx, wq, sv, C, M, Y, stream);
-    case 160: return gemm_launch_bn<CODE, 160>(tx, wq, sv, C, M, Y, stream);
-    case 128: return gemm_launch_bn<CODE, 128>(tx, wq, sv, C, M, Y, stream);
-    default: return gemm_launch_bn<CODE, 256>(tx, wq, sv, C, M, Y, stream);
+    case 224: return gemm_launch_bn<CODE, 224, DT>(tx, wq, sv, C, M, Y, stream);
+    case 192: return gemm_launch_bn<CODE, 192, DT>(tx, wq, sv, C, M, Y, stream);
+    case 160: return gemm_launch_bn<CODE, 160, DT>(tx, wq, sv, C, M, Y, stream);
+    case 128: return gemm_launch_bn<CODE, 128, DT>(tx, wq, sv, C, M, Y, stream);
+    default: return gemm_launch_bn<CODE, 256, DT>(tx, wq, sv, C, M, Y, stream);
   }
 }
 
@@ -420,13 +420,18 @@ inline nf4q_status gemm_launch(const nf4q_weight* wq, const ScaleView& sv,
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   cuuint32_t box[2] = {kGemmBK, kGemmBM};
   cuuint32_t es[2] = {1, 1};
-  if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box,
+  const int dt = wq->compute_dtype;
+  if (enc(&tx, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+          const_cast<void*>(X), dims, strides, box,
           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return NF4Q_ERR_CUDA;
   const int bn = gemm_pick_bn(M, N, sms);
-  return wq->code == 0 ? gemm_launch_code<0>(tx, wq, sv, C, M, Y, stream, bn)
-                       : gemm_launch_code<1>(tx, wq, sv, C, M, Y, stream, bn);
+  if (dt == 0)
+    return wq->code == 0 ? gemm_launch_code<0, 0>(tx, wq, sv, C, M, Y, stream, bn)
+                         : gemm_launch_code<1, 0>(tx, wq, sv, C, M, Y, stream, bn);
+  return wq->code == 0 ? gemm_launch_code<0, 1>(tx, wq, sv, C, M, Y, stream, bn)
+                       : gemm_launch_code<1, 1>(tx, wq, sv, C, M, Y, stream, bn);
 }
 
 }  // namespace nf4q

@@ -5,7 +5,7 @@
 // At M = 1 a B300 must turn ~45 packed weights per SM clock into bf16 to keep
 // up with HBM, i.e. under three instructions per weight, and at M = 16 the
 // CUDA cores could not even do the FMAs.  So the contraction runs on the
-// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with the
+// tensor cores (mma.sync m16n8k16, bf16 or fp16 in, fp32 accumulate) with the
 // weights as the 16-row A operand and x as the 8-column B operand, and the
 // per-weight work is a register table lookup:
 //   * For each (row, 64-block) the lane that owns it builds the 16 products
@@ -48,14 +48,22 @@ constexpr int kGemvMinCtasPerSm = 4;
 constexpr int kGemvMaxSplit = 8;    // CTAs of a cluster splitting K (portable limit)
 constexpr int kGemvCtrlBytes = 128;  // mbarriers and counters
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
-      "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// d += A (16x16) . B (16x8), bf16 (DT 0) or fp16 (DT 1) operands, fp32 accumulate
+template <int DT>
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  if (DT == 0)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -95,7 +103,7 @@ inline size_t gemv_smem_bytes(int R, int NT, int stages, int split) {
 
 // Launch: grid = tiles * split CTAs of 128 threads, cluster (split, 1, 1);
 // `per` chunks per CTA, `stages` ring stages (<= per, <= kGemvMaxStages).
-template <int CODE, int NT, int R>
+template <int CODE, int NT, int R, int DT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
                 const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int N, int K, int M,
@@ -197,8 +205,8 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
     RowTable<CODE> T[R][2];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      build_table<CODE>(T[r][0], scur[r][0], C);
-      build_table<CODE>(T[r][1], scur[r][1], C);
+      build_table<CODE, DT>(T[r][0], scur[r][0], C);
+      build_table<CODE, DT>(T[r][1], scur[r][1], C);
     }
     const bool in_k = blk < kblocks;
     // x of this lane's block; blocks past K read block 0 (their weights are zero)
@@ -250,8 +258,8 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
             for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
-                mma_bf16_16816(acc[r][nt], ra[2 * h], rb[2 * h], ra[2 * h + 1], rb[2 * h + 1],
-                               xb[nt][2 * h], xb[nt][2 * h + 1]);
+                mma_16816<DT>(acc[r][nt], ra[2 * h], rb[2 * h], ra[2 * h + 1], rb[2 * h + 1],
+                              xb[nt][2 * h], xb[nt][2 * h + 1]);
           }
         }
       }
@@ -294,10 +302,7 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
     // d0,d1: row g, cols 2t, 2t+1; d2,d3: row g+8
     const int row = row0 + 16 * r + (ln >> 2) + (i < 2 ? 0 : 8);
     const int col = 8 * nt + 2 * (ln & 3) + (i & 1);
-    if (row < N && col < M) {
-      const __nv_bfloat16 b = __float2bfloat16_rn(v);
-      y[static_cast<int64_t>(col) * N + row] = *reinterpret_cast<const uint16_t*>(&b);
-    }
+    if (row < N && col < M) y[static_cast<int64_t>(col) * N + row] = round_to_dt<DT>(v);
   };
   for (int item = threadIdx.x; item < kItems; item += kGemvWarps * 32) {
     float v = 0.f;

@@ -1,4 +1,5 @@
-// Exact bf16 dequantization of packed 4-bit codes with register tables.
+// Exact bf16 (or fp16) dequantization of packed 4-bit codes with register
+// tables.
 //
 // For one (row, 64-block) the 16 values w_hat_j = bf16(fp32(code_j * s_b))
 // - bit for bit what nf4_dequantize writes ("bitsandbytes tutorial", sec.
@@ -42,7 +43,7 @@ struct RowTable {
   uint32_t L[CODE == 0 ? 4 : 2];
 };
 
-template <int CODE>
+template <int CODE, int DT = 0>
 __device__ __forceinline__ void build_table(RowTable<CODE>& T, float s, const CodeValues& C) {
   uint64_t ss;
   asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
@@ -50,11 +51,18 @@ __device__ __forceinline__ void build_table(RowTable<CODE>& T, float s, const Co
 #pragma unroll
   for (int i = 0; i < (CODE == 0 ? 4 : 2); ++i) {
     const uint64_t d0 = mul2_rn(cv[2 * i], ss), d1 = mul2_rn(cv[2 * i + 1], ss);
-    uint32_t p0, p1;  // bf16x2 of codes 4i, 4i+1 and 4i+2, 4i+3
-    asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.bf16x2.f32 %0, b, a;\n}"
-        : "=r"(p0) : "l"(d0));
-    asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.bf16x2.f32 %0, b, a;\n}"
-        : "=r"(p1) : "l"(d1));
+    uint32_t p0, p1;  // bf16x2 (fp16x2) of codes 4i, 4i+1 and 4i+2, 4i+3
+    if (DT == 0) {
+      asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.bf16x2.f32 %0, b, a;\n}"
+          : "=r"(p0) : "l"(d0));
+      asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.bf16x2.f32 %0, b, a;\n}"
+          : "=r"(p1) : "l"(d1));
+    } else {
+      asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.f16x2.f32 %0, b, a;\n}"
+          : "=r"(p0) : "l"(d0));
+      asm("{\n .reg .f32 a, b;\n mov.b64 {a, b}, %1;\n cvt.rn.f16x2.f32 %0, b, a;\n}"
+          : "=r"(p1) : "l"(d1));
+    }
     T.H[i] = prmt(p0, p1, 0x7531);
     T.L[i] = prmt(p0, p1, 0x6420);
   }

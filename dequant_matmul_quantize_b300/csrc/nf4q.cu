@@ -61,6 +61,8 @@ nf4q_status check_shape(const nf4q_weight* wq) {
   if (wq->code != NF4Q_CODE_NF4 && wq->code != NF4Q_CODE_FP4)
     return NF4Q_ERR_INVALID_ARG;
   if (wq->double_quant != 0 && wq->double_quant != 1) return NF4Q_ERR_INVALID_ARG;
+  if (wq->compute_dtype != NF4Q_DT_BF16 && wq->compute_dtype != NF4Q_DT_F16)
+    return NF4Q_ERR_INVALID_ARG;
   // n_b must fit the 32-bit divisor of the exact mean
   if (wq->rows > 0 && wq->cols > 0 &&
       wq->rows > (static_cast<int64_t>(0x7FFFFFFF) * kBlock) / wq->cols)
@@ -83,12 +85,17 @@ nf4q_status check_scales(const nf4q_weight* wq) {
   return NF4Q_OK;
 }
 
-// The GEMV instantiations: code (NF4, FP4) x (NT, R) in {(1, 1), (2, 2)}.
+// The GEMV instantiations: code (NF4, FP4) x (NT, R) in {(1, 1), (2, 2)} x
+// compute dtype (bf16, fp16).
 using GemvKernelFn = void (*)(CUtensorMap, ScaleView, const uint16_t*, uint16_t*, int, int, int,
                               int, int, CodeValues);
-GemvKernelFn gemv_kernel(int code, int NT) {
-  if (code == 0) return NT == 1 ? gemv_mma_kernel<0, 1, 1> : gemv_mma_kernel<0, 2, 2>;
-  return NT == 1 ? gemv_mma_kernel<1, 1, 1> : gemv_mma_kernel<1, 2, 2>;
+template <int DT>
+GemvKernelFn gemv_kernel_dt(int code, int NT) {
+  if (code == 0) return NT == 1 ? gemv_mma_kernel<0, 1, 1, DT> : gemv_mma_kernel<0, 2, 2, DT>;
+  return NT == 1 ? gemv_mma_kernel<1, 1, 1, DT> : gemv_mma_kernel<1, 2, 2, DT>;
+}
+GemvKernelFn gemv_kernel(int code, int NT, int dt) {
+  return dt == 0 ? gemv_kernel_dt<0>(code, NT) : gemv_kernel_dt<1>(code, NT);
 }
 
 // Opt the GEMV kernels in to their largest dynamic shared memory (once per
@@ -103,9 +110,10 @@ bool gemv_attr_ready() {
   const int bytes = static_cast<int>(gemv_smem_bytes(2, 2, kGemvMaxStages, kGemvMaxSplit));
   for (int code = 0; code < 2; ++code)
     for (int nt = 1; nt <= 2; ++nt)
-      if (cudaFuncSetAttribute(gemv_kernel(code, nt), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               bytes) != cudaSuccess)
-        return false;
+      for (int dt = 0; dt < 2; ++dt)
+        if (cudaFuncSetAttribute(gemv_kernel(code, nt, dt),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+          return false;
   done[dev] = true;
   return true;
 }
@@ -119,22 +127,26 @@ bool dequantize_attr_ready() {
   if (done[dev]) return true;
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
   const int b = static_cast<int>(kDequantSmemBytes);
-  done[dev] = cudaFuncSetAttribute(dequantize_kernel<0>, A, b) == cudaSuccess &&
-              cudaFuncSetAttribute(dequantize_kernel<1>, A, b) == cudaSuccess;
+  done[dev] = cudaFuncSetAttribute(dequantize_kernel<0, 0>, A, b) == cudaSuccess &&
+              cudaFuncSetAttribute(dequantize_kernel<1, 0>, A, b) == cudaSuccess &&
+              cudaFuncSetAttribute(dequantize_kernel<0, 1>, A, b) == cudaSuccess &&
+              cudaFuncSetAttribute(dequantize_kernel<1, 1>, A, b) == cudaSuccess;
   return done[dev];
 }
 
 using QuantKernelFn = void (*)(const void*, uint2*, float*, int64_t, QuantParams,
                                DqWorkspace*, float*);
 
-// The quantize instantiation for a code, input type and fused double-quant pass.
-QuantKernelFn quantize_kernel_for(int code, int bf16, int dq) {
-  if (code == 0) {
-    if (bf16) return dq ? quantize_kernel<0, true, true> : quantize_kernel<0, true, false>;
-    return dq ? quantize_kernel<0, false, true> : quantize_kernel<0, false, false>;
-  }
-  if (bf16) return dq ? quantize_kernel<1, true, true> : quantize_kernel<1, true, false>;
-  return dq ? quantize_kernel<1, false, true> : quantize_kernel<1, false, false>;
+// The quantize instantiation for a code, input dtype (nf4q_in_dtype) and
+// fused double-quant pass.
+template <int CODE>
+QuantKernelFn quantize_kernel_code(int in, int dq) {
+  if (in == 1) return dq ? quantize_kernel<CODE, 1, true> : quantize_kernel<CODE, 1, false>;
+  if (in == 2) return dq ? quantize_kernel<CODE, 2, true> : quantize_kernel<CODE, 2, false>;
+  return dq ? quantize_kernel<CODE, 0, true> : quantize_kernel<CODE, 0, false>;
+}
+QuantKernelFn quantize_kernel_for(int code, int in, int dq) {
+  return code == 0 ? quantize_kernel_code<0>(in, dq) : quantize_kernel_code<1>(in, dq);
 }
 
 // Opt the quantize kernels in to their dynamic shared memory (once per device).
@@ -146,11 +158,11 @@ bool quantize_attr_ready() {
   const int b0 = static_cast<int>(quantize_smem_bytes(0)), b1 = static_cast<int>(quantize_smem_bytes(1));
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
   bool ok = true;
-  for (int k = 0; k < 8; ++k) {
-    const int code = k >> 2;
-    ok = ok && cudaFuncSetAttribute(quantize_kernel_for(code, (k >> 1) & 1, k & 1), A,
-                                    code == 0 ? b0 : b1) == cudaSuccess;
-  }
+  for (int code = 0; code < 2; ++code)
+    for (int in = 0; in < 3; ++in)
+      for (int dq = 0; dq < 2; ++dq)
+        ok = ok && cudaFuncSetAttribute(quantize_kernel_for(code, in, dq), A,
+                                        code == 0 ? b0 : b1) == cudaSuccess;
   done[dev] = ok;
   return ok;
 }
@@ -275,7 +287,7 @@ nf4q_status quantize_launch(const void* w, int32_t in_dtype, const nf4q_weight* 
   const int64_t grid = grid_for(n_units, kQuantThreads,
                                 static_cast<int64_t>(sm_count()) * quantize_ctas_per_sm(c));
   if (ws && cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
-  quantize_kernel_for(c, in_dtype == NF4Q_IN_BF16, ws != nullptr)<<<grid, kQuantThreads,
+  quantize_kernel_for(c, in_dtype, ws != nullptr)<<<grid, kQuantThreads,
                                                                     quantize_smem_bytes(c), s>>>(
       w, reinterpret_cast<uint2*>(wq->packed), wq->absmax, n_units, P,
       static_cast<DqWorkspace*>(ws), wq->offset);
@@ -325,7 +337,8 @@ nf4q_status nf4q_quantize(const void* w, int32_t in_dtype, const nf4q_weight* wq
                           void* stream) {
   nf4q_status st = check_shape(wq);
   if (st != NF4Q_OK) return st;
-  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16) return NF4Q_ERR_INVALID_ARG;
+  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16 && in_dtype != NF4Q_IN_F16)
+    return NF4Q_ERR_INVALID_ARG;
   if (wq->rows * wq->cols == 0) return NF4Q_OK;
   return quantize_launch(w, in_dtype, wq, nullptr, static_cast<cudaStream_t>(stream));
 }
@@ -358,7 +371,8 @@ nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight*
                              void* workspace, size_t workspace_bytes, void* stream) {
   nf4q_status st = check_shape(wq);
   if (st != NF4Q_OK) return st;
-  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16) return NF4Q_ERR_INVALID_ARG;
+  if (in_dtype != NF4Q_IN_F32 && in_dtype != NF4Q_IN_BF16 && in_dtype != NF4Q_IN_F16)
+    return NF4Q_ERR_INVALID_ARG;
   if (wq->double_quant != 1) return NF4Q_ERR_INVALID_ARG;
   if (!wq->absmax_q || !wq->scale2 || !wq->offset) return NF4Q_ERR_INVALID_ARG;
   if (!aligned4(wq->offset) || !aligned4(wq->scale2)) return NF4Q_ERR_ALIGNMENT;
@@ -393,7 +407,7 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kBlock * 2)};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlock), 32};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, es,
+    if (enc(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, out, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return NF4Q_ERR_CUDA;
@@ -403,12 +417,12 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
                                 static_cast<int64_t>(sm_count()) * kDequantCtasPerSm);
   const uint4* pk = reinterpret_cast<const uint4*>(wq->packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (wq->code == NF4Q_CODE_NF4)
-    dequantize_kernel<0><<<grid, kDequantThreads, kDequantSmemBytes, s>>>(
-        pk, scale_view(wq), tout, n_blocks, code_values(wq->code));
-  else
-    dequantize_kernel<1><<<grid, kDequantThreads, kDequantSmemBytes, s>>>(
-        pk, scale_view(wq), tout, n_blocks, code_values(wq->code));
+  using DequantFn = void (*)(const uint4*, ScaleView, CUtensorMap, int64_t, CodeValues);
+  const DequantFn k = wq->compute_dtype == NF4Q_DT_BF16
+      ? (wq->code == NF4Q_CODE_NF4 ? dequantize_kernel<0, 0> : dequantize_kernel<1, 0>)
+      : (wq->code == NF4Q_CODE_NF4 ? dequantize_kernel<0, 1> : dequantize_kernel<1, 1>);
+  k<<<grid, kDequantThreads, kDequantSmemBytes, s>>>(pk, scale_view(wq), tout, n_blocks,
+                                                     code_values(wq->code));
   return launch_status();
 }
 
@@ -478,7 +492,7 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   uint16_t* yp = static_cast<uint16_t*>(y);
   const ScaleView sv = scale_view(wq);
   const CodeValues C = code_values(wq->code);
-  if (cudaLaunchKernelEx(&cfg, gemv_kernel(code, NT), tw, sv, xp, yp, N, K, static_cast<int>(M),
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel(code, NT, wq->compute_dtype), tw, sv, xp, yp, N, K, static_cast<int>(M),
                          per, stages, C) != cudaSuccess)
     return NF4Q_ERR_CUDA;
   return launch_status();

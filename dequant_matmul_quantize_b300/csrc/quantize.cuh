@@ -107,15 +107,26 @@ __device__ __forceinline__ constexpr int nib_shift(int i) {
   return 8 * (i >> 1) + ((i & 1) ? 0 : 4);
 }
 
-template <bool BF16IN>
+// Widening of the two 16-bit values of a word: IN = 1 bf16, 2 fp16 (exact).
+template <int IN>
+__device__ __forceinline__ float lo16_to_f32(uint32_t v) {
+  return IN == 1 ? bf16lo_to_f32(v) : f16lo_to_f32(v);
+}
+template <int IN>
+__device__ __forceinline__ float hi16_to_f32(uint32_t v) {
+  return IN == 1 ? bf16hi_to_f32(v) : f16hi_to_f32(v);
+}
+
+// Input dtype IN: 0 fp32, 1 bf16, 2 fp16 (nf4q_in_dtype).
+template <int IN>
 __device__ __forceinline__ void load_unit(const void* base, int64_t unit,
                                           float (&v)[8]) {
-  if (BF16IN) {
+  if (IN != 0) {
     const uint4 r = ld_stream_u4(static_cast<const uint16_t*>(base) + unit * 8);
-    v[0] = bf16lo_to_f32(r.x); v[1] = bf16hi_to_f32(r.x);
-    v[2] = bf16lo_to_f32(r.y); v[3] = bf16hi_to_f32(r.y);
-    v[4] = bf16lo_to_f32(r.z); v[5] = bf16hi_to_f32(r.z);
-    v[6] = bf16lo_to_f32(r.w); v[7] = bf16hi_to_f32(r.w);
+    v[0] = lo16_to_f32<IN>(r.x); v[1] = hi16_to_f32<IN>(r.x);
+    v[2] = lo16_to_f32<IN>(r.y); v[3] = hi16_to_f32<IN>(r.y);
+    v[4] = lo16_to_f32<IN>(r.z); v[5] = hi16_to_f32<IN>(r.z);
+    v[6] = lo16_to_f32<IN>(r.w); v[7] = hi16_to_f32<IN>(r.w);
   } else {
     const float* p = static_cast<const float*>(base) + unit * 8;
     const uint4 r0 = ld_stream_u4(p);
@@ -128,25 +139,25 @@ __device__ __forceinline__ void load_unit(const void* base, int64_t unit,
 }
 
 // Raw 16-byte loads of the 16 elements of unit `unit` (zeros if !live).
-template <bool BF16IN>
+template <int IN>
 __device__ __forceinline__ void load_raw(const void* base, int64_t unit, bool live,
-                                         uint4 (&raw)[BF16IN ? 2 : 4]) {
+                                         uint4 (&raw)[IN != 0 ? 2 : 4]) {
 #pragma unroll
-  for (int i = 0; i < (BF16IN ? 2 : 4); ++i)
-    raw[i] = live ? ld_stream_u4(static_cast<const uint4*>(base) + unit * (BF16IN ? 2 : 4) + i)
+  for (int i = 0; i < (IN != 0 ? 2 : 4); ++i)
+    raw[i] = live ? ld_stream_u4(static_cast<const uint4*>(base) + unit * (IN != 0 ? 2 : 4) + i)
                   : make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <bool BF16IN>
-__device__ __forceinline__ void unpack_raw(const uint4 (&raw)[BF16IN ? 2 : 4], float (&v)[16]) {
+template <int IN>
+__device__ __forceinline__ void unpack_raw(const uint4 (&raw)[IN != 0 ? 2 : 4], float (&v)[16]) {
 #pragma unroll
-  for (int i = 0; i < (BF16IN ? 2 : 4); ++i) {
+  for (int i = 0; i < (IN != 0 ? 2 : 4); ++i) {
     const uint32_t q[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      if (BF16IN) {
-        v[8 * i + 2 * j] = bf16lo_to_f32(q[j]);
-        v[8 * i + 2 * j + 1] = bf16hi_to_f32(q[j]);
+      if (IN != 0) {
+        v[8 * i + 2 * j] = lo16_to_f32<IN>(q[j]);
+        v[8 * i + 2 * j + 1] = hi16_to_f32<IN>(q[j]);
       } else {
         v[4 * i + j] = __uint_as_float(q[j]);
       }
@@ -157,11 +168,11 @@ __device__ __forceinline__ void unpack_raw(const uint4 (&raw)[BF16IN ? 2 : 4], f
 // The exact rule for the word (8 elements) `word` of the weight, reading
 // its elements again (rare: only words with a value near a decision point
 // or blocks with an extreme scale come here).
-template <int CODE, bool BF16IN>
+template <int CODE, int IN>
 __device__ __noinline__ uint32_t encode_word_exact(const void* w, int64_t word, float a,
                                                    const QuantParams& P) {
   float v[8];
-  load_unit<BF16IN>(w, word, v);
+  load_unit<IN>(w, word, v);
   uint32_t out = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) out |= code_exact<CODE>(v[i], a, P) << nib_shift(i);
@@ -179,7 +190,7 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 // DQ: also the first pass of double quantization - the absmax values are
 // summed exactly into `ws` and the last CTA writes their mean to `offset`
 // (double_quant.cuh).
-template <int CODE, bool BF16IN, bool DQ>
+template <int CODE, int IN, bool DQ>
 __global__ void __launch_bounds__(kQuantThreads, 2)
 quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
                 float* __restrict__ absmax, int64_t n_units,
@@ -209,15 +220,15 @@ quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
 
   // The raw input of the next unit is loaded before the current one is
   // encoded, which doubles the bytes each lane keeps in flight.
-  constexpr int kRaw = BF16IN ? 2 : 4;  // 16-byte loads per unit
+  constexpr int kRaw = IN != 0 ? 2 : 4;  // 16-byte loads per unit
   uint4 nxt[kRaw];
   int64_t unit = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  load_raw<BF16IN>(w, unit, unit < n_units, nxt);
+  load_raw<IN>(w, unit, unit < n_units, nxt);
   for (; unit - lane < n_units; unit += nthreads) {
     const bool live = unit < n_units;
     float v[16];
-    unpack_raw<BF16IN>(nxt, v);
-    load_raw<BF16IN>(w, unit + nthreads, unit + nthreads < n_units, nxt);
+    unpack_raw<IN>(nxt, v);
+    load_raw<IN>(w, unit + nthreads, unit + nthreads < n_units, nxt);
     float a = fabsf(v[0]);
 #pragma unroll
     for (int i = 1; i < 16; ++i) a = max_nan(a, fabsf(v[i]));
@@ -255,7 +266,7 @@ quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
     if (live) {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        if (near[h] <= 1.0f || !ok) word[h] = encode_word_exact<CODE, BF16IN>(w, 2 * unit + h, a, P);
+        if (near[h] <= 1.0f || !ok) word[h] = encode_word_exact<CODE, IN>(w, 2 * unit + h, a, P);
       packed[unit] = make_uint2(word[0], word[1]);
       if ((lane & 3u) == 0u) {
         absmax[unit >> 2] = a;

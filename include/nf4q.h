@@ -71,7 +71,12 @@ typedef enum {
 } nf4q_status;
 
 typedef enum { NF4Q_CODE_NF4 = 0, NF4Q_CODE_FP4 = 1 } nf4q_code;
-typedef enum { NF4Q_IN_F32 = 0, NF4Q_IN_BF16 = 1 } nf4q_in_dtype;
+/* dtype of the weight given to nf4q_quantize / nf4q_quantize_dq */
+typedef enum { NF4Q_IN_F32 = 0, NF4Q_IN_BF16 = 1, NF4Q_IN_F16 = 2 } nf4q_in_dtype;
+/* Compute dtype (tutorial sec. 四, bnb_4bit_compute_dtype): the type of the
+ * dequantized weights, of x and of y.  w_hat = round(fp32(code_value * s_b))
+ * to this type (nearest, ties to even; fp16 overflows to infinity). */
+typedef enum { NF4Q_DT_BF16 = 0, NF4Q_DT_F16 = 1 } nf4q_compute_dtype;
 
 /* Views into caller-owned device buffers describing one quantized weight. */
 typedef struct {
@@ -88,6 +93,9 @@ typedef struct {
   int32_t code;         /* nf4q_code                                        */
   int32_t double_quant; /* 1: dequantizers use absmax_q/scale2/offset;
                            0: they use the fp32 absmax                      */
+  int32_t compute_dtype; /* nf4q_compute_dtype of nf4q_dequantize's output
+                            and of x / y of nf4q_gemv, _gemm, _matmul;
+                            0 (bf16) for callers that zero the struct       */
 } nf4q_weight;
 
 /* Library version, (major << 16) | minor. */
@@ -117,8 +125,8 @@ nf4q_status nf4q_thresholds(int32_t code, float* out, int32_t* count);
 
 /* Blockwise quantization (tutorial sec. 2.3 absmax, sec. 3.2 NF4; FP4 per the
  * introduction page, sec. 一 item 7).
- *   w      device, [rows x cols] row-major, fp32 or bf16 per `in_dtype`,
- *          16-byte aligned.  Values must be finite.
+ *   w      device, [rows x cols] row-major, fp32, bf16 or fp16 per `in_dtype`
+ *          (widened to fp32 exactly), 16-byte aligned.  Values must be finite.
  *   wq     host struct; wq->packed and wq->absmax are written (both 16-byte
  *          aligned); rows, cols, blocksize, code are read.
  * Per 64-block: absmax = max|w| (fp32); wn = fp32(w / absmax) (IEEE
@@ -157,25 +165,28 @@ nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
 nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight* wq,
                              void* workspace, size_t workspace_bytes, void* stream);
 
-/* Dequantization to bf16 (tutorial sec. 3.4).
- *   out: device bf16 [rows x cols], 16-byte aligned.
+/* Dequantization to the compute dtype (tutorial sec. 3.4).
+ *   out: device [rows x cols] of wq->compute_dtype (bf16 or fp16), 16-byte
+ *   aligned.
  * s_b = fmaf(absmax_q[b], scale2[b/256], offset) with double quant, else
- * absmax[b]; out = bf16_rn(fp32(code_value[code] * s_b)). */
+ * absmax[b]; out = round(fp32(code_value[code] * s_b)) to the compute dtype
+ * (nearest, ties to even). */
 nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream);
 
 /* Decode-shaped matmul, 1 <= M <= 16 (tutorial sec. 3.4, sec. 七 myth 5:
  * memory-bandwidth bound).  y[m, n] = sum_k x[m, k] * w_hat[n, k] with
- * w_hat exactly as nf4q_dequantize produces it, fp32 accumulation, bf16
- * output.
- *   x: device bf16 [M x cols], y: device bf16 [M x rows]; both 16-byte
- *   aligned. */
+ * w_hat exactly as nf4q_dequantize produces it, fp32 accumulation, output
+ * rounded to the compute dtype.
+ *   x: device [M x cols], y: device [M x rows], both of wq->compute_dtype
+ *   (bf16 or fp16) and 16-byte aligned. */
 nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M,
                       void* y, void* stream);
 
 /* Prefill-shaped matmul on the tcgen05 tensor cores, M >= 1 (intended for
  * M >= 64).  Same contraction and output as nf4q_gemv: Y [M x rows] =
- * X [M x cols] . w_hat^T, bf16 in, fp32 accumulate, bf16 out.
- *   X, Y: device bf16, 16-byte aligned. */
+ * X [M x cols] . w_hat^T, compute-dtype operands (bf16 or fp16), fp32
+ * accumulate, compute-dtype output.
+ *   X, Y: device, of wq->compute_dtype, 16-byte aligned. */
 nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M,
                       void* Y, void* stream);
 

@@ -50,12 +50,14 @@ def assert_bits_equal(a, b, what):
     assert bad.size == 0, f"{what}: {len(bad)} mismatches, first at {bad[:5].tolist()}"
 
 
-def check_matmul(y_gpu_bits: np.ndarray, x_bits: np.ndarray, what_bits: np.ndarray, what=""):
-    """|y - y_ref| <= 2e-3 * sum|x w_hat| + one bf16 ulp of y_ref, per output."""
-    y_ref, bound = o.matmul_ref(x_bits, what_bits)
-    y = o.bf16_bits_to_f32(y_gpu_bits).astype(np.float64)
+def check_matmul(y_gpu_bits: np.ndarray, x_bits: np.ndarray, what_bits: np.ndarray, what="",
+                 dtype: int = o.DT_BF16):
+    """|y - y_ref| <= 2e-3 * sum|x w_hat| + one ulp of y_ref in the compute
+    dtype, per output."""
+    y_ref, bound = o.matmul_ref(x_bits, what_bits, dtype)
+    y = o.from_bits(y_gpu_bits, dtype).astype(np.float64)
     err = np.abs(y - y_ref)
-    tol = o.matmul_tolerance(y_ref, bound)
+    tol = o.matmul_tolerance(y_ref, bound, dtype)
     worst = np.max(err / tol) if err.size else 0.0
     assert np.all(err <= tol), f"{what}: worst err/tol = {worst:.3f}"
     return worst

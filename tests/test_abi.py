@@ -72,9 +72,9 @@ def test_thresholds_are_round_down_midpoints(L):
 
 
 def test_argument_checks_launch_nothing(L):
-    s = nq.NF4QWeight(None, None, None, None, None, 64, 64, 64, 256, 0, 1)
-    bad = nq.NF4QWeight(None, None, None, None, None, 64, 100, 64, 256, 0, 1)
-    wrongbs = nq.NF4QWeight(None, None, None, None, None, 64, 64, 128, 256, 0, 1)
+    s = nq.NF4QWeight(None, None, None, None, None, 64, 64, 64, 256, 0, 1, 0)
+    bad = nq.NF4QWeight(None, None, None, None, None, 64, 100, 64, 256, 0, 1, 0)
+    wrongbs = nq.NF4QWeight(None, None, None, None, None, 64, 64, 128, 256, 0, 1, 0)
     R = ctypes.byref
     assert L.nf4q_quantize(None, 0, R(s), None) == 1
     assert L.nf4q_quantize(None, 0, R(bad), None) == 1
@@ -86,14 +86,20 @@ def test_argument_checks_launch_nothing(L):
     assert L.nf4q_gemv(R(s), 16, 17, 16, None) == 3
     assert L.nf4q_gemm(R(s), 16, -1, 16, None) == 1
     assert L.nf4q_gemv(None, 16, 1, 16, None) == 1
+    # an unknown compute dtype is refused by every call on the weight
+    dt = nq.NF4QWeight(None, None, None, None, None, 64, 64, 64, 256, 0, 1, 2)
+    assert L.nf4q_quantize(16, 1, R(dt), None) == 1
+    assert L.nf4q_dequantize(R(dt), 16, None) == 1
+    assert L.nf4q_gemv(R(dt), 16, 1, 16, None) == 1
+    assert L.nf4q_gemm(R(dt), 16, 64, 16, None) == 1
     # misaligned device pointers are refused before any launch
-    sp = nq.NF4QWeight(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64, 64, 64, 256, 0, 1)
+    sp = nq.NF4QWeight(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64, 64, 64, 256, 0, 1, 0)
     assert L.nf4q_quantize(0x1008, 1, R(sp), None) == 2
     assert L.nf4q_gemv(R(sp), 0x1004, 1, 0x2000, None) == 2
     # a too-small double-quant workspace
     assert L.nf4q_double_quant(R(sp), 0x6000, 8, None) == 4
     # empty weights are a no-op that succeeds
-    e = nq.NF4QWeight(None, None, None, None, None, 0, 64, 64, 256, 0, 1)
+    e = nq.NF4QWeight(None, None, None, None, None, 0, 64, 64, 256, 0, 1, 0)
     assert L.nf4q_quantize(None, 0, R(e), None) == 0
     assert L.nf4q_dequantize(R(e), None, None) == 0
 
