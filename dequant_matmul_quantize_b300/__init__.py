@@ -38,9 +38,20 @@ STATUS = {
 
 
 class Nf4qError(RuntimeError):
-    def __init__(self, func: str, status: int):
+    def __init__(self, func: str, status: int, detail: str = ""):
         self.status = status
-        super().__init__(f"{func} failed: {STATUS.get(status, status)}")
+        self.detail = detail
+        msg = f"{func} failed: {STATUS.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
+
+
+def last_cuda_error() -> str:
+    """Text of the last failing CUDA call of the library on this thread."""
+    L = lib()
+    n = L.nf4q_last_cuda_error(None, 0)
+    buf = ctypes.create_string_buffer(n + 1)
+    L.nf4q_last_cuda_error(buf, n + 1)
+    return buf.value.decode(errors="replace")
 
 
 class NF4QWeight(ctypes.Structure):
@@ -79,6 +90,7 @@ def lib() -> ctypes.CDLL:
     sig = {
         "nf4q_version": (i32, []),
         "nf4q_status_string": (ctypes.c_char_p, [i32]),
+        "nf4q_last_cuda_error": (i32, [ctypes.c_char_p, i32]),
         "nf4q_sizes": (i32, [i64, i64, i32, i32, ctypes.POINTER(sz),
                              ctypes.POINTER(i64), ctypes.POINTER(i64)]),
         "nf4q_code_values": (i32, [i32, ctypes.POINTER(ctypes.c_float)]),
@@ -104,7 +116,7 @@ def lib() -> ctypes.CDLL:
 
 def _check(func: str, status: int):
     if status != 0:
-        raise Nf4qError(func, status)
+        raise Nf4qError(func, status, last_cuda_error() if status == 5 else "")
 
 
 def _stream(stream=None) -> int:

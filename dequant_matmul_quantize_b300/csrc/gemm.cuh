@@ -27,7 +27,10 @@
 // No multicast: every CTA loads its own tiles.
 #pragma once
 
+#include <mutex>
+
 #include "common.cuh"
+#include "host.h"
 #include "lut.cuh"
 #include "tma.cuh"
 
@@ -373,25 +376,34 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
   cuuint32_t box[2] = {kGemmBK / 2, BN};
   cuuint32_t es[2] = {1, 1};
-  if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
+  nf4q_status st = cu_check(
+      enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return NF4Q_ERR_CUDA;
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+      "cuTensorMapEncodeTiled (GEMM weight)");
+  if (st != NF4Q_OK) return st;
+  // Opt in to the kernel's dynamic shared memory, once per device.
   static bool attr_set[64] = {false};
+  static std::mutex mu;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel<CODE, BN, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Cfg::kSmem)) != cudaSuccess)
-      return NF4Q_ERR_CUDA;
-    attr_set[dev] = true;
+  if ((st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) != NF4Q_OK) return st;
+  if (dev < 0 || dev >= 64) return NF4Q_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      st = cuda_check(cudaFuncSetAttribute(gemm_kernel<CODE, BN, DT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(Cfg::kSmem)),
+                      "cudaFuncSetAttribute (GEMM)");
+      if (st != NF4Q_OK) return st;
+      attr_set[dev] = true;
+    }
   }
   dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
             static_cast<unsigned>((M + 2 * kGemmBM - 1) / (2 * kGemmBM)));
-  gemm_kernel<CODE, BN, DT><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(
-      tx, tw, sv, static_cast<uint16_t*>(Y), static_cast<int>(M), static_cast<int>(N),
-      static_cast<int>(K), C);
-  return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
+  return launch("gemm_kernel", gemm_kernel<CODE, BN, DT>, grid, dim3(Cfg::kThreads), Cfg::kSmem,
+                stream, nullptr, 0, tx, tw, sv, static_cast<uint16_t*>(Y), static_cast<int>(M),
+                static_cast<int>(N), static_cast<int>(K), C);
 }
 
 template <int CODE, int DT>
@@ -414,18 +426,21 @@ inline nf4q_status gemm_launch(const nf4q_weight* wq, const ScaleView& sv,
   if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
   if ((M + 2 * kGemmBM - 1) / (2 * kGemmBM) > 65535) return NF4Q_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return NF4Q_ERR_CUDA;
+  if (!enc) return cuda_fail("cuTensorMapEncodeTiled: driver entry point not found");
+  if (ensure_context() != NF4Q_OK) return NF4Q_ERR_CUDA;
   CUtensorMap tx;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   cuuint32_t box[2] = {kGemmBK, kGemmBM};
   cuuint32_t es[2] = {1, 1};
   const int dt = wq->compute_dtype;
-  if (enc(&tx, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-          const_cast<void*>(X), dims, strides, box,
-          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return NF4Q_ERR_CUDA;
+  const nf4q_status st = cu_check(
+      enc(&tx, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+          const_cast<void*>(X), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+      "cuTensorMapEncodeTiled (GEMM activations)");
+  if (st != NF4Q_OK) return st;
   const int bn = gemm_pick_bn(M, N, sms);
   if (dt == 0)
     return wq->code == 0 ? gemm_launch_code<0, 0>(tx, wq, sv, C, M, Y, stream, bn)

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -13,6 +14,7 @@
 #include "double_quant.cuh"
 #include "gemm.cuh"
 #include "gemv_mma.cuh"
+#include "host.h"
 #include "quantize.cuh"
 
 namespace nf4q {
@@ -29,8 +31,10 @@ constexpr int kMaxDevices = 64;
 
 int sm_count() {
   static int cache[kMaxDevices] = {0};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
@@ -45,10 +49,6 @@ inline bool aligned16(const void* p) {
 }
 inline bool aligned4(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
-}
-
-inline nf4q_status launch_status() {
-  return cudaGetLastError() == cudaSuccess ? NF4Q_OK : NF4Q_ERR_CUDA;
 }
 
 // Shape and layout checks shared by every call on a quantized weight.
@@ -100,38 +100,54 @@ GemvKernelFn gemv_kernel(int code, int NT, int dt) {
 
 // Opt the GEMV kernels in to their largest dynamic shared memory (once per
 // device).
-bool gemv_attr_ready() {
+// The current device (0 .. kMaxDevices-1) or an error status.
+nf4q_status current_device(int* dev) {
+  nf4q_status st = cuda_check(cudaGetDevice(dev), "cudaGetDevice");
+  if (st == NF4Q_OK && (*dev < 0 || *dev >= kMaxDevices)) return NF4Q_ERR_UNSUPPORTED;
+  return st;
+}
+
+nf4q_status gemv_attr_ready() {
   static bool done[kMaxDevices] = {false};
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  nf4q_status st = current_device(&dev);
+  if (st != NF4Q_OK) return st;
   std::lock_guard<std::mutex> lock(mu);
-  if (done[dev]) return true;
+  if (done[dev]) return NF4Q_OK;
   const int bytes = static_cast<int>(gemv_smem_bytes(2, 2, kGemvMaxStages, kGemvMaxSplit));
   for (int code = 0; code < 2; ++code)
     for (int nt = 1; nt <= 2; ++nt)
       for (int dt = 0; dt < 2; ++dt)
-        if (cudaFuncSetAttribute(gemv_kernel(code, nt, dt),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-          return false;
+        if ((st = cuda_check(cudaFuncSetAttribute(gemv_kernel(code, nt, dt),
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  bytes),
+                             "cudaFuncSetAttribute (GEMV)")) != NF4Q_OK)
+          return st;
   done[dev] = true;
-  return true;
+  return NF4Q_OK;
 }
 
 // Opt the dequantize kernels in to their dynamic shared memory (once per
 // device).
-bool dequantize_attr_ready() {
+nf4q_status dequantize_attr_ready() {
   static bool done[kMaxDevices] = {false};
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
-  if (done[dev]) return true;
+  nf4q_status st = current_device(&dev);
+  if (st != NF4Q_OK) return st;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return NF4Q_OK;
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
   const int b = static_cast<int>(kDequantSmemBytes);
-  done[dev] = cudaFuncSetAttribute(dequantize_kernel<0, 0>, A, b) == cudaSuccess &&
-              cudaFuncSetAttribute(dequantize_kernel<1, 0>, A, b) == cudaSuccess &&
-              cudaFuncSetAttribute(dequantize_kernel<0, 1>, A, b) == cudaSuccess &&
-              cudaFuncSetAttribute(dequantize_kernel<1, 1>, A, b) == cudaSuccess;
-  return done[dev];
+  const char* what = "cudaFuncSetAttribute (dequantize)";
+  if ((st = cuda_check(cudaFuncSetAttribute(dequantize_kernel<0, 0>, A, b), what)) != NF4Q_OK ||
+      (st = cuda_check(cudaFuncSetAttribute(dequantize_kernel<1, 0>, A, b), what)) != NF4Q_OK ||
+      (st = cuda_check(cudaFuncSetAttribute(dequantize_kernel<0, 1>, A, b), what)) != NF4Q_OK ||
+      (st = cuda_check(cudaFuncSetAttribute(dequantize_kernel<1, 1>, A, b), what)) != NF4Q_OK)
+    return st;
+  done[dev] = true;
+  return NF4Q_OK;
 }
 
 using QuantKernelFn = void (*)(const void*, uint2*, float*, int64_t, QuantParams,
@@ -150,29 +166,35 @@ QuantKernelFn quantize_kernel_for(int code, int in, int dq) {
 }
 
 // Opt the quantize kernels in to their dynamic shared memory (once per device).
-bool quantize_attr_ready() {
+nf4q_status quantize_attr_ready() {
   static bool done[kMaxDevices] = {false};
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
-  if (done[dev]) return true;
+  nf4q_status st = current_device(&dev);
+  if (st != NF4Q_OK) return st;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return NF4Q_OK;
   const int b0 = static_cast<int>(quantize_smem_bytes(0)), b1 = static_cast<int>(quantize_smem_bytes(1));
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  bool ok = true;
   for (int code = 0; code < 2; ++code)
     for (int in = 0; in < 3; ++in)
       for (int dq = 0; dq < 2; ++dq)
-        ok = ok && cudaFuncSetAttribute(quantize_kernel_for(code, in, dq), A,
-                                        code == 0 ? b0 : b1) == cudaSuccess;
-  done[dev] = ok;
-  return ok;
+        if ((st = cuda_check(cudaFuncSetAttribute(quantize_kernel_for(code, in, dq), A,
+                                                  code == 0 ? b0 : b1),
+                             "cudaFuncSetAttribute (quantize)")) != NF4Q_OK)
+          return st;
+  done[dev] = true;
+  return NF4Q_OK;
 }
 
 // Resident CTAs per SM of the quantize kernel (registers and shared memory),
 // so the grid-stride grid is exactly one full wave.
 int quantize_ctas_per_sm(int code) {
   static int cache[kMaxDevices][2] = {{0}};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lock(mu);
   if (cache[dev][code] == 0) {
     int n = 0;
     const size_t smem = quantize_smem_bytes(code);
@@ -224,6 +246,17 @@ const char* nf4q_status_string(nf4q_status s) {
     case NF4Q_ERR_TIMEOUT: return "device wait timed out";
   }
   return "unknown status";
+}
+
+int32_t nf4q_last_cuda_error(char* buf, int32_t buf_bytes) {
+  const char* text = last_error_text();
+  const int32_t n = static_cast<int32_t>(std::strlen(text));
+  if (buf && buf_bytes > 0) {
+    const int32_t m = std::min(n, buf_bytes - 1);
+    std::memcpy(buf, text, static_cast<size_t>(m));
+    buf[m] = '\0';
+  }
+  return n;
 }
 
 nf4q_status nf4q_sizes(int64_t rows, int64_t cols, int32_t blocksize,
@@ -282,16 +315,18 @@ nf4q_status quantize_launch(const void* w, int32_t in_dtype, const nf4q_weight* 
     P.lut_dl[i] = T.lut_dl[c][i];
   }
   for (int i = 0; i < 15; ++i) P.thr[i] = i < T.nthr[c] ? T.thr[c][i] : 2.0f;
-  if (!quantize_attr_ready()) return NF4Q_ERR_CUDA;
+  nf4q_status st = quantize_attr_ready();
+  if (st != NF4Q_OK) return st;
   const int64_t n_units = n / 16;  // 16 elements per lane and unit
   const int64_t grid = grid_for(n_units, kQuantThreads,
                                 static_cast<int64_t>(sm_count()) * quantize_ctas_per_sm(c));
-  if (ws && cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
-  quantize_kernel_for(c, in_dtype, ws != nullptr)<<<grid, kQuantThreads,
-                                                                    quantize_smem_bytes(c), s>>>(
-      w, reinterpret_cast<uint2*>(wq->packed), wq->absmax, n_units, P,
-      static_cast<DqWorkspace*>(ws), wq->offset);
-  return launch_status();
+  if (ws && (st = cuda_check(cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s),
+                             "cudaMemsetAsync (double-quant workspace)")) != NF4Q_OK)
+    return st;
+  return launch("quantize_kernel", quantize_kernel_for(c, in_dtype, ws != nullptr),
+                dim3(static_cast<unsigned>(grid)), dim3(kQuantThreads), quantize_smem_bytes(c), s,
+                nullptr, 0, w, reinterpret_cast<uint2*>(wq->packed), wq->absmax, n_units, P,
+                static_cast<DqWorkspace*>(ws), wq->offset);
 }
 
 // Second double-quant pass: int8 codes and per-256 scales from the mean.
@@ -302,30 +337,25 @@ nf4q_status dq_quant_launch(const nf4q_weight* wq, int64_t nb, cudaStream_t s,
                             bool dependent) {
   const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;
   const int64_t g2 = grid_for(nd, kDqQuantThreads / 32, static_cast<int64_t>(sm_count()) * 8);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(g2));
-  cfg.blockDim = dim3(kDqQuantThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = dependent ? 1 : 0;
   const float* am = wq->absmax;
   const float* off = wq->offset;
-  if (cudaLaunchKernelEx(&cfg, dq_quant_kernel, am, nb, off, wq->absmax_q, wq->scale2) !=
-      cudaSuccess)
-    return NF4Q_ERR_CUDA;
-  return launch_status();
+  return launch("dq_quant_kernel", dq_quant_kernel, dim3(static_cast<unsigned>(g2)),
+                dim3(kDqQuantThreads), 0, s, attr, dependent ? 1u : 0u, am, nb, off,
+                wq->absmax_q, wq->scale2);
 }
 
 nf4q_status dq_launch(const nf4q_weight* wq, int64_t nb, void* ws, cudaStream_t s) {
-  if (cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s) != cudaSuccess) return NF4Q_ERR_CUDA;
+  nf4q_status st = cuda_check(cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s),
+                              "cudaMemsetAsync (double-quant workspace)");
+  if (st != NF4Q_OK) return st;
   const int64_t g1 = grid_for(nb / 4, kDqSumThreads, static_cast<int64_t>(sm_count()));
-  dq_sum_kernel<<<g1, kDqSumThreads, 0, s>>>(wq->absmax, nb, static_cast<DqWorkspace*>(ws),
-                                             wq->offset);
-  if (cudaGetLastError() != cudaSuccess) return NF4Q_ERR_CUDA;
+  st = launch("dq_sum_kernel", dq_sum_kernel, dim3(static_cast<unsigned>(g1)),
+              dim3(kDqSumThreads), 0, s, nullptr, 0, static_cast<const float*>(wq->absmax), nb,
+              static_cast<DqWorkspace*>(ws), wq->offset);
+  if (st != NF4Q_OK) return st;
   return dq_quant_launch(wq, nb, s, false);
 }
 }  // namespace
@@ -357,8 +387,8 @@ nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
   if (!aligned4(wq->offset) || !aligned4(wq->scale2)) return NF4Q_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (nb == 0) {
-    if (cudaMemsetAsync(wq->offset, 0, sizeof(float), s) != cudaSuccess) return NF4Q_ERR_CUDA;
-    return NF4Q_OK;
+    return cuda_check(cudaMemsetAsync(wq->offset, 0, sizeof(float), s),
+                      "cudaMemsetAsync (offset)");
   }
   if (!wq->absmax) return NF4Q_ERR_INVALID_ARG;
   if (!aligned16(wq->absmax) || !aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;
@@ -379,8 +409,8 @@ nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t nb = wq->rows * wq->cols / kBlock;
   if (nb == 0)
-    return cudaMemsetAsync(wq->offset, 0, sizeof(float), s) == cudaSuccess ? NF4Q_OK
-                                                                          : NF4Q_ERR_CUDA;
+    return cuda_check(cudaMemsetAsync(wq->offset, 0, sizeof(float), s),
+                      "cudaMemsetAsync (offset)");
   if (!aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;
   if (!workspace || workspace_bytes < sizeof(DqWorkspace)) return NF4Q_ERR_WORKSPACE;
   if (!aligned16(workspace)) return NF4Q_ERR_ALIGNMENT;
@@ -397,20 +427,22 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
   if (!out) return NF4Q_ERR_INVALID_ARG;
   if (!aligned16(out)) return NF4Q_ERR_ALIGNMENT;
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
-  if (!dequantize_attr_ready()) return NF4Q_ERR_CUDA;
+  if ((st = dequantize_attr_ready()) != NF4Q_OK) return st;
   const int64_t n_blocks = n / kBlock;
   EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return NF4Q_ERR_CUDA;
+  if (!enc) return cuda_fail("cuTensorMapEncodeTiled: driver entry point not found");
+  if ((st = ensure_context()) != NF4Q_OK) return st;
   CUtensorMap tout;
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kBlock), static_cast<cuuint64_t>(n_blocks)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kBlock * 2)};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlock), 32};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, out, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return NF4Q_ERR_CUDA;
+    st = cu_check(enc(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, out, dims, strides, box, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                  "cuTensorMapEncodeTiled (dequantize output)");
+    if (st != NF4Q_OK) return st;
   }
   const int64_t n_tiles = (n_blocks + 31) / 32;
   const int64_t grid = grid_for(n_tiles, kDequantWarps,
@@ -421,9 +453,9 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
   const DequantFn k = wq->compute_dtype == NF4Q_DT_BF16
       ? (wq->code == NF4Q_CODE_NF4 ? dequantize_kernel<0, 0> : dequantize_kernel<1, 0>)
       : (wq->code == NF4Q_CODE_NF4 ? dequantize_kernel<0, 1> : dequantize_kernel<1, 1>);
-  k<<<grid, kDequantThreads, kDequantSmemBytes, s>>>(pk, scale_view(wq), tout, n_blocks,
-                                                     code_values(wq->code));
-  return launch_status();
+  return launch("dequantize_kernel", k, dim3(static_cast<unsigned>(grid)), dim3(kDequantThreads),
+                kDequantSmemBytes, s, nullptr, 0, pk, scale_view(wq), tout, n_blocks,
+                code_values(wq->code));
 }
 
 nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
@@ -436,14 +468,14 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   if (!aligned16(x) || !aligned16(y)) return NF4Q_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (wq->cols == 0) {  // empty contraction: y = 0
-    return cudaMemsetAsync(y, 0, static_cast<size_t>(M) * wq->rows * 2, s) == cudaSuccess
-               ? NF4Q_OK : NF4Q_ERR_CUDA;
+    return cuda_check(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * wq->rows * 2, s),
+                      "cudaMemsetAsync (y of an empty contraction)");
   }
   if ((st = check_scales(wq)) != NF4Q_OK) return st;
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
   if (wq->rows > (1ll << 30) || wq->cols > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
   const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
-  if (!gemv_attr_ready()) return NF4Q_ERR_CUDA;
+  if ((st = gemv_attr_ready()) != NF4Q_OK) return st;
   // M <= 8: one 8-column MMA tile and 16 rows per CTA; M > 8: two column
   // tiles and 32 rows, so each x fragment serves twice as many weights.
   const int NT = M > 8 ? 2 : 1, R = NT;
@@ -463,39 +495,33 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   const int stages = std::min(kGemvStages, per);
   const size_t smem = gemv_smem_bytes(R, NT, stages, split);
   EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return NF4Q_ERR_CUDA;
+  if (!enc) return cuda_fail("cuTensorMapEncodeTiled: driver entry point not found");
+  if ((st = ensure_context()) != NF4Q_OK) return st;
   CUtensorMap tw;
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
     cuuint32_t box[2] = {kGemvSeg / 2, static_cast<cuuint32_t>(kGemvRows * R)};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return NF4Q_ERR_CUDA;
+    st = cu_check(enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                  "cuTensorMapEncodeTiled (GEMV weight)");
+    if (st != NF4Q_OK) return st;
   }
   if (tiles * split > 0x7FFFFFFF) return NF4Q_ERR_UNSUPPORTED;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles * split));
-  cfg.blockDim = dim3(kGemvWarps * 32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(split);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = split > 1 ? 1 : 0;
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   uint16_t* yp = static_cast<uint16_t*>(y);
   const ScaleView sv = scale_view(wq);
   const CodeValues C = code_values(wq->code);
-  if (cudaLaunchKernelEx(&cfg, gemv_kernel(code, NT, wq->compute_dtype), tw, sv, xp, yp, N, K, static_cast<int>(M),
-                         per, stages, C) != cudaSuccess)
-    return NF4Q_ERR_CUDA;
-  return launch_status();
+  return launch("gemv_mma_kernel", gemv_kernel(code, NT, wq->compute_dtype),
+                dim3(static_cast<unsigned>(tiles * split)), dim3(kGemvWarps * 32), smem, s, attr,
+                split > 1 ? 1u : 0u, tw, sv, xp, yp, N, K, static_cast<int>(M), per, stages, C);
 }
 
 nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M, void* Y,
@@ -508,8 +534,8 @@ nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M, void* Y,
   if (!aligned16(X) || !aligned16(Y)) return NF4Q_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (wq->cols == 0) {
-    return cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * wq->rows * 2, s) == cudaSuccess
-               ? NF4Q_OK : NF4Q_ERR_CUDA;
+    return cuda_check(cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * wq->rows * 2, s),
+                      "cudaMemsetAsync (Y of an empty contraction)");
   }
   if ((st = check_scales(wq)) != NF4Q_OK) return st;
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
@@ -525,15 +551,14 @@ nf4q_status nf4q_matmul(const nf4q_weight* wq, const void* X, int64_t M, void* Y
 
 nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear) {
   if (!flags) return NF4Q_ERR_INVALID_ARG;
-  if (cudaDeviceSynchronize() != cudaSuccess) return NF4Q_ERR_CUDA;
-  if (cudaMemcpyFromSymbol(flags, g_device_error, sizeof(uint32_t)) != cudaSuccess)
-    return NF4Q_ERR_CUDA;
-  if (clear) {
-    const uint32_t zero = 0;
-    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t)) != cudaSuccess)
-      return NF4Q_ERR_CUDA;
-  }
-  return NF4Q_OK;
+  nf4q_status st = cuda_check(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  if (st != NF4Q_OK) return st;
+  st = cuda_check(cudaMemcpyFromSymbol(flags, g_device_error, sizeof(uint32_t)),
+                  "cudaMemcpyFromSymbol (device error word)");
+  if (st != NF4Q_OK || !clear) return st;
+  const uint32_t zero = 0;
+  return cuda_check(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t)),
+                    "cudaMemcpyToSymbol (device error word)");
 }
 
 // ---------------------------------------------------------------- no-alloc
@@ -548,17 +573,12 @@ void* noalloc_scratch(nf4q_status* st) {
   static void* addr[kMaxDevices] = {nullptr};
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    *st = NF4Q_ERR_CUDA;
-    return nullptr;
-  }
+  if ((*st = current_device(&dev)) != NF4Q_OK) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dq_noalloc_scratch) != cudaSuccess || !p) {
-      *st = NF4Q_ERR_CUDA;
-      return nullptr;
-    }
+    *st = cuda_check(cudaGetSymbolAddress(&p, g_dq_noalloc_scratch), "cudaGetSymbolAddress");
+    if (*st != NF4Q_OK) return nullptr;
     addr[dev] = p;
   }
   *st = NF4Q_OK;
@@ -576,8 +596,8 @@ nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream) {
     return NF4Q_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (nb == 0) {
-    if (cudaMemsetAsync(wq->offset, 0, sizeof(float), s) != cudaSuccess) return NF4Q_ERR_CUDA;
-    return NF4Q_OK;
+    return cuda_check(cudaMemsetAsync(wq->offset, 0, sizeof(float), s),
+                      "cudaMemsetAsync (offset)");
   }
   if (!wq->absmax) return NF4Q_ERR_INVALID_ARG;
   if (!aligned16(wq->absmax) || !aligned16(wq->absmax_q)) return NF4Q_ERR_ALIGNMENT;

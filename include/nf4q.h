@@ -26,8 +26,12 @@
  * never written.  Outputs must not alias inputs.
  *
  * Errors: arguments are checked on the host before anything is launched
- * (a failing check launches nothing).  A CUDA launch error is reported as
- * NF4Q_ERR_CUDA.  Device-side bounded waits that give up set a sticky flag
+ * (a failing check launches nothing).  A failing CUDA call (a launch, a
+ * memset, the tensor-map encoder) is reported as NF4Q_ERR_CUDA, and its text
+ * is kept for nf4q_last_cuda_error().  The status of a launch is that
+ * launch's own: the thread's sticky CUDA "last error", which other code on
+ * the thread may have set, is never read.  Every entry point may be called
+ * from any host thread.  Device-side bounded waits that give up set a sticky flag
  * read with nf4q_device_error().
  *
  * Layout of a quantized weight W [rows x cols] (row-major, cols contiguous,
@@ -103,6 +107,15 @@ int32_t nf4q_version(void);
 
 /* Human-readable name of a status (static string, never NULL). */
 const char* nf4q_status_string(nf4q_status s);
+
+/* HOST ONLY.  The last CUDA failure of a call on the CALLING THREAD: the
+ * failing runtime or driver call and the error's name and text, e.g.
+ * "dequantize_kernel: cudaErrorInvalidValue (1): invalid argument"; "" if no
+ * call on this thread has returned NF4Q_ERR_CUDA.  Copies at most
+ * buf_bytes - 1 characters and a terminating NUL into buf (buf may be NULL
+ * when buf_bytes is 0) and returns the length of the whole text.  The text
+ * stays until the next failure on the same thread. */
+int32_t nf4q_last_cuda_error(char* buf, int32_t buf_bytes);
 
 /* HOST ONLY.  Buffer sizes of a [rows x cols] weight: packed bytes, number of
  * 64-blocks n_b and of 256-blocks n_d.  Any output pointer may be NULL. */

@@ -42,6 +42,23 @@ def test_version_and_status_strings(L):
     assert L.nf4q_status_string(99) == b"unknown status"
 
 
+def test_last_cuda_error_is_empty_before_any_failure(L):
+    # a fresh thread has no recorded failure; the call itself needs no GPU
+    import threading
+    out = {}
+
+    def probe():
+        buf = ctypes.create_string_buffer(8)
+        out["n"] = L.nf4q_last_cuda_error(buf, 8)
+        out["text"] = buf.value
+        out["n_null"] = L.nf4q_last_cuda_error(None, 0)
+
+    t = threading.Thread(target=probe)
+    t.start()
+    t.join()
+    assert out == {"n": 0, "text": b"", "n_null": 0}
+
+
 def test_sizes(L):
     assert nq.sizes(4096, 4096) == (4096 * 4096 // 2, 4096 * 4096 // 64, 1024)
     assert nq.sizes(28672, 8192)[2] == 14336

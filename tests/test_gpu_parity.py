@@ -326,3 +326,42 @@ def test_bad_arguments_leave_gpu_usable():
     y = nq.gemv(qw, x)
     torch.cuda.synchronize()
     assert torch.isfinite(y.float()).all()
+
+
+@pytest.mark.parametrize("op", ["quantize", "dequantize", "gemv1", "gemv9", "gemm"])
+def test_first_call_on_a_fresh_host_thread(op):
+    """Each entry point works as the FIRST library call on a new host thread
+    (autograd runs backward on such a thread, where no CUDA context need be
+    current): the same bytes / outputs as on the main thread."""
+    import threading
+    w = synth.normal_weight(160, 256, 0.02, seed=21).cuda()
+    qw = nq.quantize(w)
+    xs = {"gemv1": synth.activations(1, 256, seed=22).cuda(),
+          "gemv9": synth.activations(9, 256, seed=23).cuda(),
+          "gemm": synth.activations(80, 256, seed=24).cuda()}
+
+    def run():
+        if op == "quantize":
+            q = nq.quantize(w)
+            return (q.packed, q.absmax_q, q.scale2, q.offset)
+        if op == "dequantize":
+            return (nq.dequantize(qw),)
+        return (nq.matmul(qw, xs[op]),)
+
+    main = run()
+    torch.cuda.synchronize()
+    out, err = {}, []
+
+    def worker():
+        try:
+            out["r"] = run()
+            torch.cuda.synchronize()
+        except Exception as e:      # noqa: BLE001 - reported below
+            err.append(e)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert not err, err
+    for a, b in zip(main, out["r"]):
+        assert torch.equal(a, b)
