@@ -1,0 +1,100 @@
+"""Linear4bit and the nf4q custom operators.  CPU tests check registration,
+fake (shape) propagation and that torch.export traces through the operators
+without running them; GPU tests check the module against the plain binding
+calls and torch.compile(fullgraph=True) against eager."""
+import pytest
+import torch
+
+import dequant_matmul_quantize_b300 as nq
+import synth
+from dequant_matmul_quantize_b300.nn import Linear4bit
+
+
+def test_operators_are_registered():
+    for name in ("quantize", "dequantize", "matmul"):
+        assert hasattr(torch.ops.nf4q, name)
+
+
+def test_fake_shapes_and_dtypes():
+    from torch._subclasses.fake_tensor import FakeTensorMode
+    with FakeTensorMode():
+        w = torch.empty(96, 256, dtype=torch.bfloat16)
+        st = torch.ops.nf4q.quantize(w, "nf4", True, "f16")
+        assert [tuple(t.shape) for t in st] == [(96 * 256 // 2,), (384,), (384,), (2,), (1,)]
+        assert [t.dtype for t in st] == [torch.uint8, torch.float32, torch.int8,
+                                         torch.float32, torch.float32]
+        w_hat = torch.ops.nf4q.dequantize(*st, 96, 256, "nf4", True, "f16")
+        assert w_hat.shape == (96, 256) and w_hat.dtype == torch.float16
+        x = torch.empty(5, 256, dtype=torch.float16)
+        y = torch.ops.nf4q.matmul(x, *st, 96, 256, "nf4", True, "f16")
+        assert y.shape == (5, 96) and y.dtype == torch.float16
+
+
+def test_export_traces_through_the_operator():
+    m = Linear4bit(128, 48, bias=True, device="cpu")
+    ep = torch.export.export(m, (torch.empty(3, 7, 128, dtype=torch.bfloat16),))
+    targets = [str(n.target) for n in ep.graph.nodes if n.op == "call_function"]
+    assert any("nf4q.matmul" in t for t in targets), targets
+
+
+def test_module_argument_checks():
+    with pytest.raises(ValueError):
+        Linear4bit(100, 8, device="cpu")             # not a multiple of 64
+    with pytest.raises(ValueError):
+        Linear4bit(128, 8, code="int4", device="cpu")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("compute_dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M", [1, 9, 100])
+def test_linear4bit_matches_binding(compute_dtype, M):
+    dt = torch.bfloat16 if compute_dtype == "bf16" else torch.float16
+    w = synth.normal_weight(192, 512, 0.02, seed=M).cuda()
+    b = torch.randn(192, generator=torch.Generator().manual_seed(M)).to(dt).cuda()
+    lin = Linear4bit.from_weight(w, b, "nf4", True, compute_dtype)
+    qw = nq.quantize(w, "nf4", True, compute_dtype=compute_dtype)
+    x = synth.activations(M, 512, seed=M + 1).to(dt).cuda()
+    y = lin(x)
+    ref = nq.matmul(qw, x) + b
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
+    assert torch.equal(lin.dequantized_weight(), nq.dequantize(qw))
+
+
+@pytest.mark.gpu
+def test_compile_fullgraph_matches_eager():
+    torch.manual_seed(0)
+    l1 = torch.nn.Linear(512, 256).cuda()
+    l2 = torch.nn.Linear(256, 128).cuda()
+    mlp = torch.nn.Sequential(Linear4bit.from_linear(l1), torch.nn.GELU(),
+                              Linear4bit.from_linear(l2))
+    x = synth.activations(24, 512, seed=3).cuda().reshape(2, 12, 512)
+    eager = mlp(x)
+    # fullgraph: the nf4q operators trace without graph breaks; the aot_eager
+    # backend runs the traced graph as is (no code generation)
+    compiled = torch.compile(mlp, fullgraph=True, backend="aot_eager")(x)
+    torch.cuda.synchronize()
+    assert compiled.shape == (2, 12, 128)
+    assert torch.equal(compiled, eager)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("compute_dtype", ["bf16", "f16"])
+def test_backward_through_frozen_base(compute_dtype):
+    """dX = dY . w_hat (w_hat exactly as nf4q_dequantize gives it); the 4-bit
+    state gets no gradient."""
+    dt = torch.bfloat16 if compute_dtype == "bf16" else torch.float16
+    w = synth.normal_weight(160, 256, 0.02, seed=11).cuda()
+    lin = Linear4bit.from_weight(w, None, "nf4", True, compute_dtype)
+    x = synth.activations(6, 256, seed=12).to(dt).cuda().requires_grad_(True)
+    gy = synth.activations(6, 160, seed=13).to(dt).cuda()
+    lin(x).backward(gy)
+    w_hat = lin.dequantized_weight().float()
+    ref = gy.float() @ w_hat
+    torch.cuda.synchronize()
+    assert x.grad.dtype == dt and x.grad.shape == x.shape
+    err = (x.grad.float() - ref).abs()
+    # fp32 accumulation in cuBLAS plus one rounding of the output to 16 bits
+    tol = 4e-3 * (gy.float().abs() @ w_hat.abs()) + 1e-30
+    assert bool((err <= tol).all())
+    assert lin.packed.grad is None
