@@ -403,6 +403,19 @@ def matmul_ref(x_bits: np.ndarray, w_hat_bits: np.ndarray, dtype: int = DT_BF16)
     return x @ w.T, np.abs(x) @ np.abs(w).T
 
 
+def matmul_dx_ref(dy_bits: np.ndarray, w_hat_bits: np.ndarray, dtype: int = DT_BF16):
+    """dX_ref = dY . w_hat in fp64 from compute-dtype inputs, and the
+    per-output error scale sum_n |dY_n * w_hat_nk|.  dY [M, N], w_hat [N, K]
+    as bit patterns of the compute dtype.
+
+    This is the gradient of y = x . w_hat^T with respect to x, the one
+    gradient a frozen 4-bit base layer needs when only LoRA adapters train
+    (tutorial section 5.4): dL/dx_k = sum_n dL/dy_n * w_hat[n, k]."""
+    dy = from_bits(dy_bits, dtype).astype(np.float64)
+    w = from_bits(w_hat_bits, dtype).astype(np.float64)
+    return dy @ w, np.abs(dy) @ np.abs(w)
+
+
 def ulp_f16(v: np.ndarray) -> np.ndarray:
     """Spacing of fp16 numbers at |v| (2^(e-10) for 2^e <= |v| < 2^(e+1),
     2^-24 below the normal range)."""

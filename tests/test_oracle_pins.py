@@ -469,6 +469,31 @@ def test_matmul_ref_against_torch_and_one_hot():
     assert np.array_equal(y1[0], o.bf16_bits_to_f32(wb[:, 17]).astype(np.float64))
 
 
+def test_matmul_dx_ref_brute_force_one_hot_and_adjoint():
+    """dX = dY . w_hat: a triple loop on a tiny case, a one-hot dY row picks
+    a row of w_hat exactly, and <dY, x . w_hat^T> = <dY . w_hat, x> ties it
+    to the forward reference on a non-square weight."""
+    g = np.random.default_rng(5)
+    w = o.f32_to_bf16_bits((g.standard_normal((6, 64)) * 0.1).astype(np.float32))
+    dy = o.f32_to_bf16_bits(g.standard_normal((3, 6)).astype(np.float32))
+    dx, bound = o.matmul_dx_ref(dy, w)
+    assert dx.shape == (3, 64)
+    W, D = o.bf16_bits_to_f32(w).astype(np.float64), o.bf16_bits_to_f32(dy).astype(np.float64)
+    for i in range(3):
+        for k in range(64):
+            acc = sum(D[i, n] * W[n, k] for n in range(6))
+            assert abs(dx[i, k] - acc) <= 1e-12 * max(1.0, abs(acc))
+            assert abs(bound[i, k] - sum(abs(D[i, n] * W[n, k]) for n in range(6))) <= 1e-12
+    e = np.zeros((1, 6), np.float32)
+    e[0, 4] = 1.0
+    dx1, _ = o.matmul_dx_ref(o.f32_to_bf16_bits(e), w)
+    assert np.array_equal(dx1[0], W[4])
+    x = o.f32_to_bf16_bits(g.standard_normal((3, 64)).astype(np.float32))
+    y, _ = o.matmul_ref(x, w)
+    X = o.bf16_bits_to_f32(x).astype(np.float64)
+    assert abs(np.sum(D * y) - np.sum(dx * X)) <= 1e-9 * np.sum(np.abs(D) @ np.abs(W) * np.abs(X))
+
+
 def test_tolerance_has_ulp_floor():
     y = np.array([0.0, 1.0, 3.0, -1e-3])
     tol = o.matmul_tolerance(y, np.zeros(4))
@@ -532,7 +557,17 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_matmul_ref_against_torch_and_one_hot()
     monkeypatch.undo()
-    # (5) fp16 rounding by truncation instead of to nearest
+    # (5) the backward reference with the output columns mis-indexed
+    # (columns of w_hat reversed)
+    monkeypatch.setattr(o, "matmul_dx_ref", lambda db, wb, dtype=0: (
+        o.bf16_bits_to_f32(db).astype(np.float64)
+        @ o.bf16_bits_to_f32(wb).astype(np.float64)[:, ::-1],
+        np.abs(o.bf16_bits_to_f32(db).astype(np.float64))
+        @ np.abs(o.bf16_bits_to_f32(wb).astype(np.float64))))
+    with pytest.raises(AssertionError):
+        test_matmul_dx_ref_brute_force_one_hot_and_adjoint()
+    monkeypatch.undo()
+    # (6) fp16 rounding by truncation instead of to nearest
     monkeypatch.setattr(o, "f32_to_f16_bits", lambda x: np.asarray(
         [np.float16(np.float32(v)) if abs(np.float16(np.float32(v))) <= abs(v) else
          np.nextafter(np.float16(np.float32(v)), np.float16(0)) for v in np.asarray(x, np.float32)],
