@@ -514,6 +514,29 @@ def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
                                "fp16 point)",
                    "points": pts, "peak_bf16_tflops": peaks["bf16"],
                    "peak_source": peaks["src"] + " cuBLAS bf16 burst"}
+
+    # input gradient through the frozen weight: dX [M x 4096] = dY [M x 14336] . w_hat
+    N, K = w.shape
+    pts = []
+    for M in (256, 512, 2048, 4096):
+        dy = synth.activations(M, N, seed=M + N, device=dev)
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        ms = timed(lambda: L.nf4q_matmul_dx(R(s), dy.data_ptr(), N, M, dx.data_ptr(), sp))
+        deq = torch.empty_like(w)
+
+        def two():
+            L.nf4q_dequantize(R(s), deq.data_ptr(), sp)
+            torch.matmul(dy, deq, out=dx)
+        ms_two = timed(two)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        pts.append({"M": M, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                    "frac_bf16_burst": round(tf / peaks["bf16"], 4),
+                    "us_dequant_plus_cublas": round(ms_two * 1e3, 1)})
+        del deq, dy, dx
+    out["gemm_dx"] = {"workload": "QLoRA base-layer backward: dX = dY . w_hat, prefill "
+                                  "14336x4096 NF4 weight, dY bf16 [M x 14336]",
+                      "points": pts, "peak_bf16_tflops": peaks["bf16"],
+                      "peak_source": peaks["src"] + " cuBLAS bf16 burst"}
     del w, qw
 
     # Llama-3-8B stack: whole-stack quantize + double quant, one decode token

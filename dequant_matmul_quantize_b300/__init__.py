@@ -104,6 +104,7 @@ def lib() -> ctypes.CDLL:
         "nf4q_gemv": (i32, [W, vp, i32, vp, vp]),
         "nf4q_gemm": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul": (i32, [W, vp, i64, vp, vp]),
+        "nf4q_matmul_dx": (i32, [W, vp, i64, i64, vp, vp]),
         "nf4q_device_error": (i32, [ctypes.POINTER(ctypes.c_uint32), i32]),
     }
     for name, (res, args) in sig.items():
@@ -277,6 +278,22 @@ def gemm(qw, x, out=None, stream=None):
 def matmul(qw, x, out=None, stream=None):
     """Dispatch on M: gemv for M <= 16, gemm above."""
     return _mm("nf4q_matmul", qw, x, out, stream)
+
+
+def matmul_dx(qw, dy, out=None, stream=None):
+    """dX = dY . w_hat (the input gradient through the frozen 4-bit weight)
+    on the tcgen05 tensor cores.  dy [M, rows] may have a row pitch larger
+    than rows (a column slice of a wider tensor) if it is a multiple of 8."""
+    assert dy.is_cuda and dy.dtype == qw.torch_dtype and dy.dim() == 2
+    assert dy.shape[1] == qw.rows and dy.stride(1) == 1
+    M = dy.shape[0]
+    ld = dy.stride(0) if M > 1 else max(qw.rows, dy.stride(0))
+    if out is None:
+        out = torch.empty(M, qw.cols, dtype=qw.torch_dtype, device=dy.device)
+    s = qw.struct()
+    _check("nf4q_matmul_dx", lib().nf4q_matmul_dx(ctypes.byref(s), _ptr(dy), ld, M, _ptr(out),
+                                                   _stream(stream)))
+    return out
 
 
 def device_error(clear: bool = True) -> int:

@@ -118,6 +118,48 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Epilogue of a CTA's 256 x BN tile: warps 2..17 drain the two fp32
+// accumulators (warp w reads TMEM lane quarter w % 4 - the only one it may
+// access - of accumulator ((w - 2) / 4) % 2, every other 32-column chunk
+// from ((w - 2) / 8) * 32), round to the compute dtype and store rows
+// m0 .. m0 + 255 (< M) and columns c0 .. c0 + BN - 1 (< ncols) of the
+// row-major Y [M x ncols].
+template <int BN, int DT>
+__device__ __forceinline__ void store_accumulators(uint32_t tmem, int warp, int lane,
+                                                   uint16_t* __restrict__ Y, int M, int ncols,
+                                                   int m0, int c0) {
+  const int q = warp & 3;
+  const int h = ((warp - 2) >> 2) & 1;
+  const int cc = ((warp - 2) >> 3) * 32;
+  const int m = m0 + h * kGemmBM + q * 32 + lane;
+  uint16_t* yrow = Y + static_cast<int64_t>(m) * ncols + c0;
+  const bool vec = (ncols & 7) == 0;
+#pragma unroll 1
+  for (int col = cc; col < BN; col += 64) {
+    uint32_t v[32];
+    tmem_ld32(tmem + h * 256 + (static_cast<uint32_t>(q * 32) << 16) + col, v);
+    if (m < M) {
+      const int n = min(32, ncols - (c0 + col));
+      if (n == 32 && vec) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 o;
+          o.x = pack_x2<DT>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+          o.y = pack_x2<DT>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+          o.z = pack_x2<DT>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+          o.w = pack_x2<DT>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+          *reinterpret_cast<uint4*>(yrow + col + 8 * j) = o;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < n) yrow[col + j] = round_to_dt<DT>(__uint_as_float(v[j]));
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ the kernel
 template <int CODE, int BN, int DT>
 __global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
@@ -294,40 +336,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       __syncwarp();
       if (lane == 0) mbar_arrive(bfull_bar(sb));
     }
-    // ---------------- epilogue: TMEM -> bf16 -> Y (16 warps: accumulator,
-    // TMEM lane quarter, and every other 32-column chunk)
+    // ---------------- epilogue: TMEM -> bf16 -> Y
     if (warp < 18 && __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
       tc_fence_after();
-      const int q = warp & 3;                 // TMEM lane quarter this warp may read
-      const int h = ((warp - 2) >> 2) & 1;    // accumulator (M half)
-      const int c0 = ((warp - 2) >> 3) * 32;  // first column chunk
-      const int m = m0 + h * kGemmBM + q * 32 + lane;
-      uint16_t* yrow = Y + static_cast<int64_t>(m) * N + n0;
-      const bool vec = (N & 7) == 0;
-#pragma unroll 1
-      for (int col = c0; col < BN; col += 64) {
-        uint32_t v[32];
-        tmem_ld32(tmem + h * 256 + (static_cast<uint32_t>(q * 32) << 16) + col, v);
-        if (m < M) {
-          const int ncols = min(32, N - (n0 + col));
-          if (ncols == 32 && vec) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 o;
-              o.x = pack_x2<DT>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-              o.y = pack_x2<DT>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-              o.z = pack_x2<DT>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-              o.w = pack_x2<DT>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-              *reinterpret_cast<uint4*>(yrow + col + 8 * j) = o;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j < ncols) yrow[col + j] = round_to_dt<DT>(__uint_as_float(v[j]));
-            }
-          }
-        }
-      }
+      store_accumulators<BN, DT>(tmem, warp, lane, Y, M, N, m0, n0);
     }
   }
   tc_fence_before();

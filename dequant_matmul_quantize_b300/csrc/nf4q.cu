@@ -13,6 +13,7 @@
 #include "dequantize.cuh"
 #include "double_quant.cuh"
 #include "gemm.cuh"
+#include "gemm_dx.cuh"
 #include "gemv_mma.cuh"
 #include "host.h"
 #include "quantize.cuh"
@@ -540,6 +541,25 @@ nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M, void* Y,
   if ((st = check_scales(wq)) != NF4Q_OK) return st;
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
   return gemm_launch(wq, scale_view(wq), code_values(wq->code), X, M, Y, s, sm_count());
+}
+
+nf4q_status nf4q_matmul_dx(const nf4q_weight* wq, const void* dY, int64_t ld_dy, int64_t M,
+                           void* dX, void* stream) {
+  nf4q_status st = check_shape(wq);
+  if (st != NF4Q_OK) return st;
+  if (M < 0 || ld_dy < wq->rows || ld_dy % 8 != 0) return NF4Q_ERR_INVALID_ARG;
+  if (M == 0 || wq->cols == 0) return NF4Q_OK;
+  if (!dY || !dX) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(dY) || !aligned16(dX)) return NF4Q_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (wq->rows == 0) {  // empty contraction: dX = 0
+    return cuda_check(cudaMemsetAsync(dX, 0, static_cast<size_t>(M) * wq->cols * 2, s),
+                      "cudaMemsetAsync (dX of an empty contraction)");
+  }
+  if ((st = check_scales(wq)) != NF4Q_OK) return st;
+  if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
+  return gemm_dx_launch(wq, scale_view(wq), code_values(wq->code), dY, ld_dy, M, dX, s,
+                        sm_count());
 }
 
 nf4q_status nf4q_matmul(const nf4q_weight* wq, const void* X, int64_t M, void* Y,

@@ -17,8 +17,9 @@ This module does the same for libnf4q:
   x, the tcgen05 GEMM above).  The bias, not part of the pages' contraction,
   is added by PyTorch.
 * ``nf4q.matmul`` is differentiable in x (the weight is frozen): dX = dY .
-  w_hat, with w_hat from ``nf4q.dequantize`` and one cuBLAS matmul - the
-  backward of a 4-bit base layer under LoRA.
+  w_hat by ``nf4q.matmul_dx`` (nf4q_matmul_dx, a tcgen05 kernel that
+  dequantizes w_hat tile by tile, as the forward GEMM does) - the backward
+  of a 4-bit base layer under LoRA ("bitsandbytes tutorial", sec. 5.4).
 """
 from __future__ import annotations
 
@@ -28,7 +29,7 @@ import torch
 from torch import Tensor
 
 from . import (DTYPES, QuantizedWeight, dequantize as _dequantize, matmul as _matmul,
-               quantize as _quantize, sizes)
+               matmul_dx as _matmul_dx, quantize as _quantize, sizes)
 
 _TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16}
 
@@ -87,16 +88,34 @@ def _(x, packed, absmax, absmax_q, scale2, offset, rows, cols, code, double_quan
     return x.new_empty(x.shape[0], rows, dtype=_TORCH_DT[compute_dtype])
 
 
+@torch.library.custom_op("nf4q::matmul_dx", mutates_args=())
+def matmul_dx_op(dy: Tensor, packed: Tensor, absmax: Tensor, absmax_q: Tensor, scale2: Tensor,
+                 offset: Tensor, rows: int, cols: int, code: str, double_quant: bool,
+                 compute_dtype: str) -> Tensor:
+    """dX [M x cols] = dY [M x rows] . w_hat (nf4q_matmul_dx)."""
+    dy = dy.contiguous()
+    if rows % 8:  # the kernel reads dY rows at a pitch of a multiple of 8 elements
+        wide = dy.new_zeros(dy.shape[0], (rows + 7) // 8 * 8)
+        wide[:, :rows] = dy
+        dy = wide[:, :rows]
+    return _matmul_dx(_qw(packed, absmax, absmax_q, scale2, offset, rows, cols, code,
+                          double_quant, compute_dtype), dy)
+
+
+@matmul_dx_op.register_fake
+def _(dy, packed, absmax, absmax_q, scale2, offset, rows, cols, code, double_quant,
+      compute_dtype):
+    return dy.new_empty(dy.shape[0], cols, dtype=_TORCH_DT[compute_dtype])
+
+
 # The frozen 4-bit weight gets no gradient; the input's is dX = dY . w_hat
-# (QLoRA backward through the base layer, "bitsandbytes tutorial" sec. 5.4):
-# the weight is dequantized by nf4q_dequantize and multiplied by cuBLAS.
+# (QLoRA backward through the base layer, "bitsandbytes tutorial" sec. 5.4).
 def _matmul_setup_context(ctx, inputs, output):
     ctx.state = inputs[1:]
 
 
 def _matmul_backward(ctx, grad_y):
-    w_hat = torch.ops.nf4q.dequantize(*ctx.state)
-    grad_x = grad_y.to(w_hat.dtype) @ w_hat
+    grad_x = torch.ops.nf4q.matmul_dx(grad_y.to(_TORCH_DT[ctx.state[-1]]), *ctx.state)
     return (grad_x,) + (None,) * len(ctx.state)
 
 

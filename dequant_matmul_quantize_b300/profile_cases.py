@@ -10,6 +10,7 @@ Each case builds its seeded synthetic input, runs the library call twice
     gemv4096     nf4q_gemv M=1 on the 4096x4096 decode weight
     gemv70b_m16  nf4q_gemv M=16 on the 28672x8192 weight (NF4)
     gemm2048     nf4q_gemm M=2048 on the 14336x4096 prefill weight
+    dx2048       nf4q_matmul_dx M=2048 on the 14336x4096 prefill weight
 
 Kernel launches per case are listed so a capture can be aimed with ncu's
 -k / -s / -c options.
@@ -68,6 +69,14 @@ def _run(case: str, torch, nq, synth) -> None:
         y = torch.empty(2048, qw.rows, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
             ok(L.nf4q_gemm(R(s), x.data_ptr(), 2048, y.data_ptr(), sp), "gemm")
+    elif case == "dx2048":
+        qw = nq.quantize(synth.prefill_weight(device=dev))
+        s = qw.struct()
+        N, K = qw.rows, qw.cols
+        dy = synth.activations(2048, N, seed=2048 + N, device=dev)
+        dx = torch.empty(2048, K, dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            ok(L.nf4q_matmul_dx(R(s), dy.data_ptr(), N, 2048, dx.data_ptr(), sp), "matmul_dx")
     else:
         raise SystemExit(f"unknown case {case!r}; see the module docstring")
     torch.cuda.synchronize()

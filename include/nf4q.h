@@ -14,6 +14,7 @@
  *       sec. 3.3  double quantization: the block scales quantized again
  *       sec. 3.4  compute dtype: 4-bit storage, dequantize to bf16, matmul
  *       sec. 四   config keys: quant type nf4|fp4, double quant, compute dtype
+ *       sec. 5.4  QLoRA: the 4-bit base is frozen, LoRA adapters train
  *   - "bitsandbytes introduction" (modelers.csdn.net), sec. 一 item 7 and
  *       sec. 三 examples 1-2: NF4 and FP4 4-bit types
  *   - "bitsandbytes: quantifier un modèle PyTorch sans quitter PyTorch"
@@ -207,6 +208,22 @@ nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M,
 #define NF4Q_GEMV_MAX_M 16
 nf4q_status nf4q_matmul(const nf4q_weight* wq, const void* X, int64_t M,
                         void* Y, void* stream);
+
+/* Input gradient through the frozen 4-bit weight - the backward pass of a
+ * QLoRA base layer, whose 4-bit weight stays frozen while LoRA adapters
+ * train ("bitsandbytes tutorial" sec. 5.4; "bitsandbytes introduction",
+ * core techniques item 3): dX [M x cols] =
+ * dY [M x rows] . w_hat, on the tcgen05 tensor cores; w_hat exactly as
+ * nf4q_dequantize writes it, compute-dtype operands, fp32 accumulate,
+ * compute-dtype output.
+ *   dY: device, of wq->compute_dtype, row-major with row pitch ld_dy
+ *       elements (ld_dy >= rows, a multiple of 8), 16-byte aligned; only the
+ *       first `rows` elements of a row are read.
+ *   dX: device, [M x cols] row-major, of wq->compute_dtype, 16-byte aligned.
+ * M == 0 or cols == 0 launches nothing; rows == 0 writes dX = 0.  Other
+ * errors as nf4q_gemm. */
+nf4q_status nf4q_matmul_dx(const nf4q_weight* wq, const void* dY, int64_t ld_dy,
+                           int64_t M, void* dX, void* stream);
 
 /* Sticky device error flags of the current device (bit 0: a GEMM pipeline
  * wait gave up).  Synchronizes the device; `clear` != 0 resets the flags. */

@@ -11,7 +11,7 @@ from dequant_matmul_quantize_b300.nn import Linear4bit
 
 
 def test_operators_are_registered():
-    for name in ("quantize", "dequantize", "matmul"):
+    for name in ("quantize", "dequantize", "matmul", "matmul_dx"):
         assert hasattr(torch.ops.nf4q, name)
 
 
@@ -28,6 +28,8 @@ def test_fake_shapes_and_dtypes():
         x = torch.empty(5, 256, dtype=torch.float16)
         y = torch.ops.nf4q.matmul(x, *st, 96, 256, "nf4", True, "f16")
         assert y.shape == (5, 96) and y.dtype == torch.float16
+        dx = torch.ops.nf4q.matmul_dx(y, *st, 96, 256, "nf4", True, "f16")
+        assert dx.shape == (5, 256) and dx.dtype == torch.float16
 
 
 def test_export_traces_through_the_operator():
@@ -79,22 +81,22 @@ def test_compile_fullgraph_matches_eager():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("compute_dtype", ["bf16", "f16"])
-def test_backward_through_frozen_base(compute_dtype):
+@pytest.mark.parametrize("compute_dtype,rows", [("bf16", 160), ("f16", 160), ("bf16", 100)])
+def test_backward_through_frozen_base(compute_dtype, rows):
     """dX = dY . w_hat (w_hat exactly as nf4q_dequantize gives it); the 4-bit
-    state gets no gradient."""
+    state gets no gradient.  100 rows: dY is re-pitched to 104 columns."""
     dt = torch.bfloat16 if compute_dtype == "bf16" else torch.float16
-    w = synth.normal_weight(160, 256, 0.02, seed=11).cuda()
+    w = synth.normal_weight(rows, 256, 0.02, seed=11).cuda()
     lin = Linear4bit.from_weight(w, None, "nf4", True, compute_dtype)
     x = synth.activations(6, 256, seed=12).to(dt).cuda().requires_grad_(True)
-    gy = synth.activations(6, 160, seed=13).to(dt).cuda()
+    gy = synth.activations(6, rows, seed=13).to(dt).cuda()
     lin(x).backward(gy)
     w_hat = lin.dequantized_weight().float()
     ref = gy.float() @ w_hat
     torch.cuda.synchronize()
     assert x.grad.dtype == dt and x.grad.shape == x.shape
     err = (x.grad.float() - ref).abs()
-    # fp32 accumulation in cuBLAS plus one rounding of the output to 16 bits
+    # fp32 accumulation in the kernel plus one rounding of the output to 16 bits
     tol = 4e-3 * (gy.float().abs() @ w_hat.abs()) + 1e-30
     assert bool((err <= tol).all())
     assert lin.packed.grad is None
