@@ -163,20 +163,36 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
     const int kb = k0 / kBlock + c;  // block column
     const bool col_ok = active && kb < kblocks;
     const float off = sv.double_quant ? __ldg(sv.offset) : 0.f;
-    // scale of this thread's block in stage t (0 outside the weight)
-    auto scale_of = [&](int t) -> float {
-      const int n = t * kDxRows + r;
-      if (!col_ok || t >= NT || n >= N) return 0.f;
-      const int64_t b = static_cast<int64_t>(n) * kblocks + kb;
-      if (!sv.double_quant) return __ldg(sv.absmax + b);
-      const float q = static_cast<float>(__ldg(sv.absmax_q + b));
-      return __fmaf_rn(q, __ldg(sv.scale2 + (b >> 8)), off);
+    // The scale inputs of this thread's block in stage t, loaded one own
+    // stage ahead and turned into the scale only when used, so no
+    // instruction waits on the load before then.  Outside the weight
+    // (rows >= N, blocks >= K / 64) the scale is 0.
+    struct RawScale {
+      int q;       // int8 code of the double-quantized scale
+      float s;     // its scale2, or the fp32 absmax without double quant
+      bool ok;
     };
-    float sc_next = scale_of(grp);
+    auto load_scale = [&](int t) -> RawScale {
+      RawScale v{0, 0.f, false};
+      const int n = t * kDxRows + r;
+      if (!col_ok || t >= NT || n >= N) return v;
+      const int64_t b = static_cast<int64_t>(n) * kblocks + kb;
+      v.ok = true;
+      if (sv.double_quant) {
+        v.q = __ldg(sv.absmax_q + b);
+        v.s = __ldg(sv.scale2 + (b >> 8));
+      } else {
+        v.s = __ldg(sv.absmax + b);
+      }
+      return v;
+    };
+    RawScale next = load_scale(grp);
     for (int t = grp; t < NT; t += Cfg::kGroups) {
       const int sa = t % SA, sb = t % SB;
-      const float sc = sc_next;
-      sc_next = scale_of(t + Cfg::kGroups);  // one own stage ahead
+      const RawScale cur = next;
+      next = load_scale(t + Cfg::kGroups);
+      const float sc = !cur.ok ? 0.f
+                     : (sv.double_quant ? __fmaf_rn(static_cast<float>(cur.q), cur.s, off) : cur.s);
       RowTable<CODE> T;
       build_table<CODE, DT>(T, sc, C);
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(bempty_bar(sb), ((t / SB) & 1) ^ 1, abort) &&
