@@ -539,6 +539,41 @@ def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
                       "peak_source": peaks["src"] + " cuBLAS bf16 burst"}
     del w, qw
 
+    # LLM.int8(): vector-wise int8 weight, decomposition matmul at decode sizes
+    w = synth.int8_mlp70b_weight(device=dev)
+    N, K = w.shape
+    wq = nq.int8_quantize_weight(w)
+    ms_q = timed(lambda: nq.int8_quantize_weight(w), n=3)
+    cps = [nq.Int8Weight(wq.q.clone(), wq.scale, N, K) for _ in range(2)]
+    pts = []
+    for M in (1, 4, 8, 16):
+        x = synth.int8_mlp70b_x(M, device=dev)
+        ws = nq.int8_workspace(M, K, dev)
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        for c in cps:
+            nq.int8_matmul(c, x, workspace=ws, out=y)
+        best = None
+        for _ in range(3):
+            a, b = E(), E()
+            a.record(stream)
+            for i in range(10):
+                nq.int8_matmul(cps[i % 2], x, workspace=ws, out=y)
+            b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b) / 10
+            best = ms if best is None else min(best, ms)
+        by = N * K + 4 * N + 2 * M * K + 2 * M * N     # int8 weight + scales + x + y
+        pts.append({"M": M, "us": round(best * 1e3, 1), "GB/s": round(by / (best * 1e-3) / 1e9, 1),
+                    "frac_measured_hbm": round(by / (best * 1e-3) / 1e9 / peaks["hbm"], 4)})
+    del cps, wq
+    out["llm_int8"] = {"workload": "fp16 28672x8192 N(0,0.015) weight quantized to int8 per "
+                                   "row; x fp16 N(0,1) with 0.5 % outlier feature columns x20; "
+                                   "threshold 6.0; two weight copies alternate (> L2)",
+                       "quantize_weight_us": round(ms_q * 1e3, 1),
+                       "quantize_weight_GB/s": round(3 * N * K / (ms_q * 1e-3) / 1e9, 1),
+                       "points": pts}
+    del w
+
     # Llama-3-8B stack: whole-stack quantize + double quant, one decode token
     if not args.no_stack:
         stack = []

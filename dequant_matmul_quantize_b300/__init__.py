@@ -10,7 +10,9 @@ the first op raises.
 The user-facing knobs mirror ``BitsAndBytesConfig`` as the bitsandbytes
 pages describe it (tutorial at mlqm.cn/news/394670, section 四): the 4-bit
 type ``nf4`` or ``fp4``, ``double_quant`` on or off, and the compute dtype,
-which is bf16 here.
+which is bf16 (or fp16) here.  The LLM.int8() path (``int8_*``) quantizes
+fp16 weights and activations to int8 vector-wise and runs the
+mixed-precision decomposition matmul.
 """
 from __future__ import annotations
 
@@ -72,6 +74,16 @@ class NF4QWeight(ctypes.Structure):
     ]
 
 
+class NF4QInt8Weight(ctypes.Structure):
+    """Mirror of ``nf4q_int8_weight`` in include/nf4q.h."""
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("scale", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+    ]
+
+
 _lib = None
 
 
@@ -106,6 +118,11 @@ def lib() -> ctypes.CDLL:
         "nf4q_matmul": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul_dx": (i32, [W, vp, i64, i64, vp, vp]),
         "nf4q_device_error": (i32, [ctypes.POINTER(ctypes.c_uint32), i32]),
+        "nf4q_double_quant_noalloc": (i32, [W, vp]),
+        "nf4q_int8_quantize_weight": (i32, [vp, i32, ctypes.POINTER(NF4QInt8Weight), vp]),
+        "nf4q_int8_workspace_bytes": (sz, [i64, i64]),
+        "nf4q_int8_matmul": (i32, [ctypes.POINTER(NF4QInt8Weight), vp, i64, ctypes.c_float, vp,
+                                   vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -300,3 +317,74 @@ def device_error(clear: bool = True) -> int:
     flags = ctypes.c_uint32()
     _check("nf4q_device_error", lib().nf4q_device_error(ctypes.byref(flags), 1 if clear else 0))
     return flags.value
+
+
+# ---------------------------------------------------------------- LLM.int8()
+INT8_DEFAULT_THRESHOLD = 6.0
+
+
+@dataclass
+class Int8Weight:
+    """int8 codes [rows, cols] and per-row fp32 absmax (``nf4q_int8_weight``)."""
+    q: torch.Tensor
+    scale: torch.Tensor
+    rows: int
+    cols: int
+
+    def struct(self) -> NF4QInt8Weight:
+        return NF4QInt8Weight(_ptr(self.q), _ptr(self.scale), self.rows, self.cols)
+
+
+def int8_quantize_weight(w: torch.Tensor, stream=None) -> Int8Weight:
+    """Vector-wise int8 quantization of an fp16 / bf16 weight [rows, cols]."""
+    assert w.is_cuda and w.dim() == 2 and w.is_contiguous()
+    in_dt = {torch.float16: IN_F16, torch.bfloat16: IN_BF16}[w.dtype]
+    rows, cols = w.shape
+    wq = Int8Weight(torch.empty(rows, cols, dtype=torch.int8, device=w.device),
+                    torch.empty(rows, dtype=torch.float32, device=w.device), rows, cols)
+    s = wq.struct()
+    _check("nf4q_int8_quantize_weight",
+           lib().nf4q_int8_quantize_weight(_ptr(w), in_dt, ctypes.byref(s), _stream(stream)))
+    return wq
+
+
+def int8_workspace(M: int, cols: int, device=None) -> torch.Tensor:
+    n = lib().nf4q_int8_workspace_bytes(M, cols)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def int8_workspace_views(ws: torch.Tensor, M: int, cols: int):
+    """The sections of a workspace after nf4q_int8_matmul, as the header
+    lays them out: (flags u8 [cols], count, list i32 [count], sx f32 [M],
+    xq fp16 [M, cols])."""
+    def a(v):
+        return (v + 255) // 256 * 256
+    o_count = a(cols)
+    o_list = o_count + 256
+    o_sx = o_list + a(4 * cols)
+    o_xq = o_sx + a(4 * M)
+    flags = ws[:cols]
+    count = int(ws[o_count:o_count + 4].view(torch.int32).item())
+    lst = ws[o_list:o_list + 4 * cols].view(torch.int32)[:count]
+    sx = ws[o_sx:o_sx + 4 * M].view(torch.float32)
+    xq = ws[o_xq:o_xq + 2 * M * cols].view(torch.float16).view(M, cols)
+    return flags, count, lst, sx, xq
+
+
+def int8_matmul(wq: Int8Weight, x: torch.Tensor, threshold: float = INT8_DEFAULT_THRESHOLD,
+                workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """LLM.int8() decomposition matmul: y [M, rows] = x [M, cols] (fp16)
+    against the int8 weight, outlier columns (|x| > threshold) in fp16."""
+    assert x.is_cuda and x.dtype == torch.float16 and x.is_contiguous()
+    assert x.shape[-1] == wq.cols
+    M = x.shape[0]
+    if workspace is None:
+        workspace = int8_workspace(M, wq.cols, x.device)
+    if out is None:
+        out = torch.empty(M, wq.rows, dtype=torch.float16, device=x.device)
+    s = wq.struct()
+    _check("nf4q_int8_matmul",
+           lib().nf4q_int8_matmul(ctypes.byref(s), _ptr(x), M, float(threshold), _ptr(out),
+                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out

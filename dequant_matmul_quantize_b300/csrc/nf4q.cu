@@ -16,6 +16,7 @@
 #include "gemm_dx.cuh"
 #include "gemv_mma.cuh"
 #include "host.h"
+#include "int8.cuh"
 #include "quantize.cuh"
 
 namespace nf4q {
@@ -624,6 +625,99 @@ nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream) {
   void* ws = noalloc_scratch(&st);
   if (st != NF4Q_OK) return st;
   return dq_launch(wq, nb, ws, s);
+}
+
+
+// ---------------------------------------------------------------- LLM.int8()
+namespace {
+nf4q_status check_int8_weight(const nf4q_int8_weight* wq) {
+  if (!wq || wq->rows < 0 || wq->cols < 0 || wq->cols % 16 != 0) return NF4Q_ERR_INVALID_ARG;
+  if (wq->rows > 0x7FFFFFFF || wq->cols > 0x7FFFFFFF) return NF4Q_ERR_UNSUPPORTED;
+  return NF4Q_OK;
+}
+}  // namespace
+
+nf4q_status nf4q_int8_quantize_weight(const void* w, int32_t in_dtype,
+                                      const nf4q_int8_weight* wq, void* stream) {
+  nf4q_status st = check_int8_weight(wq);
+  if (st != NF4Q_OK) return st;
+  if (in_dtype != NF4Q_IN_BF16 && in_dtype != NF4Q_IN_F16) return NF4Q_ERR_INVALID_ARG;
+  if (wq->rows == 0) return NF4Q_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!wq->scale) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned4(wq->scale)) return NF4Q_ERR_ALIGNMENT;
+  if (wq->cols == 0)
+    return cuda_check(cudaMemsetAsync(wq->scale, 0, sizeof(float) * wq->rows, s),
+                      "cudaMemsetAsync (int8 scales of empty rows)");
+  if (!w || !wq->q) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(wq->q)) return NF4Q_ERR_ALIGNMENT;
+  const auto k = in_dtype == NF4Q_IN_BF16 ? int8_quant_weight_kernel<1>
+                                          : int8_quant_weight_kernel<2>;
+  return launch("int8_quant_weight_kernel", k, dim3(static_cast<unsigned>(wq->rows)),
+                dim3(kI8Threads), 0, s, nullptr, 0, static_cast<const uint16_t*>(w), wq->q,
+                wq->scale, static_cast<int>(wq->cols));
+}
+
+size_t nf4q_int8_workspace_bytes(int64_t M, int64_t cols) {
+  if (M < 0 || cols < 0) return 0;
+  return int8_workspace_layout(M, cols).total;
+}
+
+nf4q_status nf4q_int8_matmul(const nf4q_int8_weight* wq, const void* X, int64_t M,
+                             float threshold, void* Y, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  nf4q_status st = check_int8_weight(wq);
+  if (st != NF4Q_OK) return st;
+  if (M < 0) return NF4Q_ERR_INVALID_ARG;
+  if (M == 0 || wq->rows == 0) return NF4Q_OK;
+  if (M > 0x7FFFFFFF || (M + 15) / 16 > 65535) return NF4Q_ERR_UNSUPPORTED;
+  if (!X || !Y) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Y)) return NF4Q_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t N = wq->rows, K = wq->cols;
+  if (K == 0)
+    return cuda_check(cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * 2, s),
+                      "cudaMemsetAsync (Y of an empty contraction)");
+  if (!wq->q || !wq->scale) return NF4Q_ERR_INVALID_ARG;
+  if (!aligned16(wq->q) || !aligned4(wq->scale)) return NF4Q_ERR_ALIGNMENT;
+  const Int8Workspace L = int8_workspace_layout(M, K);
+  if (!workspace || workspace_bytes < L.total) return NF4Q_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NF4Q_ERR_ALIGNMENT;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* flags = ws + L.flags;
+  int32_t* count = reinterpret_cast<int32_t*>(ws + L.count);
+  int32_t* list = reinterpret_cast<int32_t*>(ws + L.list);
+  float* sx = reinterpret_cast<float*>(ws + L.sx);
+  uint16_t* xq = reinterpret_cast<uint16_t*>(ws + L.xq);
+  const uint16_t* x = static_cast<const uint16_t*>(X);
+  const int Mi = static_cast<int>(M), Ni = static_cast<int>(N), Ki = static_cast<int>(K);
+  const float thr = threshold > 0.f ? threshold : 0.f;  // NaN -> 0: no decomposition
+  // the activation side: flags, ordered outlier list, row scales and codes
+  if (M <= 16) {
+    st = launch("int8_act_small_kernel", int8_act_small_kernel, dim3(1), dim3(1024), 0, s,
+                nullptr, 0, x, Mi, Ki, thr, flags, list, count, sx, xq);
+  } else {
+    st = launch("int8_outlier_flags_kernel", int8_outlier_flags_kernel,
+                dim3(static_cast<unsigned>((K + 255) / 256)), dim3(kI8Threads), 0, s, nullptr, 0,
+                x, Mi, Ki, thr, flags);
+    if (st == NF4Q_OK)
+      st = launch("int8_outlier_list_kernel", int8_outlier_list_kernel, dim3(1), dim3(1024), 0, s,
+                  nullptr, 0, static_cast<const uint8_t*>(flags), Ki, list, count);
+    if (st == NF4Q_OK)
+      st = launch("int8_quant_act_kernel", int8_quant_act_kernel,
+                  dim3(static_cast<unsigned>(M)), dim3(kI8Threads), 0, s, nullptr, 0, x,
+                  static_cast<const uint8_t*>(flags), Ki, sx, xq);
+  }
+  if (st != NF4Q_OK) return st;
+  const int nt = M > 8 ? 2 : 1;
+  const dim3 grid(static_cast<unsigned>((N + kI8Rows - 1) / kI8Rows),
+                  static_cast<unsigned>((M + 8 * nt - 1) / (8 * nt)));
+  const auto k = nt == 2 ? int8_mm_kernel<2> : int8_mm_kernel<1>;
+  return launch("int8_mm_kernel", k, grid, dim3(kI8Threads), 0, s, nullptr, 0,
+                static_cast<const int8_t*>(wq->q), static_cast<const float*>(wq->scale), x,
+                static_cast<const uint16_t*>(xq), static_cast<const float*>(sx),
+                static_cast<const int32_t*>(list), static_cast<const int32_t*>(count),
+                static_cast<uint16_t*>(Y), Ni, Ki, Mi);
 }
 
 }  // extern "C"

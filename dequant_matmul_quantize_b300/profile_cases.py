@@ -11,6 +11,8 @@ Each case builds its seeded synthetic input, runs the library call twice
     gemv70b_m16  nf4q_gemv M=16 on the 28672x8192 weight (NF4)
     gemm2048     nf4q_gemm M=2048 on the 14336x4096 prefill weight
     dx2048       nf4q_matmul_dx M=2048 on the 14336x4096 prefill weight
+    int8_m1      nf4q_int8_quantize_weight, then nf4q_int8_matmul M=1 and
+                 M=16, on the fp16 28672x8192 weight (LLM.int8())
 
 Kernel launches per case are listed so a capture can be aimed with ncu's
 -k / -s / -c options.
@@ -77,6 +79,16 @@ def _run(case: str, torch, nq, synth) -> None:
         dx = torch.empty(2048, K, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
             ok(L.nf4q_matmul_dx(R(s), dy.data_ptr(), N, 2048, dx.data_ptr(), sp), "matmul_dx")
+    elif case == "int8_m1":
+        w = synth.int8_mlp70b_weight(device=dev)
+        for _ in range(2):
+            wq = nq.int8_quantize_weight(w)
+        for M in (1, 16):
+            x = synth.int8_mlp70b_x(M, device=dev)
+            ws = nq.int8_workspace(M, wq.cols, dev)
+            y = torch.empty(M, wq.rows, dtype=torch.float16, device=dev)
+            for _ in range(2):
+                nq.int8_matmul(wq, x, workspace=ws, out=y)
     else:
         raise SystemExit(f"unknown case {case!r}; see the module docstring")
     torch.cuda.synchronize()

@@ -251,6 +251,66 @@ nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear);
  *   by the caller.  Other arguments and errors as nf4q_double_quant. */
 nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream);
 
+/* ------------------------------------------------------------------------
+ * LLM.int8(): vector-wise int8 quantization and the mixed-precision
+ * decomposition matmul ("bitsandbytes tutorial" sec. 3.1: the outlier
+ * feature dimensions of the activations are computed in FP16, the rest in
+ * INT8, and the two results are added; sec. 四: llm_int8_threshold, default
+ * 6.0; "bitsandbytes introduction", core techniques item 2: weights and
+ * activations in 8 bits, vector-wise, outlier feature vectors in 16 bits).
+ *
+ * An int8 weight W [rows x cols] (the nn.Linear [out, in] convention):
+ *   q      int8 [rows*cols] row-major codes, 16-byte aligned
+ *   scale  fp32 [rows]  s_n = max_k |W[n, k]|, 4-byte aligned
+ *   code   q = rint(RN(127 * w / s_n)) (RN: the float32 rounding of the
+ *          quotient; rint: half to even), 0 in a row with s_n = 0
+ * cols must be a multiple of 16 (16-byte rows). */
+typedef struct {
+  int8_t* q;
+  float* scale;
+  int64_t rows;
+  int64_t cols;
+} nf4q_int8_weight;
+
+#define NF4Q_INT8_DEFAULT_THRESHOLD 6.0f
+
+/* Quantize W (device, fp16 or bf16 per `in_dtype`, row-major, 16-byte
+ * aligned) into wq->q / wq->scale.  One CTA per row. */
+nf4q_status nf4q_int8_quantize_weight(const void* w, int32_t in_dtype,
+                                      const nf4q_int8_weight* wq, void* stream);
+
+/* HOST ONLY.  Workspace bytes of nf4q_int8_matmul for M activation rows of
+ * `cols` elements.  Layout from the (16-byte aligned) start, each section
+ * starting at a multiple of 256 bytes after the previous one:
+ *   flags  uint8 [cols]    1 where the column is an outlier
+ *   count  int32 [1]       number of outlier columns (a 256-byte section)
+ *   list   int32 [cols]    the outlier columns, ascending (first `count`)
+ *   sx     fp32  [M]       activation row scales
+ *   xq     fp16  [M*cols]  activation codes as fp16 integers
+ * Section sizes are rounded up to multiples of 256 bytes. */
+size_t nf4q_int8_workspace_bytes(int64_t M, int64_t cols);
+
+/* Y [M x rows] = the decomposition matmul of X [M x cols] with the int8
+ * weight, fp16 in and out:
+ *   outlier columns  O = {k : max_m |X[m, k]| > threshold}; threshold <= 0
+ *                    (or NaN) turns the decomposition off
+ *   activation codes per row m: sx_m = max |X[m, k]| over k not in O,
+ *                    xq = rint(RN(127 * x / sx_m)), 0 in O and when sx_m = 0
+ *   Y[m, n] = fp16( C[m, n] * sx_m * s_n / 127^2
+ *                   + sum_{k in O} X[m, k] * w_hat[n, k] )
+ *   with C the sum of xq * q over k not in O (products of codes, fp32
+ *   accumulation: exact while partial sums stay below 2^24) and
+ *   w_hat = fp16(RN(RN(q * s_n) / 127)), the 16-bit weight the code gives
+ *   back.
+ *   X, Y: device fp16, row-major, 16-byte aligned.  The workspace (device,
+ *   16-byte aligned, nf4q_int8_workspace_bytes(M, cols) bytes) holds the
+ *   activation side after the call.  Streams the weight once per 16 rows of
+ *   X (decode-shaped; M is not limited).  M == 0 or rows == 0 launches
+ *   nothing; cols == 0 writes Y = 0. */
+nf4q_status nf4q_int8_matmul(const nf4q_int8_weight* wq, const void* X, int64_t M,
+                             float threshold, void* Y, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

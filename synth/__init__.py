@@ -123,3 +123,30 @@ def llama3_8b_matrix(layer: int, mid: int, device="cpu"):
 def llama3_8b_x(layer: int, mid: int, device="cpu"):
     _, n, k = LLAMA3_8B_LAYER[mid]
     return activations(1, k, 500000 + 1000 * layer + mid, device=device)
+
+
+# ---------------------------------------------------------------- LLM.int8()
+def outlier_activations(m: int, k: int, seed: int, *, outlier_frac: float = 0.005,
+                        outlier_scale: float = 20.0, device="cpu") -> torch.Tensor:
+    """x [m x k] fp16 ~ N(0, 1) with a few "outlier feature" columns: a
+    random floor(outlier_frac * k) of the columns (at least one when
+    outlier_frac > 0) are scaled by ``outlier_scale``, so most of their
+    values are far above 6 - the systematic large feature dimensions that
+    LLM.int8() splits off (the tutorial at mlqm.cn/news/394670, section 3.1,
+    puts them under 1 % of the dimensions)."""
+    g = _gen(seed, device)
+    x = torch.randn(m, k, generator=g, device=device, dtype=torch.float32)
+    n_out = max(1, int(outlier_frac * k)) if outlier_frac > 0 else 0
+    if n_out:
+        cols = torch.randperm(k, generator=g, device=device)[:n_out]
+        x[:, cols] *= outlier_scale
+    return x.to(torch.float16).contiguous()
+
+
+def int8_mlp70b_weight(device="cpu"):
+    """fp16 [28672 x 8192] ~ N(0, 0.015), seed 40 (the 70B MLP shape)."""
+    return normal_weight(28672, 8192, 0.015, 40, dtype=torch.float16, device=device)
+
+
+def int8_mlp70b_x(m: int, device="cpu"):
+    return outlier_activations(m, 8192, 41, device=device)

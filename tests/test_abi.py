@@ -59,6 +59,26 @@ def test_last_cuda_error_is_empty_before_any_failure(L):
     assert out == {"n": 0, "text": b"", "n_null": 0}
 
 
+def test_int8_workspace_layout_and_checks(L):
+    """Workspace bytes follow the header's layout; bad arguments are refused
+    before anything is launched."""
+    def a(v):
+        return (v + 255) // 256 * 256
+    for M, K in [(1, 16), (3, 320), (16, 4096), (40, 8192)]:
+        want = a(K) + 256 + a(4 * K) + a(4 * M) + a(2 * M * K)
+        assert L.nf4q_int8_workspace_bytes(M, K) == want
+    assert L.nf4q_int8_workspace_bytes(-1, 16) == 0
+    w = nq.NF4QInt8Weight(None, None, 8, 24)                 # cols % 16 != 0
+    assert L.nf4q_int8_quantize_weight(None, nq.IN_F16, ctypes.byref(w), None) == 1
+    assert L.nf4q_int8_matmul(ctypes.byref(w), None, 1, 6.0, None, None, 0, None) == 1
+    w = nq.NF4QInt8Weight(None, None, 8, 32)
+    assert L.nf4q_int8_quantize_weight(None, nq.IN_F32, ctypes.byref(w), None) == 1
+    assert L.nf4q_int8_matmul(ctypes.byref(w), None, 0, 6.0, None, None, 0, None) == 0
+    assert L.nf4q_int8_matmul(ctypes.byref(w), None, -1, 6.0, None, None, 0, None) == 1
+    assert L.nf4q_int8_matmul(ctypes.byref(w), None, 2, 6.0, None, None, 0, None) == 1
+    assert L.nf4q_int8_matmul(None, None, 2, 6.0, None, None, 0, None) == 1
+
+
 def test_sizes(L):
     assert nq.sizes(4096, 4096) == (4096 * 4096 // 2, 4096 * 4096 // 64, 1024)
     assert nq.sizes(28672, 8192)[2] == 14336
