@@ -305,6 +305,7 @@ int8_act_small_kernel(const uint16_t* __restrict__ X, int M, int K, float thresh
   const uint16_t* xr = X + static_cast<int64_t>(has_row ? team : 0) * K;
   float mx = 0.f;
   if (has_row) {
+#pragma unroll 4
     for (int gi = tin; gi < groups; gi += ts) {
       float f[8];
       widen8<2>(*reinterpret_cast<const uint4*>(xr + gi * 8), f);
@@ -323,6 +324,7 @@ int8_act_small_kernel(const uint16_t* __restrict__ X, int M, int K, float thresh
   for (int i = 0; i < wpt; ++i) sm = fmaxf(sm, red[team * wpt + i]);
   if (!has_row) return;
   if (tin == 0) sx[team] = sm;
+#pragma unroll 4
   for (int gi = tin; gi < groups; gi += ts) {
     float f[8];
     widen8<2>(*reinterpret_cast<const uint4*>(xr + gi * 8), f);
@@ -341,6 +343,20 @@ int8_act_small_kernel(const uint16_t* __restrict__ X, int M, int K, float thresh
     *reinterpret_cast<uint4*>(xq + static_cast<int64_t>(team) * K + gi * 8) =
         make_uint4(o[0], o[1], o[2], o[3]);
   }
+}
+
+// 4-byte asynchronous copy global -> shared; `valid` false fills zeros and
+// reads nothing.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- matmul
@@ -394,48 +410,65 @@ int8_mm_kernel(const int8_t* __restrict__ Wq, const float* __restrict__ sw,
   // the next k step's weight loads are issued before the current one is used
   uint4 wcur[4], wnext[4];
   if (warp < nchunks) load_w(warp, wcur);
-  // Outlier columns first, while the first weight chunk is in flight: up
-  // to kI8OutlierTile at a time, the CTA gathers w_hat of its 16 rows and x
-  // of its 8 NT activation rows into shared memory (independent loads, one
-  // round of latency), then each output thread runs the products in
-  // ascending k.
-  __shared__ float wo[kI8Rows][kI8OutlierTile + 1];
-  __shared__ float xo[8 * NT][kI8OutlierTile + 1];
+  // Outlier columns, kI8OutlierTile at a time.  The tile's column list is
+  // copied to shared memory; then every 4-byte word holding W[n, k] (16
+  // rows) and X[m, k] (8 NT rows) is gathered into shared memory with
+  // cp.async, which needs no registers: for the first tile the copies are
+  // issued before the main loop and land while it streams the weight.
+  // After the loop the words become w_hat and x (fp32), and one thread per
+  // output adds their products in ascending k.
+  __shared__ int32_t lst[kI8OutlierTile];
+  __shared__ uint32_t gw[kI8Rows][kI8OutlierTile + 1];
+  __shared__ uint32_t gx[8 * NT][kI8OutlierTile + 1];
   const int row = threadIdx.x & (kI8Rows - 1);
   const int col = threadIdx.x >> 4;       // 0 .. 8 NT - 1 for the output threads
   const bool outputs = threadIdx.x < kI8Rows * 8 * NT;
   const int n = n0 + row, m = m0 + col;
   float out = 0.f;
   const int no = *n_outl;
-  for (int j0 = 0; j0 < no; j0 += kI8OutlierTile) {
-    const int cnt = min(kI8OutlierTile, no - j0);
-    __syncthreads();  // the previous tile has been read
+  auto issue_tile = [&](int j0, int cnt) {
+    for (int i = threadIdx.x; i < cnt; i += kI8Threads) lst[i] = outl[j0 + i];
+    __syncthreads();
     for (int i = threadIdx.x; i < kI8Rows * cnt; i += kI8Threads) {
       const int r = i / cnt, j = i - r * cnt;
       const int nn = n0 + r;
-      float v = 0.f;
-      if (nn < N) {
-        const int k = __ldg(outl + j0 + j);
-        const float q = static_cast<float>(__ldg(Wq + static_cast<int64_t>(nn) * K + k));
-        v = __half2float(__float2half_rn(__fdiv_rn(__fmul_rn(q, __ldg(sw + nn)), kI8Levels)));
-      }
-      wo[r][j] = v;
+      const int8_t* src = Wq + static_cast<int64_t>(nn < N ? nn : 0) * K + (lst[j] & ~3);
+      cp_async_4(smem_u32(&gw[r][j]), src, nn < N);
     }
     for (int i = threadIdx.x; i < 8 * NT * cnt; i += kI8Threads) {
       const int r = i / cnt, j = i - r * cnt;
       const int mm = m0 + r;
-      float v = 0.f;
-      if (mm < M) {
-        const int k = __ldg(outl + j0 + j);
-        v = __half2float(__ushort_as_half(__ldg(X + static_cast<int64_t>(mm) * K + k)));
-      }
-      xo[r][j] = v;
+      const uint16_t* src = X + static_cast<int64_t>(mm < M ? mm : 0) * K + (lst[j] & ~1);
+      cp_async_4(smem_u32(&gx[r][j]), src, mm < M);
+    }
+    cp_async_commit();
+  };
+  auto finish_tile = [&](int cnt) {
+    cp_async_wait_all();
+    __syncthreads();
+    for (int i = threadIdx.x; i < kI8Rows * cnt; i += kI8Threads) {
+      const int r = i / cnt, j = i - r * cnt;
+      const int nn = n0 + r;
+      const int q = static_cast<int8_t>((gw[r][j] >> (8 * (lst[j] & 3))) & 0xFFu);
+      const float v = nn < N
+          ? __half2float(__float2half_rn(__fdiv_rn(__fmul_rn(static_cast<float>(q),
+                                                             __ldg(sw + nn)), kI8Levels)))
+          : 0.f;
+      gw[r][j] = __float_as_uint(v);
+    }
+    for (int i = threadIdx.x; i < 8 * NT * cnt; i += kI8Threads) {
+      const int r = i / cnt, j = i - r * cnt;
+      const uint32_t h = (gx[r][j] >> (16 * (lst[j] & 1))) & 0xFFFFu;
+      gx[r][j] = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(h))));
     }
     __syncthreads();
     if (outputs) {
-      for (int j = 0; j < cnt; ++j) out = __fmaf_rn(xo[col][j], wo[row][j], out);
+      for (int j = 0; j < cnt; ++j)
+        out = __fmaf_rn(__uint_as_float(gx[col][j]), __uint_as_float(gw[row][j]), out);
     }
-  }
+    __syncthreads();  // the tile's shared memory may be reused
+  };
+  if (no > 0) issue_tile(0, min(kI8OutlierTile, no));
   for (int kc = warp; kc < nchunks; kc += kI8Warps) {
     if (kc + kI8Warps < nchunks) load_w(kc + kI8Warps, wnext);
     const int p = kc * kI8Chunk + 32 * c;
@@ -465,6 +498,13 @@ int8_mm_kernel(const int8_t* __restrict__ Wq, const float* __restrict__ sw,
     if (kc + kI8Warps < nchunks) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) wcur[j] = wnext[j];
+    }
+  }
+  if (no > 0) {
+    finish_tile(min(kI8OutlierTile, no));
+    for (int j0 = kI8OutlierTile; j0 < no; j0 += kI8OutlierTile) {
+      issue_tile(j0, min(kI8OutlierTile, no - j0));
+      finish_tile(min(kI8OutlierTile, no - j0));
     }
   }
   // C fragment: acc[t][0..1] = rows g, columns 2c, 2c+1; [2..3] = rows g + 8
