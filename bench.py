@@ -143,20 +143,24 @@ def kernel_bytes(N, K, M=1):
 # the three weights, from one ncu capture of this script (the launch list in
 # profiles/ncu_launches_llama7b_decode_step.md).  They hold only for the
 # kernel sources they were measured on: `traffic` is reported as null as soon
-# as the digest of csrc/ differs.
-MEASURED_TRAFFIC = {"csrc_digest": "dda367bdf97f700a",
-                    "quantize_dq": 75462135, "dequantize": 36832836, "gemv": 18426778}
+# as the digest of those sources (STEP_SOURCES) differs.
+MEASURED_TRAFFIC = {"csrc_digest": "64581ecce4c6ce98",
+                    "quantize_dq": 75457172, "dequantize": 36857290, "gemv": 18425694}
+
+
+# The sources of the step's kernels and of their launch code.
+STEP_SOURCES = ("common.cuh", "tables.h", "lut.cuh", "tma.cuh", "quantize.cuh",
+                "double_quant.cuh", "dequantize.cuh", "gemv_mma.cuh", "nf4q.cu")
 
 
 def csrc_digest() -> str:
     import hashlib
     d = os.path.join(ROOT, "dequant_matmul_quantize_b300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in STEP_SOURCES:
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -238,78 +242,136 @@ def run_ours(args):
     # dequantize, gemv
     launches_per_step = 3 * (2 + 1 + 1)
 
-    def launch(m, k):
+    def launch(m, k, st=None):
         s = m["s"]
+        sp_ = (st or stream).cuda_stream
         if k == 0:
             check(L.nf4q_quantize_dq(m["w"].data_ptr(), nq.IN_BF16, R(s), m["ws"].data_ptr(),
-                                     m["ws"].numel(), sp), "quantize_dq")
+                                     m["ws"].numel(), sp_), "quantize_dq")
         elif k == 1:
-            check(L.nf4q_dequantize(R(s), m["out"].data_ptr(), sp), "dequantize")
+            check(L.nf4q_dequantize(R(s), m["out"].data_ptr(), sp_), "dequantize")
         else:
-            check(L.nf4q_gemv(R(s), m["x"].data_ptr(), 1, m["y"].data_ptr(), sp), "gemv")
+            check(L.nf4q_gemv(R(s), m["x"].data_ptr(), 1, m["y"].data_ptr(), sp_), "gemv")
 
-    def step(evs=None):
+    # The timed step.  The three weights are independent problems: each gets
+    # its own pair of streams.  On the first, quantize + double quant, then
+    # dequantize; on the second, the GEMV as soon as the weight's quantized
+    # state is ready.  Every stream first waits for the step's start and the
+    # main stream waits for all of them at its end, so the step's events
+    # bracket all of its work.
+    s_a = [torch.cuda.Stream(dev) for _ in mats]
+    s_b = [torch.cuda.Stream(dev) for _ in mats]
+    Ent = lambda: torch.cuda.Event()
+    ev_go = Ent()
+    ev_q = [Ent() for _ in mats]
+    ev_end = [Ent() for _ in range(2 * len(mats))]
+
+    def fork(main):
+        ev_go.record(main)
+        for sa, sb in zip(s_a, s_b):
+            sa.wait_event(ev_go)
+            sb.wait_event(ev_go)
+
+    def join(main):
+        for i, (sa, sb) in enumerate(zip(s_a, s_b)):
+            ev_end[2 * i].record(sa)
+            ev_end[2 * i + 1].record(sb)
+        for e in ev_end:
+            main.wait_event(e)
+
+    def step(main=None):
+        main = main or stream
+        fork(main)
+        for i, m in enumerate(mats):
+            launch(m, 0, s_a[i])
+            ev_q[i].record(s_a[i])
+            s_b[i].wait_event(ev_q[i])
+            launch(m, 2, s_b[i])
+            launch(m, 1, s_a[i])
+        join(main)
+
+    def step_serial(evs):
         j = 0
         for m in mats:
             for k in range(nphase):
-                if evs is not None:
-                    evs[j].record(stream)
+                evs[j].record(stream)
                 launch(m, k)
                 j += 1
-        if evs is not None:
-            evs[j].record(stream)
+        evs[j].record(stream)
 
-    step_bytes = sum(m["bytes"][n] for m in mats for n in names)
+    # The step as one CUDA graph (its streams become branches), so that the
+    # host's launch cost does not pace the device.
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
 
+    step_bytes = sum(m["bytes"][n] for m in mats for n in names)
     E = lambda: torch.cuda.Event(enable_timing=True)
-    per_step = [[E() for _ in range(3 * nphase + 1)] for _ in range(args.steps)]
+
+    # per-phase breakdown: the same work one kernel at a time on one stream
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n_serial = max(3, min(args.steps, 200))
+    ser = [[E() for _ in range(3 * nphase + 1)] for _ in range(n_serial)]
+    for i in range(n_serial):
+        flush()
+        step_serial(ser[i])
+    torch.cuda.synchronize()
+    kern_ms = {n: 0.0 for n in names}
+    for evs in ser:
+        for j in range(3 * nphase):
+            kern_ms[names[j % nphase]] += evs[j].elapsed_time(evs[j + 1])
+    serial_ms = sum(kern_ms.values())
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        graph.replay()
+    torch.cuda.synchronize()
+    per_step = [(E(), E()) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
             flush()
-            step(per_step[i])
+            per_step[i][0].record(stream)
+            graph.replay()
+            per_step[i][1].record(stream)
         torch.cuda.synchronize()
         barrier()
         wall = time.perf_counter() - t0
     clocks = clk.summary()
-    kern_ms = {n: 0.0 for n in names}
-    step_ms = []
-    for evs in per_step:
-        tot = 0.0
-        for j in range(3 * nphase):
-            dt = evs[j].elapsed_time(evs[j + 1])
-            kern_ms[names[j % nphase]] += dt
-            tot += dt
-        step_ms.append(tot)
-    dev_ms = sum(step_ms)
+    dev_ms = sum(a.elapsed_time(b) for a, b in per_step)
+    dom = max(kern_ms, key=kern_ms.get)            # the largest share of the serial step
+    dom_ms = kern_ms[dom] / n_serial * args.steps  # its launches, timed one by one
     dev_ms_max = slowest(dev_ms)
     ms_per_step = dev_ms_max / args.steps
     value = job_throughput(world, step_bytes, ms_per_step)
 
-    # roofline of the kernel with the largest share of the step
-    dom = max(kern_ms, key=kern_ms.get)
+    # roofline of the kernel with the largest share of the step, timed with
+    # events around each of its launches on its stream (the serial pass: the
+    # graph's nodes carry no events)
     dom_bytes = sum(m["bytes"][dom] for m in mats)      # per step, 3 launches
-    dom_ms = kern_ms[dom] / args.steps                  # per step
-    launches_dom = 3
-    achieved = (dom_bytes / launches_dom) / (dom_ms / launches_dom * 1e-3) / 1e9
+    launches_dom = 3 * args.steps
+    achieved = (dom_bytes * args.steps / launches_dom) / (dom_ms / launches_dom * 1e-3) / 1e9
     traffic_ok = csrc_digest() == MEASURED_TRAFFIC["csrc_digest"]
     roofline = {"kernel": "nf4q_" + dom, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                 "peak_source": peaks["src"] + " HBM copy bandwidth",
-                "bytes_per_launch": dom_bytes // launches_dom,
+                "bytes_per_launch": dom_bytes // 3,
                 "traffic": MEASURED_TRAFFIC.get(dom) if traffic_ok else None,
                 "traffic_note": "DRAM read+write per call from the ncu launch list; writes "
                                 "still in L2 when the kernel ends are not counted",
-                "share_of_step": round(kern_ms[dom] / dev_ms, 3)}
-    breakdown = {n: {"ms_per_step": round(kern_ms[n] / args.steps, 4),
+                "share_of_serial_step": round(kern_ms[dom] / serial_ms, 3)}
+    breakdown = {n: {"ms_per_step": round(kern_ms[n] / n_serial, 4),
                      "GB/s": round(sum(m["bytes"][n] for m in mats)
-                                   / (kern_ms[n] / args.steps * 1e-3) / 1e9, 1),
-                     "share": round(kern_ms[n] / dev_ms, 3),
+                                   / (kern_ms[n] / n_serial * 1e-3) / 1e9, 1),
+                     "share": round(kern_ms[n] / serial_ms, 3),
                      "bytes_per_call": sum(m["bytes"][n] for m in mats) // 3,
                      "traffic_per_call": MEASURED_TRAFFIC.get(n) if traffic_ok else None}
                  for n in names}
@@ -320,8 +382,14 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "bytes_per_step": step_bytes,
                    "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "streams": "one CUDA graph per step; each weight on its own two "
+                              "branches: quantize + double quant then dequantize, and the "
+                              "GEMV once the quantized state is ready",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roofline, "breakdown": breakdown,
+        "roofline": roofline,
+        "breakdown": {"note": f"the same step one kernel at a time on one stream "
+                              f"({n_serial} steps, L2 flushed), "
+                              f"{round(serial_ms / n_serial, 4)} ms per step", **breakdown},
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_region": round(wall, 4),
         "clocks": clocks,
@@ -335,12 +403,21 @@ def run_ours(args):
     d2h = sum(t.numel() * 2 for t in host_y)
 
     def e2e_step():
-        for m, hw, hx, hy in zip(mats, host_w, host_x, host_y):
-            m["w"].copy_(hw, non_blocking=True)
-            m["x"].copy_(hx, non_blocking=True)
-            for k in range(nphase):
-                launch(m, k)
-            hy.copy_(m["y"], non_blocking=True)
+        # the same streams as the timed step: each weight's inputs are copied
+        # in on its first stream, its y copied out after its GEMV
+        fork(stream)
+        for i, (m, hw, hx, hy) in enumerate(zip(mats, host_w, host_x, host_y)):
+            with torch.cuda.stream(s_a[i]):
+                m["w"].copy_(hw, non_blocking=True)
+                m["x"].copy_(hx, non_blocking=True)
+            launch(m, 0, s_a[i])
+            ev_q[i].record(s_a[i])
+            s_b[i].wait_event(ev_q[i])
+            launch(m, 2, s_b[i])
+            with torch.cuda.stream(s_b[i]):
+                hy.copy_(m["y"], non_blocking=True)
+            launch(m, 1, s_a[i])
+        join(stream)
 
     e2e_steps = max(3, min(args.steps, 50))
     for _ in range(2):
