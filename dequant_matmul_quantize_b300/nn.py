@@ -20,6 +20,12 @@ This module does the same for libnf4q:
   w_hat by ``nf4q.matmul_dx`` (nf4q_matmul_dx, a tcgen05 kernel that
   dequantizes w_hat tile by tile, as the forward GEMM does) - the backward
   of a 4-bit base layer under LoRA ("bitsandbytes tutorial", sec. 5.4).
+* ``Linear8bitLt`` is the LLM.int8() layer the pages name beside
+  ``Linear4bit`` ("bitsandbytes: quantifier un modele PyTorch sans quitter
+  PyTorch"; "bitsandbytes tutorial", sec. 3.1 and ``llm_int8_threshold`` in
+  sec. 四): an fp16 weight stored as per-row int8 codes, and the
+  decomposition matmul through ``nf4q.int8_quantize_weight`` /
+  ``nf4q.int8_matmul``.
 """
 from __future__ import annotations
 
@@ -28,7 +34,9 @@ from typing import Optional, Tuple
 import torch
 from torch import Tensor
 
-from . import (DTYPES, QuantizedWeight, dequantize as _dequantize, matmul as _matmul,
+from . import (DTYPES, INT8_DEFAULT_THRESHOLD, Int8Weight, QuantizedWeight,
+               dequantize as _dequantize, int8_matmul as _int8_matmul,
+               int8_quantize_weight as _int8_quantize_weight, matmul as _matmul,
                matmul_dx as _matmul_dx, quantize as _quantize, sizes)
 
 _TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16}
@@ -122,6 +130,31 @@ def _matmul_backward(ctx, grad_y):
 matmul_op.register_autograd(_matmul_backward, setup_context=_matmul_setup_context)
 
 
+@torch.library.custom_op("nf4q::int8_quantize_weight", mutates_args=())
+def int8_quantize_weight_op(w: Tensor) -> Tuple[Tensor, Tensor]:
+    """w [rows x cols] (fp16 / bf16, CUDA) -> (int8 codes, fp32 row absmax)."""
+    wq = _int8_quantize_weight(w.contiguous())
+    return wq.q, wq.scale
+
+
+@int8_quantize_weight_op.register_fake
+def _(w):
+    return (w.new_empty(w.shape[0], w.shape[1], dtype=torch.int8),
+            w.new_empty(w.shape[0], dtype=torch.float32))
+
+
+@torch.library.custom_op("nf4q::int8_matmul", mutates_args=())
+def int8_matmul_op(x: Tensor, q: Tensor, scale: Tensor, threshold: float) -> Tensor:
+    """y [M x rows] = the LLM.int8() decomposition matmul of x [M x cols] (fp16)
+    with the int8 weight (nf4q_int8_matmul)."""
+    return _int8_matmul(Int8Weight(q, scale, q.shape[0], q.shape[1]), x.contiguous(), threshold)
+
+
+@int8_matmul_op.register_fake
+def _(x, q, scale, threshold):
+    return x.new_empty(x.shape[0], q.shape[0], dtype=torch.float16)
+
+
 # ---------------------------------------------------------------- module
 class Linear4bit(torch.nn.Module):
     """y = x @ w_hat.T + bias with the weight stored as 4-bit codes.
@@ -194,3 +227,55 @@ class Linear4bit(torch.nn.Module):
         return (f"in_features={self.in_features}, out_features={self.out_features}, "
                 f"code={self.code}, double_quant={self.double_quant}, "
                 f"compute_dtype={self.compute_dtype}, bias={self.bias is not None}")
+
+
+class Linear8bitLt(torch.nn.Module):
+    """y = x @ w_hat.T + bias with the weight stored as per-row int8 codes and
+    the LLM.int8() decomposition: activation columns with a value above
+    ``threshold`` (6.0 by default) in fp16, the rest in int8.  fp16 in and out;
+    inference only (the int8 weight is frozen)."""
+
+    def __init__(self, in_features: int, out_features: int, bias: bool = True,
+                 threshold: float = INT8_DEFAULT_THRESHOLD, device=None):
+        super().__init__()
+        if in_features % 16:
+            raise ValueError("in_features must be a multiple of 16")
+        self.in_features, self.out_features, self.threshold = in_features, out_features, threshold
+        dev = torch.device(device) if device is not None else torch.device("cuda")
+        self.register_buffer("q", torch.zeros(out_features, in_features, dtype=torch.int8,
+                                              device=dev))
+        self.register_buffer("scale", torch.zeros(out_features, dtype=torch.float32, device=dev))
+        if bias:
+            self.register_buffer("bias", torch.zeros(out_features, dtype=torch.float16, device=dev))
+        else:
+            self.bias = None
+
+    @classmethod
+    def from_weight(cls, weight: Tensor, bias: Optional[Tensor] = None,
+                    threshold: float = INT8_DEFAULT_THRESHOLD) -> "Linear8bitLt":
+        out_f, in_f = weight.shape
+        m = cls(in_f, out_f, bias is not None, threshold, device=weight.device)
+        q, scale = torch.ops.nf4q.int8_quantize_weight(weight)
+        m.q.copy_(q)
+        m.scale.copy_(scale)
+        if bias is not None:
+            m.bias.copy_(bias.to(torch.float16))
+        return m
+
+    @classmethod
+    def from_linear(cls, linear: torch.nn.Linear,
+                    threshold: float = INT8_DEFAULT_THRESHOLD) -> "Linear8bitLt":
+        return cls.from_weight(linear.weight.detach().to(torch.float16),
+                               None if linear.bias is None else linear.bias.detach(), threshold)
+
+    def forward(self, x: Tensor) -> Tensor:
+        lead = x.shape[:-1]
+        y = torch.ops.nf4q.int8_matmul(x.reshape(-1, self.in_features), self.q, self.scale,
+                                       float(self.threshold))
+        if self.bias is not None:
+            y = y + self.bias
+        return y.reshape(*lead, self.out_features)
+
+    def extra_repr(self) -> str:
+        return (f"in_features={self.in_features}, out_features={self.out_features}, "
+                f"threshold={self.threshold}, bias={self.bias is not None}")

@@ -7,11 +7,12 @@ import torch
 
 import dequant_matmul_quantize_b300 as nq
 import synth
-from dequant_matmul_quantize_b300.nn import Linear4bit
+from dequant_matmul_quantize_b300.nn import Linear4bit, Linear8bitLt
 
 
 def test_operators_are_registered():
-    for name in ("quantize", "dequantize", "matmul", "matmul_dx"):
+    for name in ("quantize", "dequantize", "matmul", "matmul_dx", "int8_quantize_weight",
+                 "int8_matmul"):
         assert hasattr(torch.ops.nf4q, name)
 
 
@@ -30,6 +31,20 @@ def test_fake_shapes_and_dtypes():
         assert y.shape == (5, 96) and y.dtype == torch.float16
         dx = torch.ops.nf4q.matmul_dx(y, *st, 96, 256, "nf4", True, "f16")
         assert dx.shape == (5, 256) and dx.dtype == torch.float16
+
+
+def test_int8_fake_shapes_and_export():
+    from torch._subclasses.fake_tensor import FakeTensorMode
+    with FakeTensorMode():
+        w = torch.empty(48, 64, dtype=torch.float16)
+        q, sc = torch.ops.nf4q.int8_quantize_weight(w)
+        assert q.shape == (48, 64) and q.dtype == torch.int8 and sc.shape == (48,)
+        y = torch.ops.nf4q.int8_matmul(torch.empty(3, 64, dtype=torch.float16), q, sc, 6.0)
+        assert y.shape == (3, 48) and y.dtype == torch.float16
+    m = Linear8bitLt(64, 32, bias=True, device="cpu")
+    ep = torch.export.export(m, (torch.empty(2, 5, 64, dtype=torch.float16),))
+    targets = [str(n.target) for n in ep.graph.nodes if n.op == "call_function"]
+    assert any("nf4q.int8_matmul" in t for t in targets), targets
 
 
 def test_export_traces_through_the_operator():
@@ -100,3 +115,41 @@ def test_backward_through_frozen_base(compute_dtype, rows):
     tol = 4e-3 * (gy.float().abs() @ w_hat.abs()) + 1e-30
     assert bool((err <= tol).all())
     assert lin.packed.grad is None
+
+
+@pytest.mark.gpu
+def test_linear8bitlt_matches_binding_and_compiles():
+    """Linear8bitLt gives the binding's int8 matmul (+ bias) bit for bit, in
+    eager mode and under torch.compile(fullgraph=True)."""
+    w = synth.normal_weight(96, 256, 0.02, seed=31, dtype=torch.float16).cuda()
+    b = synth.normal_weight(1, 96, 0.1, seed=32, dtype=torch.float16).cuda().reshape(-1)
+    lin = Linear8bitLt.from_weight(w, b)
+    x = synth.outlier_activations(12, 256, seed=33, outlier_frac=0.02).cuda().reshape(3, 4, 256)
+    y = lin(x)
+    wq = nq.int8_quantize_weight(w)
+    ref = nq.int8_matmul(wq, x.reshape(12, 256)) + b.to(torch.float16)
+    torch.cuda.synchronize()
+    assert torch.equal(lin.q, wq.q) and torch.equal(lin.scale, wq.scale)
+    assert torch.equal(y.reshape(12, 96), ref)
+    compiled = torch.compile(lin, fullgraph=True, backend="aot_eager")
+    assert torch.equal(compiled(x), y)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("code,dq", [("fp4", True), ("nf4", False), ("fp4", False)])
+def test_linear4bit_other_configs_forward_and_backward(code, dq):
+    """The module over the rest of the config matrix (FP4, no double quant):
+    forward equals the binding; the input gradient is dY . w_hat."""
+    w = synth.normal_weight(128, 320, 0.02, seed=41).cuda()
+    lin = Linear4bit.from_weight(w, None, code, dq, "bf16")
+    qw = nq.quantize(w, code, dq)
+    x = synth.activations(70, 320, seed=42).cuda().requires_grad_(True)
+    y = lin(x)
+    assert torch.equal(y, nq.matmul(qw, x.detach()))
+    gy = synth.activations(70, 128, seed=43).cuda()
+    y.backward(gy)
+    w_hat = nq.dequantize(qw).float()
+    ref = gy.float() @ w_hat
+    torch.cuda.synchronize()
+    tol = 4e-3 * (gy.float().abs() @ w_hat.abs()) + 1e-30
+    assert bool(((x.grad.float() - ref).abs() <= tol).all())
