@@ -10,6 +10,7 @@ Each case builds its seeded synthetic input, runs the library call twice
     gemv4096     nf4q_gemv M=1 on the 4096x4096 decode weight
     gemv70b_m16  nf4q_gemv M=16 on the 28672x8192 weight (NF4)
     gemm2048     nf4q_gemm M=2048 on the 14336x4096 prefill weight
+    gemm64       nf4q_gemm M=64 on the 14336x4096 prefill weight
     dx2048       nf4q_matmul_dx M=2048 on the 14336x4096 prefill weight
     int8_m1      nf4q_int8_quantize_weight, then nf4q_int8_matmul M=1 and
                  M=16, on the fp16 28672x8192 weight (LLM.int8())
@@ -64,13 +65,14 @@ def _run(case: str, torch, nq, synth) -> None:
         y = torch.empty(1, qw.rows, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
             ok(L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), sp), "gemv")
-    elif case == "gemm2048":
+    elif case in ("gemm2048", "gemm64"):
+        M = 2048 if case == "gemm2048" else 64
         qw = nq.quantize(synth.prefill_weight(device=dev))
         s = qw.struct()
-        x = synth.prefill_x(2048, device=dev)
-        y = torch.empty(2048, qw.rows, dtype=torch.bfloat16, device=dev)
+        x = synth.prefill_x(M, device=dev)
+        y = torch.empty(M, qw.rows, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
-            ok(L.nf4q_gemm(R(s), x.data_ptr(), 2048, y.data_ptr(), sp), "gemm")
+            ok(L.nf4q_gemm(R(s), x.data_ptr(), M, y.data_ptr(), sp), "gemm")
     elif case == "dx2048":
         qw = nq.quantize(synth.prefill_weight(device=dev))
         s = qw.struct()
