@@ -711,33 +711,52 @@ def _limit_threads():
         return None
 
 
-def oracle_sample(rows=1024):
-    """The oracle's whole path on the first `rows` rows of the [4096x4096]
-    decode weight: quantize, double quant, dequantize, fp64 GEMV.  Returns
-    (seconds, algorithmic bytes of the same work on the GPU path)."""
+_DECODE_CPU = None
+
+
+def _decode_cpu():
+    """The three decode weights and their x rows on the CPU (drawn once)."""
+    global _DECODE_CPU
+    if _DECODE_CPU is None:
+        import synth
+        _DECODE_CPU = [synth.llama7b_decode(i, device="cpu") for i in range(3)]
+    return _DECODE_CPU
+
+
+def oracle_sample(rows=None, weights=(0, 1, 2)):
+    """The oracle's whole path - quantize, double quant, dequantize, fp64
+    GEMV - on the first `rows` rows (all if None) of the given decode
+    weights.  Returns (seconds, algorithmic bytes of the same work on the GPU
+    path)."""
     import numpy as np
     import torch
-    import synth
     from oracle import nf4_oracle as o
-    w, x = synth.llama7b_decode(0, device="cpu")
-    w = w[:rows].float().numpy()
-    xb = x.view(torch.int16).numpy().view(np.uint16)
-    t0 = time.perf_counter()
-    r = o.quantize_full(w)
-    o.matmul_ref(xb, r["w_hat"].reshape(w.shape))
-    dt = time.perf_counter() - t0
-    return dt, sum(kernel_bytes(rows, w.shape[1]).values())
+    tot, by = 0.0, 0
+    for i in weights:
+        w, x = _decode_cpu()[i]
+        wf = (w if rows is None else w[:rows]).float().numpy()
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        r = o.quantize_full(wf)
+        o.matmul_ref(xb, r["w_hat"].reshape(wf.shape))
+        tot += time.perf_counter() - t0
+        by += sum(kernel_bytes(*wf.shape).values())
+    return tot, by
 
 
 def cpu_baseline_sample():
+    """One whole decode step of the oracle (all three weights, every row),
+    single-threaded: about 10-20 s on a server core."""
+    import os
     lim = _limit_threads()
-    dt, b = oracle_sample(1024)
+    dt, b = oracle_sample()
     if lim is not None:
         lim.unregister() if hasattr(lim, "unregister") else None
     return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "seconds": round(dt, 3),
-            "sample": "rows 0..1023 of the 4096x4096 decode weight: quantize + double "
-                      "quant + dequantize + fp64 GEMV (NumPy, one thread)"}
+            "host_cpus": os.cpu_count(), "affinity": len(os.sched_getaffinity(0)),
+            "sample": "one whole step: the three decode weights, every row - quantize + "
+                      "double quant + dequantize + fp64 GEMV (NumPy, one thread)"}
 
 
 def run_reference(args):
@@ -745,12 +764,12 @@ def run_reference(args):
     if rank != 0:
         return
     lim = _limit_threads()
-    rows = 256
+    rows = 128  # per step, so that a run of --steps 1000 ends in a couple of minutes
     for _ in range(max(3, args.warmup)):
-        oracle_sample(rows)
+        oracle_sample(rows, weights=(0,))
     tot, b = 0.0, 0
     for _ in range(args.steps):
-        dt, bb = oracle_sample(rows)
+        dt, bb = oracle_sample(rows, weights=(0,))
         tot += dt
         b += bb
     value = b / tot / 1e9
