@@ -346,7 +346,11 @@ def run_ours(args):
         barrier()
         wall = time.perf_counter() - t0
     clocks = clk.summary()
-    dev_ms = sum(a.elapsed_time(b) for a, b in per_step)
+    step_times = sorted(a.elapsed_time(b) for a, b in per_step)
+    dev_ms = sum(step_times)
+
+    def pct(q):
+        return round(step_times[min(len(step_times) - 1, int(q * len(step_times)))], 4)
     dom = max(kern_ms, key=kern_ms.get)            # the largest share of the serial step
     dom_ms = kern_ms[dom] / n_serial * args.steps  # its launches, timed one by one
     dev_ms_max = slowest(dev_ms)
@@ -379,6 +383,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "bytes_per_step": step_bytes,
                    "l2": "flushed before every step (256 MiB write, outside the events)",
