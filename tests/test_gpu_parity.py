@@ -310,6 +310,43 @@ def test_llama3_stack_matrices(layer, mid):
     _sampled_full_size(w, "nf4", [x], n_rows=16, seed=layer * 10 + mid)
 
 
+def test_beyond_2_31_elements():
+    """A 32768 x 65536 weight (2^31 elements, 4 GB bf16): every index above
+    2^31 must be 64-bit.  Codes and absmax of sampled rows against the oracle;
+    their dequantized rows against the oracle's formula on the GPU's stored
+    scales; the GEMV on those rows within the matmul tolerance."""
+    N, K = 32768, 65536
+    w = synth.normal_weight(N, K, 0.02, seed=77, device="cuda")
+    qw = nq.quantize(w)
+    x = synth.activations(1, K, seed=78, device="cuda")
+    y = nq.gemv(qw, x)
+    torch.cuda.synchronize()
+    kb = K // 64
+    rows = np.unique(np.concatenate([[0, 1, N // 2, N - 1],
+                                     np.random.default_rng(79).integers(0, N, 8)]))
+    idx = torch.from_numpy(rows).cuda()
+    packed = qw.packed.view(N, K // 2)[idx].cpu().numpy()
+    absmax = qw.absmax.view(N, kb)[idx].cpu().numpy()
+    aq = qw.absmax_q.view(N, kb)[idx].cpu().numpy()
+    s2 = qw.scale2.cpu().numpy()
+    off = np.float32(qw.offset.cpu().numpy()[0])
+    w_rows = as_f32(w[idx])
+    del w
+    what = []
+    for i, r in enumerate(rows):
+        p_ref, a_ref = o.quantize(w_rows[i])
+        assert_bits_equal(packed[i], p_ref, f"packed row {r}")
+        assert_bits_equal(absmax[i], a_ref, f"absmax row {r}")
+        b = np.arange(kb, dtype=np.int64) + int(r) * kb      # global block indices
+        sc = o.fma_f32(aq[i].astype(np.float32), s2[b // 256], off)
+        what.append(o.dequantize(p_ref, sc))
+    what = np.stack(what)
+    dq = nq.dequantize(qw)
+    assert_bits_equal(bf16_bits(dq[idx]).reshape(-1), what.reshape(-1), "w_hat rows")
+    del dq
+    check_matmul(bf16_bits(y[:, idx]), bf16_bits(x), what, "gemv 32768x65536")
+
+
 # ---------------------------------------------------------------- errors
 def test_bad_arguments_leave_gpu_usable():
     w = synth.normal_weight(64, 256, 0.02, seed=1).cuda()
