@@ -21,7 +21,8 @@
 //               Afterwards the 16 warps drain the two accumulators
 //               (tcgen05.ld), round to bf16 and store Y.
 // BN (128..256) is picked per shape so the tile count fills whole waves of
-// the SMs.  Every wait is bounded (1 s of %globaltimer); a wait that gives up
+// the SMs.  For M <= 128 a CTA has one accumulator (128 x 128 tiles) and,
+// with X stages half the size, an 8-stage TMA ring.  Every wait is bounded (1 s of %globaltimer); a wait that gives up
 // sets bit 0 of the device error word and the CTA winds down: its other
 // waits stop, its TMA copies and MMAs are drained (bounded), its TMEM freed.
 // No multicast: every CTA loads its own tiles.
@@ -41,12 +42,15 @@ constexpr int kGemmBK = 64;
 constexpr int kGemmATile = kGemmBM * kGemmBK * 2;    // 16 KB
 constexpr int kGemmTmemCols = 512;
 
-template <int BN>
+// MT = X tiles (128-row accumulators) per CTA: 2, or 1 for M <= 128, where
+// the smaller TMA stages leave room for a deeper ring.
+template <int BN, int MT = 2>
 struct GemmCfg {
   static constexpr int kBTile = BN * kGemmBK * 2;     // bf16 W tile
   static constexpr int kPTile = BN * kGemmBK / 2;     // packed W tile
-  static constexpr int kAStages = 4;                  // TMA stages: 2 X tiles + packed W
-  static constexpr int kAStage = 2 * kGemmATile + kPTile;
+  static constexpr int kAStages =                     // TMA stages: MT X tiles + packed W
+      MT == 2 ? 4 : (BN <= 128 ? 8 : 6);
+  static constexpr int kAStage = MT * kGemmATile + kPTile;
   static constexpr int kBStages =                     // dequantized W stages
       (kAStages * kAStage + 3 * kBTile + 2048 <= 232448 - 1024) ? 3 : 2;
   static constexpr size_t kSmem = 1024 + kAStages * kAStage + kBStages * kBTile + 1024;
@@ -57,6 +61,7 @@ struct GemmCfg {
   static constexpr int kThreads = 64 + kGroups * 256;   // + TMA warp and MMA warp
   static_assert(kPTile % 1024 == 0 && kBTile % 1024 == 0, "1 KB alignment of tiles");
   static_assert(kSmem <= 232448, "shared memory");
+  static_assert(MT == 1 || MT == 2, "one or two accumulators");
 };
 
 // Scale inputs of one W row for 16 consecutive k-steps (64-blocks): the 16
@@ -124,12 +129,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // from ((w - 2) / 8) * 32), round to the compute dtype and store rows
 // m0 .. m0 + 255 (< M) and columns c0 .. c0 + BN - 1 (< ncols) of the
 // row-major Y [M x ncols].
-template <int BN, int DT>
+template <int BN, int DT, int MT = 2>
 __device__ __forceinline__ void store_accumulators(uint32_t tmem, int warp, int lane,
                                                    uint16_t* __restrict__ Y, int M, int ncols,
                                                    int m0, int c0) {
   const int q = warp & 3;
   const int h = ((warp - 2) >> 2) & 1;
+  if (h >= MT) return;  // a CTA with one accumulator owns only its first 128 rows
   const int cc = ((warp - 2) >> 3) * 32;
   const int m = m0 + h * kGemmBM + q * 32 + lane;
   uint16_t* yrow = Y + static_cast<int64_t>(m) * ncols + c0;
@@ -161,20 +167,20 @@ __device__ __forceinline__ void store_accumulators(uint32_t tmem, int warp, int 
 }
 
 // ------------------------------------------------------------ the kernel
-template <int CODE, int BN, int DT>
-__global__ void __launch_bounds__(GemmCfg<BN>::kThreads, 1)
+template <int CODE, int BN, int DT, int MT>
+__global__ void __launch_bounds__(GemmCfg<BN, MT>::kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
             const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
             uint16_t* __restrict__ Y, int M, int N, int K,
             const __grid_constant__ CodeValues C) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, MT>;
   constexpr int SA = Cfg::kAStages, SB = Cfg::kBStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   auto sA = [&](int s, int h) { return base + s * Cfg::kAStage + h * kGemmATile; };
-  auto sP = [&](int s) { return base + s * Cfg::kAStage + 2 * kGemmATile; };
+  auto sP = [&](int s) { return base + s * Cfg::kAStage + MT * kGemmATile; };
   auto sB = [&](int s) { return base + SA * Cfg::kAStage + s * Cfg::kBTile; };
   const uint32_t sBar = base + SA * Cfg::kAStage + SB * Cfg::kBTile;   // 1 KB of barriers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sBar - base) + 512);
@@ -188,7 +194,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const uint32_t acc_bar = sBar + 8u * (2 * SA + 2 * SB);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (2 * kGemmBM);
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (MT * kGemmBM);
   const int KT = K / kGemmBK;
 
   if (threadIdx.x == 0) {
@@ -226,9 +232,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const int s = kt % SA;
         const uint32_t ph = (kt / SA) & 1;
         if (!mbar_wait(aempty_bar(s), ph ^ 1, abort)) break;
-        mbar_arrive_expect_tx(full_bar(s), 2 * kGemmATile + Cfg::kPTile);
+        mbar_arrive_expect_tx(full_bar(s), MT * kGemmATile + Cfg::kPTile);
         tma_load_2d(sA(s, 0), &tmap_x, kt * kGemmBK, m0, full_bar(s));
-        tma_load_2d(sA(s, 1), &tmap_x, kt * kGemmBK, m0 + kGemmBM, full_bar(s));
+        if (MT == 2) tma_load_2d(sA(s, 1), &tmap_x, kt * kGemmBK, m0 + kGemmBM, full_bar(s));
         tma_load_2d(sP(s), &tmap_w, kt * (kGemmBK / 2), n0, full_bar(s));
         issued = kt + 1;
       }
@@ -249,7 +255,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
           const uint64_t bdesc = smem_desc_sw128(sB(sb) + 32 * k);
           const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
           mma_bf16(tmem, smem_desc_sw128(sA(sa, 0) + 32 * k), bdesc, idesc, acc);
-          mma_bf16(tmem + 256, smem_desc_sw128(sA(sa, 1) + 32 * k), bdesc, idesc, acc);
+          if (MT == 2) mma_bf16(tmem + 256, smem_desc_sw128(sA(sa, 1) + 32 * k), bdesc, idesc, acc);
         }
         mma_commit(aempty_bar(sa));
         mma_commit(bempty_bar(sb));
@@ -339,7 +345,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // ---------------- epilogue: TMEM -> bf16 -> Y
     if (warp < 18 && __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
       tc_fence_after();
-      store_accumulators<BN, DT>(tmem, warp, lane, Y, M, N, m0, n0);
+      store_accumulators<BN, DT, MT>(tmem, warp, lane, Y, M, N, m0, n0);
     }
   }
   tc_fence_before();
@@ -377,10 +383,10 @@ inline int gemm_pick_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-template <int CODE, int BN, int DT>
+template <int CODE, int BN, int DT, int MT = 2>
 inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, const ScaleView& sv,
                                   const CodeValues& C, int64_t M, void* Y, cudaStream_t stream) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, MT>;
   const int64_t N = wq->rows, K = wq->cols;
   EncodeTiledFn enc = encode_tiled_fn();
   CUtensorMap tw;
@@ -403,7 +409,7 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(gemm_kernel<CODE, BN, DT>,
+      st = cuda_check(cudaFuncSetAttribute(gemm_kernel<CODE, BN, DT, MT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(Cfg::kSmem)),
                       "cudaFuncSetAttribute (GEMM)");
@@ -412,8 +418,8 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
     }
   }
   dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
-            static_cast<unsigned>((M + 2 * kGemmBM - 1) / (2 * kGemmBM)));
-  return launch("gemm_kernel", gemm_kernel<CODE, BN, DT>, grid, dim3(Cfg::kThreads), Cfg::kSmem,
+            static_cast<unsigned>((M + MT * kGemmBM - 1) / (MT * kGemmBM)));
+  return launch("gemm_kernel", gemm_kernel<CODE, BN, DT, MT>, grid, dim3(Cfg::kThreads), Cfg::kSmem,
                 stream, nullptr, 0, tx, tw, sv, static_cast<uint16_t*>(Y), static_cast<int>(M),
                 static_cast<int>(N), static_cast<int>(K), C);
 }
@@ -422,6 +428,9 @@ template <int CODE, int DT>
 inline nf4q_status gemm_launch_code(const CUtensorMap& tx, const nf4q_weight* wq,
                                     const ScaleView& sv, const CodeValues& C, int64_t M, void* Y,
                                     cudaStream_t stream, int bn) {
+  // M <= 128: one accumulator per CTA and 128-row W tiles, with the deeper
+  // TMA ring the smaller stages allow
+  if (M <= kGemmBM) return gemm_launch_bn<CODE, 128, DT, 1>(tx, wq, sv, C, M, Y, stream);
   switch (bn) {
     case 224: return gemm_launch_bn<CODE, 224, DT>(tx, wq, sv, C, M, Y, stream);
     case 192: return gemm_launch_bn<CODE, 192, DT>(tx, wq, sv, C, M, Y, stream);
