@@ -30,7 +30,9 @@ def _oracle_what(w, code):
 
 @pytest.mark.parametrize("M,N,K", [
     (1, 256, 64), (64, 256, 256), (128, 512, 512), (200, 300, 320), (129, 257, 192),
-    (256, 1000, 1024), (383, 768, 2048), (512, 256, 4096)])
+    (256, 1000, 1024), (383, 768, 2048), (512, 256, 4096),
+    # one-accumulator CTAs (M <= 128) with ragged N and K
+    (100, 300, 320), (128, 200, 4160), (1, 129, 64), (77, 1000, 192)])
 def test_gemm_small(M, N, K):
     w = synth.normal_weight(N, K, 0.02, seed=N + K, outlier_frac=1e-3)
     x = synth.activations(M, K, seed=M)
