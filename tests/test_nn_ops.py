@@ -153,3 +153,24 @@ def test_linear4bit_other_configs_forward_and_backward(code, dq):
     torch.cuda.synchronize()
     tol = 4e-3 * (gy.float().abs() @ w_hat.abs()) + 1e-30
     assert bool(((x.grad.float() - ref).abs() <= tol).all())
+
+
+@pytest.mark.gpu
+def test_from_linear_and_state_dict_round_trip():
+    """Both modules built from an nn.Linear; their state (codes, scales, bias)
+    survives a state_dict round trip into fresh modules bit for bit."""
+    torch.manual_seed(0)
+    lin = torch.nn.Linear(256, 96, bias=True).cuda()
+    m4 = Linear4bit.from_linear(lin, "nf4", True, "bf16")
+    fresh4 = Linear4bit(256, 96, True, "nf4", True, "bf16")
+    fresh4.load_state_dict(m4.state_dict())
+    x = synth.activations(5, 256, seed=51).cuda()
+    assert torch.equal(fresh4(x), m4(x))
+    ref = nq.matmul(nq.quantize(lin.weight.detach()), x) + lin.bias.detach().to(torch.bfloat16)
+    assert torch.equal(m4(x), ref)
+    m8 = Linear8bitLt.from_linear(lin)
+    fresh8 = Linear8bitLt(256, 96, True)
+    fresh8.load_state_dict(m8.state_dict())
+    x16 = synth.outlier_activations(5, 256, seed=52, outlier_frac=0.02).cuda()
+    torch.cuda.synchronize()
+    assert torch.equal(fresh8(x16), m8(x16))
