@@ -41,7 +41,6 @@ namespace nf4q {
 constexpr int kGemvRows = 16;       // rows of one MMA tile
 constexpr int kGemvSeg = 256;       // columns per warp per stage (128 packed bytes a row)
 constexpr int kGemvWarps = 4;       // warps per CTA = segments per stage
-constexpr int kGemvChunk = kGemvSeg * kGemvWarps;  // columns per stage
 constexpr int kGemvMaxStages = 4;
 constexpr int kGemvStages = 2;      // stages used (more cost occupancy, measured slower)
 constexpr int kGemvMinCtasPerSm = 4;
