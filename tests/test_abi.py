@@ -35,6 +35,46 @@ def test_exports_every_declared_symbol(L):
     assert not missing, missing
 
 
+def _prototypes():
+    """{name: number of parameters} of every function declared in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(nf4q_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(L):
+    """Every function the binding declares has the header's parameter count
+    (a drifted binding would pass wrong arguments silently)."""
+    protos = _prototypes()
+    assert len(protos) == len(_declared_functions())
+    for name, n in protos.items():
+        f = getattr(L, name)
+        if f.argtypes is not None:
+            assert len(f.argtypes) == n, (name, len(f.argtypes), n)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/nf4q.h compiles as C99 and as C++ (no CUDA or torch types)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use.c"
+    src.write_text('#include "nf4q.h"\nint main(void) { nf4q_weight w = {0}; '
+                   'nf4q_int8_weight q = {0}; (void)w; (void)q; '
+                   'return (int)nf4q_sizes(64, 64, 64, 256, 0, 0, 0); }\n')
+    for cmd in ([gcc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only"],
+                [shutil.which("g++") or gcc, "-x", "c++", "-std=c++17", "-Wall", "-Werror",
+                 "-fsyntax-only"]):
+        r = subprocess.run(cmd + ["-I", os.path.dirname(HEADER), str(src)],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_version_and_status_strings(L):
     assert L.nf4q_version() >> 16 == 1
     for s in range(7):
