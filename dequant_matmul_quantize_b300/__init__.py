@@ -132,6 +132,15 @@ def lib() -> ctypes.CDLL:
     return L
 
 
+_IN_DTYPES = {torch.float32: IN_F32, torch.bfloat16: IN_BF16, torch.float16: IN_F16}
+
+
+def _require(cond: bool, what: str):
+    """Argument check of the binding (raised even under python -O)."""
+    if not cond:
+        raise ValueError(what)
+
+
 def _check(func: str, status: int):
     if status != 0:
         raise Nf4qError(func, status, last_cuda_error() if status == 5 else "")
@@ -213,9 +222,11 @@ class QuantizedWeight:
 
 # ------------------------------------------------------------------ ops
 def quantize_into(qw: QuantizedWeight, w: torch.Tensor, stream=None):
-    """nf4q_quantize: writes qw.packed and qw.absmax from w (fp32 or bf16)."""
-    assert w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols)
-    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16, torch.float16: IN_F16}[w.dtype]
+    """nf4q_quantize: writes qw.packed and qw.absmax from w (fp32, bf16 or fp16)."""
+    _require(w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols),
+             "w must be a contiguous CUDA tensor of the weight's shape")
+    _require(w.dtype in _IN_DTYPES, "w must be fp32, bf16 or fp16")
+    dt = _IN_DTYPES[w.dtype]
     s = qw.struct()
     _check("nf4q_quantize", lib().nf4q_quantize(_ptr(w), dt, ctypes.byref(s), _stream(stream)))
 
@@ -238,8 +249,10 @@ def double_quant_into(qw: QuantizedWeight, workspace: Optional[torch.Tensor] = N
 def quantize_dq_into(qw: QuantizedWeight, w: torch.Tensor,
                      workspace: Optional[torch.Tensor] = None, stream=None):
     """nf4q_quantize_dq: quantize and double-quantize w into qw in one call."""
-    assert w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols)
-    dt = {torch.float32: IN_F32, torch.bfloat16: IN_BF16, torch.float16: IN_F16}[w.dtype]
+    _require(w.is_cuda and w.is_contiguous() and tuple(w.shape) == (qw.rows, qw.cols),
+             "w must be a contiguous CUDA tensor of the weight's shape")
+    _require(w.dtype in _IN_DTYPES, "w must be fp32, bf16 or fp16")
+    dt = _IN_DTYPES[w.dtype]
     if workspace is None:
         workspace = dq_workspace(qw.absmax.numel(), qw.absmax.device)
     s = qw.struct()
@@ -272,8 +285,9 @@ def dequantize(qw: QuantizedWeight, out: Optional[torch.Tensor] = None,
 
 
 def _mm(name: str, qw: QuantizedWeight, x: torch.Tensor, out, stream):
-    assert x.is_cuda and x.dtype == qw.torch_dtype and x.is_contiguous()
-    assert x.shape[-1] == qw.cols
+    _require(x.is_cuda and x.dtype == qw.torch_dtype and x.is_contiguous() and x.dim() == 2,
+             "x must be a contiguous 2-D CUDA tensor of the compute dtype")
+    _require(x.shape[-1] == qw.cols, "x must have the weight's number of columns")
     M = x.shape[0]
     if out is None:
         out = torch.empty(M, qw.rows, dtype=qw.torch_dtype, device=x.device)
@@ -301,8 +315,10 @@ def matmul_dx(qw, dy, out=None, stream=None):
     """dX = dY . w_hat (the input gradient through the frozen 4-bit weight)
     on the tcgen05 tensor cores.  dy [M, rows] may have a row pitch larger
     than rows (a column slice of a wider tensor) if it is a multiple of 8."""
-    assert dy.is_cuda and dy.dtype == qw.torch_dtype and dy.dim() == 2
-    assert dy.shape[1] == qw.rows and dy.stride(1) == 1
+    _require(dy.is_cuda and dy.dtype == qw.torch_dtype and dy.dim() == 2,
+             "dy must be a 2-D CUDA tensor of the compute dtype")
+    _require(dy.shape[1] == qw.rows and dy.stride(1) == 1,
+             "dy must have the weight's number of rows, contiguous along them")
     M = dy.shape[0]
     ld = dy.stride(0) if M > 1 else max(qw.rows, dy.stride(0))
     if out is None:
@@ -337,8 +353,10 @@ class Int8Weight:
 
 def int8_quantize_weight(w: torch.Tensor, stream=None) -> Int8Weight:
     """Vector-wise int8 quantization of an fp16 / bf16 weight [rows, cols]."""
-    assert w.is_cuda and w.dim() == 2 and w.is_contiguous()
-    in_dt = {torch.float16: IN_F16, torch.bfloat16: IN_BF16}[w.dtype]
+    _require(w.is_cuda and w.dim() == 2 and w.is_contiguous(),
+             "w must be a contiguous 2-D CUDA tensor")
+    _require(w.dtype in (torch.float16, torch.bfloat16), "w must be fp16 or bf16")
+    in_dt = _IN_DTYPES[w.dtype]
     rows, cols = w.shape
     wq = Int8Weight(torch.empty(rows, cols, dtype=torch.int8, device=w.device),
                     torch.empty(rows, dtype=torch.float32, device=w.device), rows, cols)
@@ -376,8 +394,9 @@ def int8_matmul(wq: Int8Weight, x: torch.Tensor, threshold: float = INT8_DEFAULT
                 stream=None) -> torch.Tensor:
     """LLM.int8() decomposition matmul: y [M, rows] = x [M, cols] (fp16)
     against the int8 weight, outlier columns (|x| > threshold) in fp16."""
-    assert x.is_cuda and x.dtype == torch.float16 and x.is_contiguous()
-    assert x.shape[-1] == wq.cols
+    _require(x.is_cuda and x.dtype == torch.float16 and x.is_contiguous() and x.dim() == 2,
+             "x must be a contiguous 2-D fp16 CUDA tensor")
+    _require(x.shape[-1] == wq.cols, "x must have the weight's number of columns")
     M = x.shape[0]
     if workspace is None:
         workspace = int8_workspace(M, wq.cols, x.device)

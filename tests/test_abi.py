@@ -7,6 +7,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import dequant_matmul_quantize_b300 as nq
 from oracle import nf4_oracle as o
@@ -183,3 +184,20 @@ def test_argument_checks_launch_nothing(L):
 
 def test_workspace_size(L):
     assert L.nf4q_double_quant_workspace_bytes(1 << 20) >= 64
+
+
+def test_binding_rejects_bad_tensors_before_any_call():
+    """Host tensors, wrong dtypes and shapes raise ValueError in the binding
+    (no GPU needed: nothing reaches the library)."""
+    qw = nq.QuantizedWeight(*(torch.empty(0) for _ in range(5)), 4, 64, "nf4", True)
+    with pytest.raises(ValueError):
+        nq.quantize_into(qw, torch.zeros(4, 64))                     # not on a GPU
+    with pytest.raises(ValueError):
+        nq.gemv(qw, torch.zeros(1, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        nq.matmul_dx(qw, torch.zeros(3, 4, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        nq.int8_quantize_weight(torch.zeros(4, 64, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        nq.int8_matmul(nq.Int8Weight(torch.empty(0), torch.empty(0), 4, 64),
+                       torch.zeros(1, 64, dtype=torch.float16))
