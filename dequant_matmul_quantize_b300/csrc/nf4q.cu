@@ -87,17 +87,18 @@ nf4q_status check_scales(const nf4q_weight* wq) {
   return NF4Q_OK;
 }
 
-// The GEMV instantiations: code (NF4, FP4) x (NT, R) in {(1, 1), (2, 2)} x
-// compute dtype (bf16, fp16).
+// The GEMV instantiations: code (NF4, FP4) x (NT, R) in {(1, 1), (1, 2),
+// (2, 2)} x compute dtype (bf16, fp16).
 using GemvKernelFn = void (*)(CUtensorMap, ScaleView, const uint16_t*, uint16_t*, int, int, int,
                               int, int, CodeValues);
-template <int DT>
-GemvKernelFn gemv_kernel_dt(int code, int NT) {
-  if (code == 0) return NT == 1 ? gemv_mma_kernel<0, 1, 1, DT> : gemv_mma_kernel<0, 2, 2, DT>;
-  return NT == 1 ? gemv_mma_kernel<1, 1, 1, DT> : gemv_mma_kernel<1, 2, 2, DT>;
+template <int CODE, int DT>
+GemvKernelFn gemv_kernel_cd(int NT, int R) {
+  if (NT == 2) return gemv_mma_kernel<CODE, 2, 2, DT>;
+  return R == 2 ? gemv_mma_kernel<CODE, 1, 2, DT> : gemv_mma_kernel<CODE, 1, 1, DT>;
 }
-GemvKernelFn gemv_kernel(int code, int NT, int dt) {
-  return dt == 0 ? gemv_kernel_dt<0>(code, NT) : gemv_kernel_dt<1>(code, NT);
+GemvKernelFn gemv_kernel(int code, int NT, int R, int dt) {
+  if (dt == 0) return code == 0 ? gemv_kernel_cd<0, 0>(NT, R) : gemv_kernel_cd<1, 0>(NT, R);
+  return code == 0 ? gemv_kernel_cd<0, 1>(NT, R) : gemv_kernel_cd<1, 1>(NT, R);
 }
 
 // Opt the GEMV kernels in to their largest dynamic shared memory (once per
@@ -118,10 +119,11 @@ nf4q_status gemv_attr_ready() {
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return NF4Q_OK;
   const int bytes = static_cast<int>(gemv_smem_bytes(2, 2, kGemvMaxStages, kGemvMaxSplit));
+  const int shapes[3][2] = {{1, 1}, {1, 2}, {2, 2}};  // (NT, R)
   for (int code = 0; code < 2; ++code)
-    for (int nt = 1; nt <= 2; ++nt)
+    for (const auto& sh : shapes)
       for (int dt = 0; dt < 2; ++dt)
-        if ((st = cuda_check(cudaFuncSetAttribute(gemv_kernel(code, nt, dt),
+        if ((st = cuda_check(cudaFuncSetAttribute(gemv_kernel(code, sh[0], sh[1], dt),
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   bytes),
                              "cudaFuncSetAttribute (GEMV)")) != NF4Q_OK)
@@ -478,9 +480,10 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   if (wq->rows > (1ll << 30) || wq->cols > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
   const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
   if ((st = gemv_attr_ready()) != NF4Q_OK) return st;
-  // M <= 8: one 8-column MMA tile and 16 rows per CTA; M > 8: two column
-  // tiles and 32 rows, so each x fragment serves twice as many weights.
-  const int NT = M > 8 ? 2 : 1, R = NT;
+  // M <= 4: one 8-column MMA tile and 16 rows per CTA; M = 5..8: 32 rows,
+  // so each x fragment (by then up to eight distinct rows of x) serves twice
+  // as many weights; M > 8: two column tiles and 32 rows.
+  const int NT = M > 8 ? 2 : 1, R = M > 4 ? 2 : 1;
   const int code = wq->code == NF4Q_CODE_NF4 ? 0 : 1;
   const int64_t tiles = (N + kGemvRows * R - 1) / (kGemvRows * R);
   const int nseg = (K + kGemvSeg - 1) / kGemvSeg;
@@ -521,7 +524,7 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   uint16_t* yp = static_cast<uint16_t*>(y);
   const ScaleView sv = scale_view(wq);
   const CodeValues C = code_values(wq->code);
-  return launch("gemv_mma_kernel", gemv_kernel(code, NT, wq->compute_dtype),
+  return launch("gemv_mma_kernel", gemv_kernel(code, NT, R, wq->compute_dtype),
                 dim3(static_cast<unsigned>(tiles * split)), dim3(kGemvWarps * 32), smem, s, attr,
                 split > 1 ? 1u : 0u, tw, sv, xp, yp, N, K, static_cast<int>(M), per, stages, C);
 }

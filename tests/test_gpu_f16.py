@@ -74,7 +74,7 @@ def test_f16_dequantize_overflows_to_infinity():
 
 
 @pytest.mark.parametrize("code", ["nf4", "fp4"])
-@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("M", [1, 5, 8, 16])
 def test_f16_gemv(code, M):
     w = synth.normal_weight(200, 1536, 0.02, seed=M + 40, outlier_frac=1e-3)
     qw, w_hat = _f16_check(w, code, True, "gemv")

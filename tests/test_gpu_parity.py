@@ -223,7 +223,7 @@ def test_dequantize_unaligned_fp32_scales(shape):
 
 
 # ---------------------------------------------------------------- GEMV
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 12, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8, 12, 16])
 @pytest.mark.parametrize("shape", [(37, 320), (256, 1024), (129, 4160)])
 def test_gemv_small(M, shape):
     w = synth.normal_weight(*shape, 0.02, seed=M * 7 + shape[0], outlier_frac=1e-3)
@@ -246,10 +246,11 @@ def test_gemv_one_hot_column_is_exact():
         assert np.array_equal(bf16_bits(y)[0], w_hat[:, k])
 
 
-def test_gemv_fp4():
+@pytest.mark.parametrize("M", [4, 7])
+def test_gemv_fp4(M):
     w = synth.normal_weight(96, 768, 0.015, seed=21)
     qw, w_hat = _full_check(w, "fp4", True, "fp4 gemv")
-    x = synth.activations(4, 768, seed=22)
+    x = synth.activations(M, 768, seed=22)
     check_matmul(bf16_bits(nq.gemv(qw, x.cuda())), bf16_bits(x), w_hat, "fp4 gemv")
 
 
