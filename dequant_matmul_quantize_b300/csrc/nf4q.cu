@@ -482,9 +482,15 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   if ((st = gemv_attr_ready()) != NF4Q_OK) return st;
   // M <= 4: one 8-column MMA tile and 16 rows per CTA; M = 5..8: 32 rows,
   // so each x fragment (by then up to eight distinct rows of x) serves twice
-  // as many weights; M > 8: two column tiles and 32 rows.
-  const int NT = M > 8 ? 2 : 1, R = M > 4 ? 2 : 1;
+  // as many weights; M > 8: two column tiles and 32 rows.  FP4, whose lookup
+  // is cheaper, takes 32 rows from M = 2 when those tiles alone give every SM
+  // its four CTAs (measured on 28672 x 8192: 69.1 -> 57.2 us at M = 4); with
+  // fewer rows the K split it would need costs more than it saves.
   const int code = wq->code == NF4Q_CODE_NF4 ? 0 : 1;
+  const bool fp4_wide = code == 1 && M > 1 &&
+                        (N + 2 * kGemvRows - 1) / (2 * kGemvRows) >=
+                            static_cast<int64_t>(kGemvMinCtasPerSm) * sm_count();
+  const int NT = M > 8 ? 2 : 1, R = M > 4 || fp4_wide ? 2 : 1;
   const int64_t tiles = (N + kGemvRows * R - 1) / (kGemvRows * R);
   const int nseg = (K + kGemvSeg - 1) / kGemvSeg;
   const int nchunks = (nseg + kGemvWarps - 1) / kGemvWarps;

@@ -254,6 +254,16 @@ def test_gemv_fp4(M):
     check_matmul(bf16_bits(nq.gemv(qw, x.cuda())), bf16_bits(x), w_hat, "fp4 gemv")
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_gemv_fp4_many_rows(M):
+    """FP4 with enough rows (19001 > 148 SMs x 4 CTAs x 32 rows) that M = 2..4
+    runs on 32-row CTAs: every output against the oracle, ragged last tile."""
+    w = synth.normal_weight(19001, 192, 0.015, seed=23)
+    qw, w_hat = _full_check(w, "fp4", True, "fp4 many rows")
+    x = synth.activations(M, 192, seed=24 + M)
+    check_matmul(bf16_bits(nq.gemv(qw, x.cuda())), bf16_bits(x), w_hat, f"fp4 19001 M={M}")
+
+
 # ---------------------------------------------------------------- full sizes
 def _sampled_full_size(w_gpu: torch.Tensor, code: str, xs, n_rows=48, seed=0):
     """Full-size weight: the whole scale state is compared exactly (the
