@@ -101,8 +101,6 @@ GemvKernelFn gemv_kernel(int code, int NT, int R, int dt) {
   return code == 0 ? gemv_kernel_cd<0, 1>(NT, R) : gemv_kernel_cd<1, 1>(NT, R);
 }
 
-// Opt the GEMV kernels in to their largest dynamic shared memory (once per
-// device).
 // The current device (0 .. kMaxDevices-1) or an error status.
 nf4q_status current_device(int* dev) {
   nf4q_status st = cuda_check(cudaGetDevice(dev), "cudaGetDevice");
@@ -110,6 +108,8 @@ nf4q_status current_device(int* dev) {
   return st;
 }
 
+// Opt the GEMV kernels in to their largest dynamic shared memory (once per
+// device).
 nf4q_status gemv_attr_ready() {
   static bool done[kMaxDevices] = {false};
   static std::mutex mu;
@@ -269,6 +269,7 @@ nf4q_status nf4q_sizes(int64_t rows, int64_t cols, int32_t blocksize,
   if (rows < 0 || cols < 0 || blocksize != kBlock || dq_blocksize != kDqBlock ||
       cols % kBlock != 0)
     return NF4Q_ERR_INVALID_ARG;
+  if (cols > 0 && rows > INT64_MAX / cols) return NF4Q_ERR_UNSUPPORTED;  // rows*cols overflows
   const int64_t n = rows * cols;
   const int64_t nb = n / kBlock;
   if (packed_bytes) *packed_bytes = static_cast<size_t>(n / 2);
@@ -299,7 +300,6 @@ nf4q_status nf4q_thresholds(int32_t code, float* out, int32_t* count) {
 
 namespace nf4q {
 namespace {
-// Both passes of the double quantization, on a cleared workspace record.
 // Quantize launch after the argument checks common to both entry points
 // (n > 0).  ws != nullptr: fused first double-quant pass into ws (cleared
 // here) and wq->offset.
@@ -351,6 +351,7 @@ nf4q_status dq_quant_launch(const nf4q_weight* wq, int64_t nb, cudaStream_t s,
                 wq->absmax_q, wq->scale2);
 }
 
+// Both passes of the double quantization, on a cleared workspace record.
 nf4q_status dq_launch(const nf4q_weight* wq, int64_t nb, void* ws, cudaStream_t s) {
   nf4q_status st = cuda_check(cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s),
                               "cudaMemsetAsync (double-quant workspace)");

@@ -119,7 +119,10 @@ const char* nf4q_status_string(nf4q_status s);
 int32_t nf4q_last_cuda_error(char* buf, int32_t buf_bytes);
 
 /* HOST ONLY.  Buffer sizes of a [rows x cols] weight: packed bytes, number of
- * 64-blocks n_b and of 256-blocks n_d.  Any output pointer may be NULL. */
+ * 64-blocks n_b and of 256-blocks n_d.  Any output pointer may be NULL.
+ * NF4Q_ERR_INVALID_ARG for negative sizes, cols not a multiple of 64 or other
+ * block sizes; NF4Q_ERR_UNSUPPORTED when rows*cols does not fit in int64_t
+ * (nothing is written then). */
 nf4q_status nf4q_sizes(int64_t rows, int64_t cols, int32_t blocksize,
                        int32_t dq_blocksize, size_t* packed_bytes,
                        int64_t* n_b, int64_t* n_d);

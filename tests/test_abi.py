@@ -127,6 +127,11 @@ def test_sizes(L):
     assert nq.sizes(0, 64) == (0, 0, 0)
     with pytest.raises(nq.Nf4qError):
         nq.sizes(4, 100)                           # cols % 64 != 0
+    big = (2 ** 63 - 1) // 64                      # rows * 64 still fits in int64
+    assert nq.sizes(big, 64) == (big * 32, big, (big + 255) // 256)
+    for rows, cols in ((big + 1, 64), (2 ** 40, 2 ** 40), (2 ** 62, 2 ** 6 * 3)):
+        with pytest.raises(nq.Nf4qError, match="UNSUPPORTED"):
+            nq.sizes(rows, cols)                   # rows * cols overflows int64
 
 
 def test_code_values_match_oracle_bit_exact(L):
