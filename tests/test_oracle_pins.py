@@ -383,6 +383,24 @@ def test_all_zero_block():
     assert np.all(o.unpack_nibbles(packed)[:64] == 0)
 
 
+def test_normalize_is_the_correctly_rounded_quotient():
+    """wn = fp32(w / absmax) with IEEE division: the float32 nearest to the
+    exact rational quotient, checked with Fraction arithmetic on values where
+    multiplying by a rounded reciprocal gives a different float32."""
+    g = np.random.default_rng(77)
+    a = np.abs(g.standard_normal(400)).astype(np.float32) * np.float32(0.03) + np.float32(1e-4)
+    w = (g.uniform(-1, 1, (400, 64)) * a[:, None]).astype(np.float32)
+    wn = o.normalize(w.reshape(-1), a).reshape(400, 64)
+    recip_differs = 0
+    for i in range(400):
+        r = np.float32(1) / a[i]
+        for j in range(0, 64, 4):
+            want = _exact_f32_round(Fraction(float(w[i, j])) / Fraction(float(a[i])))
+            assert wn[i, j] == want, (i, j, w[i, j], a[i], wn[i, j], want)
+            recip_differs += int(np.float32(w[i, j] * r) != want)
+    assert recip_differs > 50     # the check can tell the two apart
+
+
 # ------------------------------------------------------------ double quant
 def test_double_quant_worked_example():
     a = np.array([0.5, 1.5], np.float32)
@@ -395,6 +413,20 @@ def test_double_quant_worked_example():
     assert off == np.float32(0.25) and np.all(s2 == 0) and np.all(q == 0)
     s = o.block_scales(q, s2, off)
     assert np.all(s == np.float32(0.25))
+
+
+def test_double_quant_rounds_exact_halves_to_even():
+    """Worked example with exact .5 quotients: absmax = 1 + c with c in
+    {+-127, +-2.5, +-3.5, +-0.5, +-1.5}/128 has the exact mean 1, so
+    c = fp32(absmax - 1) exactly, scale2 = (127/128)/127 = 1/128 exactly and
+    c / scale2 lands on the halves; ties to even give 2, 4, 0, 2 (rounding
+    half away from zero would give 3, 4, 1, 2)."""
+    c = np.array([127, -127, 2.5, -2.5, 3.5, -3.5, 0.5, -0.5, 1.5, -1.5]) / 128
+    a = (1.0 + c).astype(np.float32)
+    assert np.array_equal(a.astype(np.float64) - 1.0, c)      # exact inputs
+    q, s2, off = o.double_quant(a)
+    assert off == np.float32(1.0) and s2[0] == np.float32(2.0 ** -7)
+    assert q.tolist() == [127, -127, 2, -2, 4, -4, 0, 0, 2, -2]
 
 
 def test_double_quant_invariants():
@@ -423,6 +455,32 @@ def test_dequant_closed_form_unit_scale():
         w = o.dequantize(packed, np.ones(1, np.float32), code)
         want = torch.from_numpy(o.code_table(code)[idx]).to(torch.bfloat16)
         assert np.array_equal(w, want.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_dequant_single_rounding_with_scales():
+    """w_hat = bf16(fp32(code * s)): the exact product rounded once to
+    float32 (Fraction arithmetic), then to bf16 by torch's cast.  The scales
+    cover many magnitudes; rounding the code to bf16 before the product (a
+    double rounding) gives other bits on a good share of them."""
+    g = np.random.default_rng(91)
+    s = (np.abs(g.standard_normal(300)) * 10.0 ** g.integers(-6, 3, 300)).astype(np.float32)
+    idx = np.tile(np.arange(16, dtype=np.uint8), 4 * 300)
+    packed = o.pack_nibbles(idx)
+    for code in (o.CODE_NF4, o.CODE_FP4):
+        t = o.code_table(code)
+        got = o.dequantize(packed, s, code).reshape(300, 64)
+        f32 = np.empty((300, 16), np.float32)
+        for b in range(300):
+            for j in range(16):
+                v = _exact_f32_round(Fraction(float(t[j])) * Fraction(float(s[b])))
+                f32[b, j] = np.copysign(v, t[j])    # FP4 code 8 is -0: -0 * s = -0
+        want = torch.from_numpy(f32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got[:, :16], want)
+        if code == o.CODE_NF4:
+            tb = torch.from_numpy(t).to(torch.bfloat16).float().numpy()
+            dbl = torch.from_numpy((tb[None, :] * s[:, None]).astype(np.float32)).to(
+                torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert np.sum(dbl != want) > 100
 
 
 def test_roundtrip_error_bound():
@@ -574,4 +632,23 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         dtype=np.float16).view(np.uint16))
     with pytest.raises(AssertionError):
         test_f16_rounding_matches_brute_force_grid()
+    monkeypatch.undo()
+    # (7) division replaced by a multiply with the rounded reciprocal
+    monkeypatch.setattr(o, "normalize", lambda w, a, blocksize=o.BLOCKSIZE: (
+        np.asarray(w, np.float32).reshape(-1, blocksize)
+        * (np.float32(1) / np.asarray(a, np.float32).reshape(-1, 1))).astype(np.float32).reshape(-1))
+    with pytest.raises(AssertionError):
+        test_normalize_is_the_correctly_rounded_quotient()
+    monkeypatch.undo()
+    # (8) int8 scale codes rounded half away from zero instead of to even
+    monkeypatch.setattr(o.np, "rint", lambda v: np.trunc(v + np.copysign(0.5, v)))
+    with pytest.raises(AssertionError):
+        test_double_quant_rounds_exact_halves_to_even()
+    monkeypatch.undo()
+    # (9) the code value rounded to bf16 before the scale (double rounding)
+    orig_table = o.code_table
+    monkeypatch.setattr(o, "code_table", lambda code: torch.from_numpy(orig_table(code)).to(
+        torch.bfloat16).float().numpy())
+    with pytest.raises(AssertionError):
+        test_dequant_single_rounding_with_scales()
     monkeypatch.undo()
