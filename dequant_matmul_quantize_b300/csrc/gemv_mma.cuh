@@ -159,6 +159,10 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
     fence_proxy_async_smem();
   }
   __syncthreads();
+  // Cluster K split: every CTA of the cluster must be known to run before
+  // another writes into its shared memory.  Arrive now, wait just before
+  // the first remote store (after the main loop), so the wait costs nothing.
+  if (nrank > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   if (threadIdx.x == 0)
     for (int i = 0; i < min(stages, nmine); ++i) issue(i, i);
 
@@ -303,6 +307,7 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
     const int col = 8 * nt + 2 * (ln & 3) + (i & 1);
     if (row < N && col < M) y[static_cast<int64_t>(col) * N + row] = round_to_dt<DT>(v);
   };
+  if (nrank > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   for (int item = threadIdx.x; item < kItems; item += kGemvWarps * 32) {
     float v = 0.f;
 #pragma unroll

@@ -67,6 +67,39 @@ inline nf4q_status ensure_context() {
   return cuda_check(cudaSetDevice(dev), "cudaSetDevice (bind the primary context)");
 }
 
+// Unique id of the calling thread's current context (cuCtxGetId: unique over
+// the process lifetime, unlike the CUcontext handle, whose value may be
+// reused after a context is destroyed).  *id = 0 when no context is current.
+inline nf4q_status current_context_id(unsigned long long* id) {
+  using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+  using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static const CtxGetCurrentFn get_current = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return static_cast<CtxGetCurrentFn>(nullptr);
+  }();
+  static const CtxGetIdFn get_id = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetIdFn>(p);
+    return static_cast<CtxGetIdFn>(nullptr);
+  }();
+  if (!get_current || !get_id) return cuda_fail("cuCtxGetCurrent/cuCtxGetId: driver entry point not found");
+  CUcontext ctx = nullptr;
+  nf4q_status st = cu_check(get_current(&ctx), "cuCtxGetCurrent");
+  if (st != NF4Q_OK) return st;
+  *id = 0;
+  if (!ctx) return NF4Q_OK;
+  return cu_check(get_id(ctx, id), "cuCtxGetId");
+}
+
 // One launch of `kernel` on `stream`; `attrs` (may be null) are passed on as
 // cudaLaunchKernelEx launch attributes.
 template <typename... KArgs, typename... Args>

@@ -600,17 +600,26 @@ static __device__ __align__(256) unsigned char g_dq_noalloc_scratch[256];
 static_assert(sizeof(DqWorkspace) <= 256, "double-quant record must fit the static scratch");
 
 namespace {
+// The scratch's device address in the current context, looked up with
+// cudaGetSymbolAddress the first time a device is used and again whenever the
+// current context is not the one the cached address belongs to (a device
+// reset, or another context made current on the device).
 void* noalloc_scratch(nf4q_status* st) {
   static void* addr[kMaxDevices] = {nullptr};
+  static unsigned long long ctx_of[kMaxDevices] = {0};
   static std::mutex mu;
   int dev = 0;
   if ((*st = current_device(&dev)) != NF4Q_OK) return nullptr;
+  if ((*st = ensure_context()) != NF4Q_OK) return nullptr;
+  unsigned long long ctx = 0;
+  if ((*st = current_context_id(&ctx)) != NF4Q_OK) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx_of[dev] != ctx) {
     void* p = nullptr;
     *st = cuda_check(cudaGetSymbolAddress(&p, g_dq_noalloc_scratch), "cudaGetSymbolAddress");
     if (*st != NF4Q_OK) return nullptr;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *st = NF4Q_OK;
   return addr[dev];
@@ -623,8 +632,6 @@ nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream) {
   const int64_t nb = wq->rows * wq->cols / kBlock;
   if (!wq->absmax_q || !wq->scale2 || !wq->offset) return NF4Q_ERR_INVALID_ARG;
   if (!aligned4(wq->offset) || !aligned4(wq->scale2)) return NF4Q_ERR_ALIGNMENT;
-  if (nf4q_double_quant_workspace_bytes(nb) > sizeof(g_dq_noalloc_scratch))
-    return NF4Q_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (nb == 0) {
     return cuda_check(cudaMemsetAsync(wq->offset, 0, sizeof(float), s),
@@ -642,7 +649,8 @@ nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream) {
 namespace {
 nf4q_status check_int8_weight(const nf4q_int8_weight* wq) {
   if (!wq || wq->rows < 0 || wq->cols < 0 || wq->cols % 16 != 0) return NF4Q_ERR_INVALID_ARG;
-  if (wq->rows > 0x7FFFFFFF || wq->cols > 0x7FFFFFFF) return NF4Q_ERR_UNSUPPORTED;
+  // the kernels step int column indices by up to a few thousand past cols
+  if (wq->rows > 0x7FFFFFFF || wq->cols > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
   return NF4Q_OK;
 }
 }  // namespace

@@ -243,11 +243,14 @@ nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear);
  *   on every GPU the library is loaded on until the process exits.  The call
  *   allocates nothing and calls no allocating routine.
  *   Limit: the scratch holds one double-quant record, which serves any tensor
- *   the library accepts (n_b = rows*cols/64 up to 2^31 - 1); a tensor whose
- *   workspace would not fit is refused with NF4Q_ERR_UNSUPPORTED.
+ *   the library accepts; the only size limit is the library-wide one of every
+ *   double-quant call, n_b = rows*cols/64 <= 2^31 - 1 (NF4Q_ERR_UNSUPPORTED
+ *   beyond it).
  *   Set-up: the first call on each device looks up the scratch's device
- *   address (cudaGetSymbolAddress) with that device current; make that first
- *   call before any stream capture.
+ *   address (cudaGetSymbolAddress) with that device current, and caches it
+ *   with the id of the current context; a call in another context (after a
+ *   cudaDeviceReset, for example) looks it up again.  Make the first call in
+ *   a context before any stream capture.
  *   Sharing: every call on a device uses the same scratch; the call clears it
  *   (cudaMemsetAsync on `stream`) before use.  Calls whose work overlaps on
  *   the GPU (other streams, other threads) race on it and must be serialized
@@ -278,7 +281,8 @@ typedef struct {
 #define NF4Q_INT8_DEFAULT_THRESHOLD 6.0f
 
 /* Quantize W (device, fp16 or bf16 per `in_dtype`, row-major, 16-byte
- * aligned) into wq->q / wq->scale.  One CTA per row. */
+ * aligned) into wq->q / wq->scale.  One CTA per row.  Every int8 call
+ * refuses cols > 2^30 and rows > 2^31 - 1 with NF4Q_ERR_UNSUPPORTED. */
 nf4q_status nf4q_int8_quantize_weight(const void* w, int32_t in_dtype,
                                       const nf4q_int8_weight* wq, void* stream);
 

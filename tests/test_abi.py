@@ -118,6 +118,11 @@ def test_int8_workspace_layout_and_checks(L):
     assert L.nf4q_int8_matmul(ctypes.byref(w), None, -1, 6.0, None, None, 0, None) == 1
     assert L.nf4q_int8_matmul(ctypes.byref(w), None, 2, 6.0, None, None, 0, None) == 1
     assert L.nf4q_int8_matmul(None, None, 2, 6.0, None, None, 0, None) == 1
+    # cols beyond 2^30 would overflow the kernels' int column counters
+    w = nq.NF4QInt8Weight(0x1000, 0x2000, 8, (1 << 30) + 16)
+    assert L.nf4q_int8_quantize_weight(0x3000, nq.IN_F16, ctypes.byref(w), None) == 3
+    assert L.nf4q_int8_matmul(ctypes.byref(w), 0x3000, 1, 6.0, 0x4000, 0x5000, 1 << 40,
+                              None) == 3
 
 
 def test_sizes(L):
