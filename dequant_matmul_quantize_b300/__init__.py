@@ -114,6 +114,7 @@ def lib() -> ctypes.CDLL:
         "nf4q_quantize_dq": (i32, [vp, i32, W, vp, sz, vp]),
         "nf4q_dequantize": (i32, [W, vp, vp]),
         "nf4q_gemv": (i32, [W, vp, i32, vp, vp]),
+        "nf4q_gemv_exact": (i32, [W, vp, i32, vp, vp]),
         "nf4q_gemm": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul_dx": (i32, [W, vp, i64, i64, vp, vp]),
@@ -297,8 +298,15 @@ def _mm(name: str, qw: QuantizedWeight, x: torch.Tensor, out, stream):
 
 
 def gemv(qw, x, out=None, stream=None):
-    """y = x . w_hat^T for 1 <= M <= 16 (decode)."""
+    """y = x . w_hat^T for 1 <= M <= 16 (decode); for M <= 8 the block scale
+    is folded after an fp16 contraction with the code values (see nf4q.h)."""
     return _mm("nf4q_gemv", qw, x, out, stream)
+
+
+def gemv_exact(qw, x, out=None, stream=None):
+    """y = x . w_hat^T for 1 <= M <= 16 with w_hat rebuilt bit for bit inside
+    the contraction."""
+    return _mm("nf4q_gemv_exact", qw, x, out, stream)
 
 
 def gemm(qw, x, out=None, stream=None):

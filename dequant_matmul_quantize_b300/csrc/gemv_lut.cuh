@@ -1,0 +1,553 @@
+// nf4_gemv for decode shapes, block-scale folded ("bitsandbytes tutorial",
+// sec. 3.4: 4-bit storage, 16-bit compute; sec. 七 myth 5: decode is bound by
+// moving the packed weights):
+//
+//   y[m, n] = sum_b  s_{n,b} * sum_{k in b} x[m, k] * c[code(n, k)]
+//
+// with c the 16 code values and s_{n,b} the scale of 64-block b of row n.
+// The inner sum runs on the tensor cores (mma.sync m16n8k16, fp16 operands,
+// fp32 accumulate) with the code VALUES as the A operand - the same table
+// for every block - and the block scale is applied to each block's fp32
+// partial sum afterwards.  So the per-weight work is only a table lookup,
+// with no per-block table to build:
+//
+//   * A byte of packed codes holds two neighbouring weights; the lookup
+//     takes the whole byte: a 256-entry table in shared memory gives the
+//     fp16x2 pair (c[hi nibble], c[lo nibble]), which is exactly one
+//     A-fragment register.  The table is replicated 32 times so that lane l
+//     always reads bank l (no conflicts whatever the codes); entry v of
+//     replica l sits at 0x10000 + 256 v + 4 l, so a single byte permute
+//     (PRMT) forms the address from the packed word and a per-lane constant.
+//   * x becomes fp16: for a bf16 compute dtype each row m of x is scaled by
+//     a power of two 2^-F_m (F_m from the row's largest |x|) so that every
+//     value keeps its 8 significant bits; the factor 2^F_m is folded back
+//     together with the block scale.
+//
+// What this computes differs from the dequantize-then-multiply reference
+// only by rounding: the reference multiplies x by w_hat = bf16(c * s), this
+// kernel by c * s with c rounded to fp16 (relative error below 3.3e-4 for
+// the NF4 and FP4 values, 2^-11 at most for any value).  Per term the
+// difference is at most 2^-8 + 2^-11 of |x * w_hat| for bf16 and 2^-10 for
+// fp16; it has the sign of the rounding of each w_hat and so averages out
+// over a dot product.  (The bit-faithful variant, which rebuilds w_hat exactly inside
+// the contraction, is gemv_mma.cuh.)
+//
+// Work split.  One CTA per SM (the table takes 64 KB), 16 warps, each with
+// its own three-stage TMA ring of 16-row x 256-column boxes of packed codes
+// (2 KB, 128-byte swizzle).  A warp owns one 16-row tile at a time and one
+// of P parts of the K range; the P warps of a tile add their partial sums
+// in a fixed order in shared memory, so y is deterministic.  Tiles go to the
+// CTAs round robin.
+#pragma once
+
+#include "common.cuh"
+#include "tma.cuh"
+
+namespace nf4q {
+
+constexpr int kLutWarps = 16;
+constexpr int kLutThreads = kLutWarps * 32;
+constexpr int kLutStages = 3;                 // per warp
+constexpr uint32_t kLutBoxBytes = 16 * 128;   // 16 rows x 256 packed columns
+constexpr uint32_t kLutTable = 0x10000;       // shared address of the table
+constexpr uint32_t kLutRing = 0x20000;        // shared address of the rings
+constexpr uint32_t kLutSmemTop = kLutRing + kLutWarps * kLutStages * kLutBoxBytes;  // 0x38000
+constexpr uint32_t kLutMaxBase = 0x1000;      // dynamic shared memory must start below
+// Shared memory below the table available to x: [kLutMaxBase, kLutTable).
+constexpr uint32_t kLutXBytes = kLutTable - kLutMaxBase;
+constexpr int kLutMaxM = 8;
+
+// The unused upper half of each 256-byte table row is a 128-byte "piece";
+// pieces hold the control data.
+__device__ __forceinline__ uint32_t lut_piece(int p) { return kLutTable + 256u * p + 128u; }
+constexpr int kLutPieceBars = 0;    // 16 warps x 32 B (3 stages x 8 B)  (4 pieces)
+constexpr int kLutPieceScale = 4;   // per warp 2 x 256 B          (64 pieces)
+constexpr int kLutPieceRed = 68;    // per warp 2 x 512 B          (128 pieces)
+constexpr int kLutPieceMisc = 196;  // F factors, reduction scratch (8 pieces)
+
+// fp16 bits of the 16 code values, built on the host.
+struct __align__(16) HalfCodes {
+  uint16_t h[16];
+};
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128_lut(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts64(uint32_t addr, float a, float b) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t prmt_lut(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Bounded wait for a stage, letting the warp sleep inside try_wait (a
+// suspend-time hint of 20 us) instead of spinning on issue slots that the
+// other warps of the SM need; gives up after the usual time limit.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_sleep(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(&g_device_error, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+// d = A (16x16) . B (16x8) + 0, fp16 operands, fp32 accumulate (first MMA of
+// a block) and d += A . B (the others).
+__device__ __forceinline__ void mma_f16_first(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+      "{%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ void mma_f16_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+      "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Shared-memory layout of staged x (fp16): row m, 64-block j is a 128-byte
+// piece at xbase + (m * kbx + j) * 128; element i of the block sits at byte
+// (2 i + 16 m) mod 128, so that the eight rows a quarter-warp reads fall on
+// distinct banks.
+__device__ __forceinline__ uint32_t lut_x_addr(uint32_t xbase, int kbx, int m, int j, int byte) {
+  return xbase + static_cast<uint32_t>((m * kbx + j) * 128) +
+         static_cast<uint32_t>((byte + 16 * m) & 127);
+}
+
+// Launch: grid <= SM count, 512 threads, 0x38000 bytes of dynamic shared
+// memory (minus nothing: the layout uses absolute shared addresses and
+// checks that the dynamic area starts below kLutMaxBase).  P = parts of K
+// (1, 2, 4, 8 or 16), kbx = 64-blocks of staged x per row (a multiple of 4,
+// >= K/64).  Requires M <= 8 and M * kbx * 128 <= kLutXBytes.
+template <int DT, bool DQ>
+__global__ void __launch_bounds__(kLutThreads, 1)
+gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
+                const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int N, int K, int M,
+                int P, int kbx, const __grid_constant__ HalfCodes hc) {
+  extern __shared__ __align__(1024) uint8_t lsm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t base = smem_u32(lsm);
+  if (base > kLutMaxBase) {  // never expected; the layout would not fit
+    if (threadIdx.x == 0) atomicOr(&g_device_error, 2u);
+    return;
+  }
+  const uint32_t xbase = kLutMaxBase;
+  const int KB = K / kBlock;
+  const int nbox = (KB + 3) / 4;
+  const int SL = kLutWarps / P;
+  const int slot = warp / P, part = warp % P;
+  const int pb0 = part * nbox / P, pb1 = (part + 1) * nbox / P;
+  const int nmy = pb1 - pb0;
+  const int T = (N + 15) / 16;
+  const int tile_stride = static_cast<int>(gridDim.x) * SL;
+  const int tile0 = static_cast<int>(blockIdx.x) * SL + slot;
+  const int nunits = (tile0 < T && nmy > 0) ? (T - tile0 + tile_stride - 1) / tile_stride : 0;
+  const int total = nunits * nmy;
+
+  const uint32_t barw = lut_piece(kLutPieceBars + warp / 4) + 32u * (warp % 4);
+  auto bar_of = [&](int st) { return barw + 8u * st; };
+  const uint32_t ring = kLutRing + static_cast<uint32_t>(warp * kLutStages) * kLutBoxBytes;
+
+  // box q of this warp's stream: (tile, box index along K)
+  auto box_coords = [&](int q, int& tile, int& bb) {
+    const int u = q / nmy;
+    tile = tile0 + u * tile_stride;
+    bb = pb0 + (q - u * nmy);
+  };
+  auto issue_at = [&](int tile, int bb, int st) {
+    const uint32_t bar = bar_of(st);
+    mbar_arrive_expect_tx(bar, kLutBoxBytes);
+    tma_load_2d(ring + st * kLutBoxBytes, &tmap_w, bb * 128, tile * 16, bar);
+  };
+  auto issue = [&](int q) {
+    int tile, bb;
+    box_coords(q, tile, bb);
+    issue_at(tile, bb, q % kLutStages);
+  };
+
+  // 1. barriers, first loads
+  if (lane == 0) {
+    for (int st = 0; st < kLutStages; ++st) mbar_init(bar_of(st), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+    for (int q = 0; q < min(kLutStages, total); ++q) issue(q);
+  }
+
+  // 2. the byte-pair table: thread i writes entry i/2, replicas 16*(i&1) .. +15
+  {
+    const int e = threadIdx.x >> 1;
+    const uint32_t v = static_cast<uint32_t>(hc.h[e >> 4]) |
+                       (static_cast<uint32_t>(hc.h[e & 15]) << 16);
+    const uint4 vv = make_uint4(v, v, v, v);
+    const uint32_t a = kLutTable + 256u * e + 64u * (threadIdx.x & 1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sts128(a + 16 * k, vv);
+  }
+
+  // 3. x -> fp16 with a power-of-two scale per row (bf16), staged
+  const uint32_t misc = lut_piece(kLutPieceMisc);  // F of each row of x
+  // per-warp maxima [16 warps][8 rows] (4 pieces)
+  auto fscr_addr = [&](int w, int m) {
+    const int i = w * kLutMaxM + m;
+    return lut_piece(kLutPieceMisc + 1 + i / 32) + 4u * (i % 32);
+  };
+  const int n8 = K / 8;  // 16-byte groups per row
+  if (DT == 0) {
+    for (int m = 0; m < M; ++m) {
+      float mx = 0.f;
+      for (int i = threadIdx.x; i < n8; i += kLutThreads) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(m) * K) + i);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mx = fmaxf(mx, fmaxf(fabsf(bf16lo_to_f32(wv[k])), fabsf(bf16hi_to_f32(wv[k]))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      if (lane == 0) sts32(fscr_addr(warp, m), __float_as_uint(mx));
+    }
+  }
+  __syncthreads();
+  if (DT == 0 && threadIdx.x < M) {
+    float mx = 0.f;
+    for (int w = 0; w < kLutWarps; ++w)
+      mx = fmaxf(mx, __uint_as_float(lds32(fscr_addr(w, threadIdx.x))));
+    // F = exponent of mx minus 14: mx * 2^-F lies in [2^14, 2^15)
+    int F = 0;
+    if (mx > 0.f && mx == mx) {
+      const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+      F = max(-126, min(127, e - 14));
+    }
+    sts32(misc + 4u * threadIdx.x, static_cast<uint32_t>(F));
+  }
+  __syncthreads();
+  {
+    // convert / copy: thread -> 8 consecutive values of one row
+    const int groups = M * kbx * 8;  // 16-byte groups of staged x
+    for (int i = threadIdx.x; i < groups; i += kLutThreads) {
+      const int m = i / (kbx * 8), rem = i - m * kbx * 8;
+      const int j = rem >> 3, c = rem & 7;  // block j, values 8c .. 8c+7
+      const int k0 = j * kBlock + 8 * c;
+      uint4 out = make_uint4(0, 0, 0, 0);
+      if (k0 < K) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(m) * K + k0));
+        if (DT == 0) {
+          const int F = static_cast<int>(lds32(misc + 4u * m));
+          const float sc = __uint_as_float(static_cast<uint32_t>(127 - F) << 23);
+          out.x = pack_f16x2(bf16lo_to_f32(v.x) * sc, bf16hi_to_f32(v.x) * sc);
+          out.y = pack_f16x2(bf16lo_to_f32(v.y) * sc, bf16hi_to_f32(v.y) * sc);
+          out.z = pack_f16x2(bf16lo_to_f32(v.z) * sc, bf16hi_to_f32(v.z) * sc);
+          out.w = pack_f16x2(bf16lo_to_f32(v.w) * sc, bf16hi_to_f32(v.w) * sc);
+        } else {
+          out = v;
+        }
+      }
+      sts128(lut_x_addr(xbase, kbx, m, j, 16 * c), out);
+    }
+  }
+
+  // per-lane fold factors 2^F for its D columns 2t, 2t+1
+  float f0 = 0.f, f1 = 0.f;
+  {
+    const int m0 = 2 * t, m1 = 2 * t + 1;
+    if (DT == 0) {
+      if (m0 < M) f0 = __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(lds32(misc + 4u * m0))) << 23);
+      if (m1 < M) f1 = __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(lds32(misc + 4u * m1))) << 23);
+    } else {
+      f0 = m0 < M ? 1.f : 0.f;
+      f1 = m1 < M ? 1.f : 0.f;
+    }
+  }
+  __syncthreads();  // table and x are complete
+
+  // 4. block scales.  Lane l computes rows l & 15, blocks 2 (l >> 4) + {0, 1}
+  //    of a box and keeps them in the warp's scale slot: float (j, r) (block
+  //    j, tile row r) at index 16 j + r, indices 32.. rotated by 16 floats so
+  //    that the two half-warps store to different banks.  With M = 1 the
+  //    slot holds s * 2^F of the single row of x.
+  const float off = DQ ? __ldg(sv.offset) : 0.f;
+  // Raw scale data of one box: lane l takes tile row l & 15 and blocks
+  // 2 (l >> 4) and 2 (l >> 4) + 1 of the box.  With K / 64 even the two int8
+  // codes are one aligned 16-bit word and share their scale2 (the pair never
+  // straddles a multiple of 256); otherwise two byte loads and two scale2.
+  // The loads run two boxes ahead of their use.
+  const int srow = lane & 15, sjb = 2 * (lane >> 4);
+  const bool kb_even = (KB & 1) == 0;
+  struct Raw {
+    uint32_t q2;     // the two int8 codes (bytes 0, 1)
+    float a, b;      // scale2 of the two blocks (DQ), or their fp32 absmax
+    uint32_t okm;    // bit h: block h exists
+  };
+  auto scale_load = [&](int tile, int bb, Raw& r) {
+    const int row = tile * 16 + srow;
+    const int jb = bb * 4 + sjb;
+    r.q2 = 0;
+    r.a = r.b = 0.f;
+    r.okm = row < N ? (jb + 1 < KB ? 3u : (jb < KB ? 1u : 0u)) : 0u;
+    if (r.okm) {
+      const int64_t b0 = static_cast<int64_t>(row) * KB + jb;
+      if (DQ) {
+        if (kb_even) {
+          r.q2 = __ldg(reinterpret_cast<const uint16_t*>(sv.absmax_q + b0));
+          r.a = r.b = __ldg(sv.scale2 + (b0 >> 8));
+        } else {
+          r.q2 = static_cast<uint8_t>(__ldg(sv.absmax_q + b0));
+          r.a = __ldg(sv.scale2 + (b0 >> 8));
+          if (r.okm & 2u) {
+            r.q2 |= static_cast<uint32_t>(static_cast<uint8_t>(__ldg(sv.absmax_q + b0 + 1))) << 8;
+            r.b = __ldg(sv.scale2 + ((b0 + 1) >> 8));
+          }
+        }
+      } else {
+        r.a = __ldg(sv.absmax + b0);
+        if (r.okm & 2u) r.b = __ldg(sv.absmax + b0 + 1);
+      }
+    }
+  };
+  auto slot_off = [](int idx) -> uint32_t {
+    return idx < 32 ? 4u * idx : 256u + 4u * ((idx + 16) & 31);
+  };
+  const uint32_t slot0 = lut_piece(kLutPieceScale + 4 * warp);
+  // with M = 1 the slot holds s * 2^F of row 0 of x (the same for every lane)
+  const float fs =
+      M != 1 ? 1.f
+             : (DT == 0 ? __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(lds32(misc))) << 23)
+                        : 1.f);
+  const uint32_t soff0 = slot_off(sjb * 16 + srow), soff1 = slot_off((sjb + 1) * 16 + srow);
+  auto scale_store = [&](int buf, const Raw& r) {
+    // rows past N and blocks past K get scale 0
+    float s0, s1;
+    if (DQ) {
+      s0 = __fmaf_rn(static_cast<float>(static_cast<int8_t>(r.q2 & 0xFFu)), r.a, off);
+      s1 = __fmaf_rn(static_cast<float>(static_cast<int8_t>((r.q2 >> 8) & 0xFFu)), r.b, off);
+    } else {
+      s0 = r.a;
+      s1 = r.b;
+    }
+    s0 = (r.okm & 1u) ? s0 * fs : 0.f;
+    s1 = (r.okm & 2u) ? s1 * fs : 0.f;
+    sts32(slot0 + 512u * buf + soff0, __float_as_uint(s0));
+    sts32(slot0 + 512u * buf + soff1, __float_as_uint(s1));
+  };
+
+  // 5. per-lane constants.  MMA row g is tile row 2g, MMA row g + 8 is tile
+  //    row 2g + 1, so that the four rows a half-warp reads in one load sit
+  //    on distinct banks under the 128-byte swizzle: row r's 16-byte chunk c
+  //    is at chunk c ^ (r & 7), and this lane's 8 bytes of block j are chunk
+  //    2j + (t >> 1), half t & 1.
+  const uint32_t SB0 = 256u * g + 32u * (g & 3) + 16u * (t >> 1) + 8u * (t & 1);
+  const uint32_t SB1 = (SB0 + 128u) ^ 16u;
+  const int mx_row = min(g, M - 1);
+  const uint32_t xrow = xbase + static_cast<uint32_t>(mx_row * kbx * 128);
+  const uint32_t xo0 = static_cast<uint32_t>((32 * t + 16 * mx_row) & 127);
+  const uint32_t xo1 = static_cast<uint32_t>((32 * t + 16 + 16 * mx_row) & 127);
+  // table address = [lane * 4, code byte, 0x01, 0]: the table sits at 0x10000
+  const uint32_t L = kLutTable | (static_cast<uint32_t>(lane) << 2);
+
+  // stream positions: consumer, scale loader (two boxes ahead), producer
+  // (kLutStages ahead, lane 0); each advances one box at a time
+  auto advance = [&](int& tile, int& bi) {
+    if (++bi == nmy) {
+      bi = 0;
+      tile += tile_stride;
+    }
+  };
+  // raw scales: box q + 1 in rA, box q + 2 in rB while box q is consumed
+  Raw rA, rB;
+  int s_tile = tile0, s_bi = 0;
+  if (total > 0) {
+    scale_load(s_tile, pb0 + s_bi, rA);
+    scale_store(0, rA);
+    advance(s_tile, s_bi);
+  }
+  if (total > 1) {
+    scale_load(s_tile, pb0 + s_bi, rA);
+    advance(s_tile, s_bi);
+  }
+  if (total > 2) {
+    scale_load(s_tile, pb0 + s_bi, rB);
+    advance(s_tile, s_bi);
+  }
+  int p_tile = tile0, p_bi = 0;
+  for (int i = 0; i < min(kLutStages, total); ++i) advance(p_tile, p_bi);
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  bool dead = false;
+  int waited_q = -1;  // last box whose stage wait succeeded (waits go in order)
+  int issued_n = min(kLutStages, total);
+  int c_tile = tile0, c_bi = 0, u = 0;
+  int st = 0;
+  uint32_t ph = 0;
+
+  for (int q = 0; q < total; ++q) {
+    __syncwarp();
+    if (!dead) {
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar_of(st), ph));
+      if (!ok) dead = true;
+      else waited_q = q;
+    }
+    const uint32_t stage = ring + st * kLutBoxBytes;
+    const uint32_t w0 = stage + SB0, w1 = stage + SB1;
+    const uint32_t xbox = xrow + static_cast<uint32_t>((pb0 + c_bi) * 512);
+    const uint32_t sl = slot0 + 512u * (q & 1) + 8u * g;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint2 wg = lds64(w0 ^ (32u * j));
+      const uint2 wh = lds64(w1 ^ (32u * j));
+      // x: values 16t .. 16t+15 of block j of row g; lanes whose column
+      // g is past M load nothing (their outputs are never stored), so a
+      // load moves only the M rows' bytes
+      uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+      if (g < M) {
+        xa = lds128_lut(xbox + 128u * j + xo0);
+        xb = lds128_lut(xbox + 128u * j + xo1);
+      }
+      const uint32_t xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      const uint32_t wr[2][2] = {{wg.x, wg.y}, {wh.x, wh.y}};
+      float d[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // MMA i: bytes 2i, 2i+1 of the lane's 8 bytes (word i / 2, bytes 2(i&1), +1)
+        const uint32_t sel0 = 0x7604u | (static_cast<uint32_t>(2 * (i & 1)) << 4);
+        const uint32_t sel1 = 0x7604u | (static_cast<uint32_t>(2 * (i & 1) + 1) << 4);
+        const uint32_t a0 = lds32(prmt_lut(wr[0][i >> 1], L, sel0));
+        const uint32_t a1 = lds32(prmt_lut(wr[1][i >> 1], L, sel0));
+        const uint32_t a2 = lds32(prmt_lut(wr[0][i >> 1], L, sel1));
+        const uint32_t a3 = lds32(prmt_lut(wr[1][i >> 1], L, sel1));
+        if (i == 0)
+          mma_f16_first(d, a0, a1, a2, a3, xr[2 * i], xr[2 * i + 1]);
+        else
+          mma_f16_acc(d, a0, a1, a2, a3, xr[2 * i], xr[2 * i + 1]);
+      }
+      // (s of tile row 2g, of row 2g + 1) for block j
+      const uint2 sg = lds64(sl + (j < 2 ? 64u * j : 256u + 64u * ((j + 1) & 1)));
+      const float sa = __uint_as_float(sg.x), sb = __uint_as_float(sg.y);
+      if (M == 1) {
+        acc[0] = __fmaf_rn(d[0], sa, acc[0]);
+        acc[2] = __fmaf_rn(d[2], sb, acc[2]);
+      } else {
+        acc[0] = __fmaf_rn(d[0], sa * f0, acc[0]);
+        acc[1] = __fmaf_rn(d[1], sa * f1, acc[1]);
+        acc[2] = __fmaf_rn(d[2], sb * f0, acc[2]);
+        acc[3] = __fmaf_rn(d[3], sb * f1, acc[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && !dead && q + kLutStages < total) {
+      fence_proxy_async_smem();
+      issue_at(p_tile, pb0 + p_bi, st);
+      advance(p_tile, p_bi);
+      ++issued_n;
+    }
+    // scales of the next box into the other slot; raw loads for box q + 3
+    if (q + 1 < total) {
+      scale_store((q + 1) & 1, rA);
+      rA = rB;
+      if (q + 3 < total) {
+        scale_load(s_tile, pb0 + s_bi, rB);
+        advance(s_tile, s_bi);
+      }
+    }
+    if (++st == kLutStages) {
+      st = 0;
+      ph ^= 1u;
+    }
+    // end of a unit (tile, part): reduce over the P parts and store y
+    if (++c_bi == nmy) {
+      const int row = c_tile * 16 + 2 * g;
+      auto store = [&](const float (&v)[4]) {
+        const int c0 = 2 * t, c1 = 2 * t + 1;
+        if (row < N) {
+          if (c0 < M) y[static_cast<int64_t>(c0) * N + row] = round_to_dt<DT>(v[0]);
+          if (c1 < M) y[static_cast<int64_t>(c1) * N + row] = round_to_dt<DT>(v[1]);
+        }
+        if (row + 1 < N) {
+          if (c0 < M) y[static_cast<int64_t>(c0) * N + row + 1] = round_to_dt<DT>(v[2]);
+          if (c1 < M) y[static_cast<int64_t>(c1) * N + row + 1] = round_to_dt<DT>(v[3]);
+        }
+      };
+      if (P == 1) {
+        store(acc);
+      } else {
+        auto red_addr = [&](int w, int par, int l) {
+          return lut_piece(kLutPieceRed + 8 * w + 4 * par + (l >> 3)) + 16u * (l & 7);
+        };
+        sts128(red_addr(warp, u & 1, lane),
+               make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                          __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + slot), "r"(P * 32) : "memory");
+        if (part == 0) {
+          float v[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int p = 0; p < P; ++p) {
+            const uint4 r = lds128_lut(red_addr(slot * P + p, u & 1, lane));
+            v[0] += __uint_as_float(r.x);
+            v[1] += __uint_as_float(r.y);
+            v[2] += __uint_as_float(r.z);
+            v[3] += __uint_as_float(r.w);
+          }
+          store(v);
+        }
+      }
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      c_bi = 0;
+      c_tile += tile_stride;
+      ++u;
+    }
+  }
+  // drain copies still landing (only after a wait gave up)
+  if (lane == 0 && dead) {
+    for (int s2 = 0; s2 < kLutStages; ++s2) {
+      const int n_st = issued_n > s2 ? (issued_n - s2 + kLutStages - 1) / kLutStages : 0;
+      const int w_st = waited_q >= s2 ? (waited_q - s2) / kLutStages + 1 : 0;
+      if (n_st > w_st) mbar_wait_drain(bar_of(s2), static_cast<uint32_t>((n_st - 1) & 1));
+    }
+  }
+}
+
+}  // namespace nf4q

@@ -3,6 +3,7 @@
 // library is one translation unit.
 #include "nf4q.h"
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -14,6 +15,7 @@
 #include "double_quant.cuh"
 #include "gemm.cuh"
 #include "gemm_dx.cuh"
+#include "gemv_lut.cuh"
 #include "gemv_mma.cuh"
 #include "host.h"
 #include "int8.cuh"
@@ -132,6 +134,28 @@ nf4q_status gemv_attr_ready() {
   return NF4Q_OK;
 }
 
+// Opt the block-scale-folded GEMV kernels in to their shared memory (once
+// per device).
+nf4q_status gemv_lut_attr_ready() {
+  static bool done[kMaxDevices] = {false};
+  static std::mutex mu;
+  int dev = 0;
+  nf4q_status st = current_device(&dev);
+  if (st != NF4Q_OK) return st;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return NF4Q_OK;
+  const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  const int b = static_cast<int>(kLutSmemTop);
+  const char* what = "cudaFuncSetAttribute (GEMV, folded)";
+  if ((st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<0, true>, A, b), what)) != NF4Q_OK ||
+      (st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<1, true>, A, b), what)) != NF4Q_OK ||
+      (st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<0, false>, A, b), what)) != NF4Q_OK ||
+      (st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<1, false>, A, b), what)) != NF4Q_OK)
+    return st;
+  done[dev] = true;
+  return NF4Q_OK;
+}
+
 // Opt the dequantize kernels in to their dynamic shared memory (once per
 // device).
 nf4q_status dequantize_attr_ready() {
@@ -223,6 +247,16 @@ CodeValues code_values(int code) {
   CodeValues C;
   for (int i = 0; i < 16; ++i) C.v[i] = tables().values[code][i];
   return C;
+}
+
+// fp16 bits (round to nearest even) of the 16 code values.
+HalfCodes half_codes(int code) {
+  HalfCodes H;
+  for (int i = 0; i < 16; ++i) {
+    const __half h = __float2half_rn(tables().values[code][i]);
+    std::memcpy(&H.h[i], &h, sizeof(uint16_t));
+  }
+  return H;
 }
 
 int64_t grid_for(int64_t work_items, int64_t per_cta, int64_t cap) {
@@ -463,15 +497,22 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream) {
                 code_values(wq->code));
 }
 
-nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
-                      void* stream) {
+}  // extern "C"
+
+namespace nf4q {
+namespace {
+
+// Checks shared by both GEMV entry points.  *done = true when nothing (or
+// only the y = 0 of an empty contraction) was to be launched.
+nf4q_status gemv_checks(const nf4q_weight* wq, const void* x, int32_t M, void* y,
+                        cudaStream_t s, bool* done) {
+  *done = true;
   nf4q_status st = check_shape(wq);
   if (st != NF4Q_OK) return st;
   if (M < 1 || M > NF4Q_GEMV_MAX_M) return NF4Q_ERR_UNSUPPORTED;
   if (wq->rows == 0) return NF4Q_OK;
   if (!x || !y) return NF4Q_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return NF4Q_ERR_ALIGNMENT;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (wq->cols == 0) {  // empty contraction: y = 0
     return cuda_check(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * wq->rows * 2, s),
                       "cudaMemsetAsync (y of an empty contraction)");
@@ -479,6 +520,79 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   if ((st = check_scales(wq)) != NF4Q_OK) return st;
   if (!tables().ok) return NF4Q_ERR_UNSUPPORTED;
   if (wq->rows > (1ll << 30) || wq->cols > (1ll << 30)) return NF4Q_ERR_UNSUPPORTED;
+  *done = false;
+  return NF4Q_OK;
+}
+
+// 2D tensor map of the packed weight [rows x cols/2 bytes], boxes of
+// `box_rows` rows x 128 bytes with the 128-byte swizzle.
+nf4q_status gemv_weight_map(const nf4q_weight* wq, int box_rows, CUtensorMap* tw) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cuda_fail("cuTensorMapEncodeTiled: driver entry point not found");
+  nf4q_status st = ensure_context();
+  if (st != NF4Q_OK) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(wq->cols / 2), static_cast<cuuint64_t>(wq->rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(wq->cols / 2)};
+  cuuint32_t box[2] = {kGemvSeg / 2, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return cu_check(enc(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                  "cuTensorMapEncodeTiled (GEMV weight)");
+}
+
+// Staged x of the folded GEMV: 64-blocks per row, a multiple of four.
+int64_t lut_kbx(int64_t K) { return (K / kBlock + 3) / 4 * 4; }
+
+// Whether the folded GEMV takes this call (M <= 8 and x fits its staging).
+bool lut_fits(int64_t K, int32_t M) {
+  return M <= kLutMaxM && static_cast<int64_t>(M) * lut_kbx(K) * 128 <= kLutXBytes;
+}
+
+// The block-scale-folded GEMV (gemv_lut.cuh).  Chooses the number of K
+// parts P a tile is split into (over P warps of a CTA) by the modelled
+// efficiency: tiles per round of the grid times boxes per part.
+nf4q_status gemv_lut_launch(const nf4q_weight* wq, const void* x, int32_t M, void* y,
+                            cudaStream_t s) {
+  nf4q_status st = gemv_lut_attr_ready();
+  if (st != NF4Q_OK) return st;
+  const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
+  const int64_t T = (N + 15) / 16;
+  const int64_t nbox = (K / kBlock + 3) / 4;
+  const int64_t sms = sm_count();
+  int bestP = 1;
+  double best = -1.0;
+  for (int P = 1; P <= kLutWarps; P *= 2) {
+    if (P > nbox) break;
+    const int64_t SL = kLutWarps / P;
+    const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
+    const int64_t rounds = (T + grid * SL - 1) / (grid * SL);
+    const int64_t per = (nbox + P - 1) / P;
+    const double eff = static_cast<double>(T) * nbox /
+                       (static_cast<double>(sms) * kLutWarps * rounds * per);
+    if (eff > best + 1e-9) {
+      best = eff;
+      bestP = P;
+    }
+  }
+  const int64_t SL = kLutWarps / bestP;
+  const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
+  CUtensorMap tw;
+  if ((st = gemv_weight_map(wq, 16, &tw)) != NF4Q_OK) return st;
+  const bool bf = wq->compute_dtype == NF4Q_DT_BF16;
+  const auto k = wq->double_quant ? (bf ? gemv_lut_kernel<0, true> : gemv_lut_kernel<1, true>)
+                                  : (bf ? gemv_lut_kernel<0, false> : gemv_lut_kernel<1, false>);
+  return launch("gemv_lut_kernel", k, dim3(static_cast<unsigned>(grid)), dim3(kLutThreads),
+                kLutSmemTop, s, nullptr, 0, tw, scale_view(wq),
+                static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), N, K,
+                static_cast<int>(M), bestP, static_cast<int>(lut_kbx(K)), half_codes(wq->code));
+}
+
+// The bit-faithful GEMV (gemv_mma.cuh): w_hat rebuilt exactly inside the
+// contraction.
+nf4q_status gemv_exact_launch(const nf4q_weight* wq, const void* x, int32_t M, void* y,
+                              cudaStream_t s) {
+  nf4q_status st;
   const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
   if ((st = gemv_attr_ready()) != NF4Q_OK) return st;
   // M <= 4: one 8-column MMA tile and 16 rows per CTA; M = 5..8: 32 rows,
@@ -506,21 +620,8 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   split = (nchunks + per - 1) / per;  // CTAs that get chunks
   const int stages = std::min(kGemvStages, per);
   const size_t smem = gemv_smem_bytes(R, NT, stages, split);
-  EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return cuda_fail("cuTensorMapEncodeTiled: driver entry point not found");
-  if ((st = ensure_context()) != NF4Q_OK) return st;
   CUtensorMap tw;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[2] = {kGemvSeg / 2, static_cast<cuuint32_t>(kGemvRows * R)};
-    cuuint32_t es[2] = {1, 1};
-    st = cu_check(enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq->packed, dims, strides, box, es,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
-                  "cuTensorMapEncodeTiled (GEMV weight)");
-    if (st != NF4Q_OK) return st;
-  }
+  if ((st = gemv_weight_map(wq, kGemvRows * R, &tw)) != NF4Q_OK) return st;
   if (tiles * split > 0x7FFFFFFF) return NF4Q_ERR_UNSUPPORTED;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -534,6 +635,30 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   return launch("gemv_mma_kernel", gemv_kernel(code, NT, R, wq->compute_dtype),
                 dim3(static_cast<unsigned>(tiles * split)), dim3(kGemvWarps * 32), smem, s, attr,
                 split > 1 ? 1u : 0u, tw, sv, xp, yp, N, K, static_cast<int>(M), per, stages, C);
+}
+
+}  // namespace
+}  // namespace nf4q
+
+extern "C" {
+
+nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
+                      void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool done = false;
+  nf4q_status st = gemv_checks(wq, x, M, y, s, &done);
+  if (st != NF4Q_OK || done) return st;
+  if (lut_fits(wq->cols, M)) return gemv_lut_launch(wq, x, M, y, s);
+  return gemv_exact_launch(wq, x, M, y, s);
+}
+
+nf4q_status nf4q_gemv_exact(const nf4q_weight* wq, const void* x, int32_t M, void* y,
+                            void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool done = false;
+  nf4q_status st = gemv_checks(wq, x, M, y, s, &done);
+  if (st != NF4Q_OK || done) return st;
+  return gemv_exact_launch(wq, x, M, y, s);
 }
 
 nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M, void* Y,

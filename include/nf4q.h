@@ -191,13 +191,28 @@ nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight*
 nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream);
 
 /* Decode-shaped matmul, 1 <= M <= 16 (tutorial sec. 3.4, sec. 七 myth 5:
- * memory-bandwidth bound).  y[m, n] = sum_k x[m, k] * w_hat[n, k] with
- * w_hat exactly as nf4q_dequantize produces it, fp32 accumulation, output
- * rounded to the compute dtype.
+ * memory-bandwidth bound): y[m, n] = sum_k x[m, k] * w_hat[n, k], fp32
+ * accumulation, output rounded to the compute dtype.
  *   x: device [M x cols], y: device [M x rows], both of wq->compute_dtype
- *   (bf16 or fp16) and 16-byte aligned. */
+ *   (bf16 or fp16) and 16-byte aligned.
+ * For M <= 8 (when M * cols <= 30720, the staging room for x) the block
+ * scale is folded: y = sum_b s_b * sum_{k in b} x_k * code_value[code_k],
+ * with the code values rounded to fp16 and x converted to fp16 after a
+ * power-of-two scaling per row (exact for every bf16 x within 2^31 of its
+ * row's largest |x|).  This differs from x . w_hat^T only by the rounding of
+ * w_hat = bf16(code_value * s_b) and of the code values: at most 2^-8 + 2^-11
+ * of |x_k w_hat_k| per term (fp16 compute dtype: 2^-10), signed like those
+ * roundings.
+ * Other calls, and nf4q_gemv_exact always, use w_hat itself. */
 nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M,
                       void* y, void* stream);
+
+/* nf4q_gemv with w_hat rebuilt bit for bit inside the contraction: y =
+ * x . w_hat^T with w_hat exactly as nf4q_dequantize produces it, fp32
+ * accumulation (only the order of the additions differs from an exact
+ * dot product).  Same arguments and errors as nf4q_gemv. */
+nf4q_status nf4q_gemv_exact(const nf4q_weight* wq, const void* x, int32_t M,
+                            void* y, void* stream);
 
 /* Prefill-shaped matmul on the tcgen05 tensor cores, M >= 1 (intended for
  * M >= 64).  Same contraction and output as nf4q_gemv: Y [M x rows] =

@@ -1,13 +1,15 @@
 """Single workloads for profiling one kernel at a time (ncu / nsight).
 
-    python -m dequant_matmul_quantize_b300.profile_cases CASE [CASE ...]
+    python profile_cases.py CASE [CASE ...]
 
 Each case builds its seeded synthetic input, runs the library call twice
 (a warm-up and the one to capture) and synchronizes.  Cases:
 
     quant11008   nf4q_quantize_dq then nf4q_dequantize, 11008x4096 decode weight
     gemv70b      nf4q_gemv M=1 on the 28672x8192 weight (NF4)
+    gemv70b_exact  nf4q_gemv_exact M=1 on the same weight
     gemv4096     nf4q_gemv M=1 on the 4096x4096 decode weight
+    gemv11008    nf4q_gemv M=1 on the 11008x4096 decode weight
     gemv70b_m16  nf4q_gemv M=16 on the 28672x8192 weight (NF4)
     gemm2048     nf4q_gemm M=2048 on the 14336x4096 prefill weight
     gemm64       nf4q_gemm M=64 on the 14336x4096 prefill weight
@@ -24,7 +26,7 @@ import ctypes
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -50,16 +52,17 @@ def _run(case: str, torch, nq, synth) -> None:
             ok(L.nf4q_quantize_dq(w.data_ptr(), nq.IN_BF16, R(s), ws.data_ptr(), ws.numel(), sp),
                "quantize_dq")
             ok(L.nf4q_dequantize(R(s), out.data_ptr(), sp), "dequantize")
-    elif case in ("gemv70b", "gemv70b_m16"):
+    elif case in ("gemv70b", "gemv70b_m16", "gemv70b_exact"):
         M = 16 if case.endswith("m16") else 1
+        fn = L.nf4q_gemv_exact if case.endswith("exact") else L.nf4q_gemv
         qw = nq.quantize(synth.mlp70b_weight(device=dev))
         s = qw.struct()
         x = synth.mlp70b_x(M, device=dev)
         y = torch.empty(M, qw.rows, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
-            ok(L.nf4q_gemv(R(s), x.data_ptr(), M, y.data_ptr(), sp), "gemv")
-    elif case == "gemv4096":
-        w, x = synth.llama7b_decode(0, device=dev)
+            ok(fn(R(s), x.data_ptr(), M, y.data_ptr(), sp), "gemv")
+    elif case in ("gemv4096", "gemv11008"):
+        w, x = synth.llama7b_decode(0 if case == "gemv4096" else 1, device=dev)
         qw = nq.quantize(w)
         s = qw.struct()
         y = torch.empty(1, qw.rows, dtype=torch.bfloat16, device=dev)

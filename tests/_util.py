@@ -61,3 +61,24 @@ def check_matmul(y_gpu_bits: np.ndarray, x_bits: np.ndarray, what_bits: np.ndarr
     worst = np.max(err / tol) if err.size else 0.0
     assert np.all(err <= tol), f"{what}: worst err/tol = {worst:.3f}"
     return worst
+
+
+def full_check(w, code: str, double_quant=True, what=""):
+    """Quantize on the GPU and in the oracle; compare every byte of the
+    stored state and of the dequantized weights.  Returns the GPU weight and
+    the ORACLE's w_hat (bit patterns, shaped like w)."""
+    import dequant_matmul_quantize_b300 as nq
+    qw = nq.quantize(w.cuda(), code, double_quant)
+    what_gpu = nq.dequantize(qw)
+    torch.cuda.synchronize()
+    g = gpu_state(qw)
+    ref = oracle_state(as_f32(w).reshape(-1), code, double_quant)
+    assert_bits_equal(g["absmax"], ref["absmax"], what + " absmax")
+    assert_bits_equal(g["packed"], ref["packed"], what + " packed")
+    if double_quant:
+        assert_bits_equal(np.array([g["offset"]]), np.array([ref["offset"]]), what + " offset")
+        assert_bits_equal(g["scale2"], ref["scale2"], what + " scale2")
+        assert_bits_equal(g["absmax_q"], ref["absmax_q"], what + " absmax_q")
+    w_hat = o.dequantize(ref["packed"], ref["scales"], CODE_ID[code])
+    assert_bits_equal(bf16_bits(what_gpu).reshape(-1), w_hat, what + " w_hat")
+    return qw, w_hat.reshape(w.shape)

@@ -1,0 +1,150 @@
+"""The block-scale-folded GEMV (nf4q_gemv for M <= 8) against the oracle.
+
+The folded kernel multiplies x by code_value * s_b (code values rounded to
+fp16) instead of by w_hat = bf16(code_value * s_b); it is held to the same
+tolerance as every matmul here, |y - y_ref| <= 2e-3 * sum|x w_hat| + one ulp
+of y_ref, with y_ref the fp64 product of x and the ORACLE's w_hat.
+
+Shapes are chosen so that the launch picks each split of K over the warps of
+a CTA (P = 1, 2, 4, 8, 16), with ragged row tiles and a K that is not a
+multiple of the 256-column boxes.  The error analysis of the fold is checked
+on its own inputs: random activations, activations whose signs follow the
+rounding of w_hat (the sign-adversarial case, inside the tolerance because
+the mean relative bf16 rounding error is below 2e-3), and activations that
+also sit only on the weights with the largest rounding error (bounded by the
+per-term analytic bound 2^-8 + 2^-11, which exceeds the tolerance)."""
+import numpy as np
+import pytest
+import torch
+
+import dequant_matmul_quantize_b300 as nq
+import synth
+from oracle import nf4_oracle as o
+from tests._util import CODE_ID, bf16_bits, check_matmul, full_check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from dequant_matmul_quantize_b300 import build
+    build.build()
+    nq.lib()
+    yield
+    torch.cuda.synchronize()
+    assert nq.device_error() == 0
+
+
+# (rows, cols) -> the split the launch picks: (37, 320) P=2, (256, 1024) P=4,
+# (129, 4160) P=16, (4000, 256) P=1, (2400, 1024) P=4, (700, 2112) P=8
+SHAPES = [(37, 320), (256, 1024), (129, 4160), (4000, 256), (2400, 1024), (700, 2112)]
+
+
+@pytest.mark.parametrize("code", ["nf4", "fp4"])
+@pytest.mark.parametrize("M", [1, 2, 5, 8])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_folded_gemv_parity(code, M, shape):
+    w = synth.normal_weight(*shape, 0.02, seed=shape[0] + M, outlier_frac=1e-3)
+    qw, w_hat = full_check(w, code, True, f"{code} {shape}")
+    x = synth.activations(M, shape[1], seed=100 + M)
+    y = nq.gemv(qw, x.cuda())
+    check_matmul(bf16_bits(y), bf16_bits(x), w_hat, f"folded {code} M={M} {shape}")
+
+
+@pytest.mark.parametrize("M", [1, 6])
+def test_folded_gemv_fp16_and_no_double_quant(M):
+    w = synth.normal_weight(300, 1088, 0.02, seed=7)
+    # fp16 compute dtype (the stored state is the same; w_hat is fp16)
+    qw = nq.quantize(w.cuda(), "nf4", True, compute_dtype="f16")
+    ref = full_check(w, "nf4", True, "fp16 state")[0]
+    assert torch.equal(qw.packed, ref.packed)
+    st = o.quantize_full(w.float().numpy().reshape(-1), o.CODE_NF4)
+    scales = o.block_scales(st["absmax_q"], st["scale2"], st["offset"])
+    w_hat16 = o.dequantize(st["packed"], scales, o.CODE_NF4, dtype=o.DT_F16).reshape(300, 1088)
+    x = synth.activations(M, 1088, seed=8).to(torch.float16)
+    y = nq.gemv(qw, x.cuda())
+    check_matmul(y.cpu().view(torch.int16).numpy().view(np.uint16),
+                 x.view(torch.int16).numpy().view(np.uint16), w_hat16, "folded fp16", o.DT_F16)
+    # no double quantization: the fp32 absmax is the scale
+    qn, w_hat_n = full_check(w, "fp4", False, "no-dq")
+    xb = synth.activations(M, 1088, seed=9)
+    check_matmul(bf16_bits(nq.gemv(qn, xb.cuda())), bf16_bits(xb), w_hat_n, "folded no-dq")
+
+
+def test_folded_gemv_rows_of_x_far_apart_in_magnitude():
+    """Each row of x gets its own power-of-two scaling before it becomes
+    fp16: rows at 2^-100 .. 2^100, an all-zero row, and a row whose values
+    span 2^-30 .. 2^0 are all inside the tolerance."""
+    K = 1024
+    w = synth.normal_weight(200, K, 0.02, seed=11)
+    qw, w_hat = full_check(w, "nf4", True, "x scales")
+    base = synth.activations(7, K, seed=12).float()
+    scale = torch.tensor([2.0 ** -100, 2.0 ** -20, 1.0, 2.0 ** 20, 2.0 ** 100, 0.0, 1.0])
+    x = base * scale[:, None]
+    g = torch.Generator().manual_seed(13)
+    x[6] = x[6] * torch.exp2(-30.0 * torch.rand(K, generator=g))
+    x = x.to(torch.bfloat16)
+    y = nq.gemv(qw, x.cuda())
+    assert torch.all(y[5] == 0)
+    check_matmul(bf16_bits(y), bf16_bits(x), w_hat, "x row scales")
+
+
+def test_folded_gemv_is_deterministic_and_near_the_exact_kernel():
+    w = synth.normal_weight(1500, 2048, 0.02, seed=14, outlier_frac=1e-3)
+    qw, w_hat = full_check(w, "nf4", True, "determinism")
+    x = synth.activations(3, 2048, seed=15).cuda()
+    y1 = nq.gemv(qw, x)
+    y2 = nq.gemv(qw, x)
+    assert torch.equal(y1, y2)
+    ye = nq.gemv_exact(qw, x)
+    check_matmul(bf16_bits(y1), bf16_bits(x), w_hat, "folded")
+    check_matmul(bf16_bits(ye), bf16_bits(x), w_hat, "exact")
+
+
+def _fold_error_terms(w_hat_bits, scales, packed, code):
+    """Per weight: the value the folded kernel multiplies x by, fp16(code)
+    * s (exact in fp64), and w_hat; both [N, K] float64."""
+    idx = o.unpack_nibbles(packed)
+    c16 = o.code_table(code).astype(np.float16).astype(np.float64)
+    s = np.repeat(np.asarray(scales, np.float64), 64)
+    folded = (c16[idx] * s).reshape(w_hat_bits.shape)
+    return folded, o.bf16_bits_to_f32(w_hat_bits).astype(np.float64)
+
+
+@pytest.mark.parametrize("code", ["nf4", "fp4"])
+def test_folded_gemv_error_analysis(code):
+    N, K = 512, 4096
+    w = synth.normal_weight(N, K, 0.02, seed=16)
+    qw, w_hat = full_check(w, code, True, "error analysis")
+    st = o.quantize_full(w.float().numpy().reshape(-1), CODE_ID[code])
+    scales = o.block_scales(st["absmax_q"], st["scale2"], st["offset"])
+    folded, what = _fold_error_terms(w_hat, scales, st["packed"], CODE_ID[code])
+    delta = folded - what
+
+    # random activations: far inside the tolerance
+    x = synth.activations(1, K, seed=17)
+    worst_random = check_matmul(bf16_bits(nq.gemv(qw, x.cuda())), bf16_bits(x), w_hat,
+                                "random x")
+    assert worst_random < 0.2
+
+    # signs of x follow the rounding of w_hat of row 0, |x| = 1
+    xs = np.where(delta[0] >= 0, 1.0, -1.0).astype(np.float32)[None, :]
+    xt = torch.from_numpy(xs).to(torch.bfloat16)
+    y = nq.gemv(qw, xt.cuda())
+    worst_sign = check_matmul(bf16_bits(y[:, :1]), bf16_bits(xt), w_hat[:1], "sign-adversarial")
+    assert worst_sign < 1.0
+
+    # x only on the weights of row 0 whose relative rounding error exceeds
+    # 3e-3, signs aligned: beyond the 2e-3 tolerance by construction, but
+    # within the per-term bound (2^-8 + 2^-11) * sum|x w_hat| + one ulp
+    rel = np.abs(delta[0]) / np.maximum(np.abs(what[0]), 1e-300)
+    sel = (rel > 3e-3) & (what[0] != 0)
+    assert sel.sum() > 20
+    xa = np.where(sel, np.sign(delta[0]), 0.0).astype(np.float32)[None, :]
+    xat = torch.from_numpy(xa).to(torch.bfloat16)
+    ya = nq.gemv(qw, xat.cuda()).float().cpu().numpy()[0, 0]
+    y_ref, bound = o.matmul_ref(bf16_bits(xat), w_hat[:1])
+    err = abs(ya - y_ref[0, 0])
+    analytic = (2.0 ** -8 + 2.0 ** -11 + 2.0 ** -20) * bound[0, 0] + o.ulp_bf16(y_ref[0, 0])
+    assert err <= analytic, (err, analytic)

@@ -14,7 +14,7 @@ import dequant_matmul_quantize_b300 as nq
 import synth
 from oracle import nf4_oracle as o
 from tests._util import (CODE_ID, as_f32, assert_bits_equal, bf16_bits, check_matmul,
-                         gpu_state, oracle_state)
+                         full_check, gpu_state, oracle_state)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,20 +32,7 @@ def _setup():
 
 def _full_check(w: torch.Tensor, code: str, double_quant=True, what=""):
     """Quantize on the GPU and in the oracle; compare every byte."""
-    qw = nq.quantize(w.cuda(), code, double_quant)
-    what_gpu = nq.dequantize(qw)
-    torch.cuda.synchronize()
-    g = gpu_state(qw)
-    ref = oracle_state(as_f32(w).reshape(-1), code, double_quant)
-    assert_bits_equal(g["absmax"], ref["absmax"], what + " absmax")
-    assert_bits_equal(g["packed"], ref["packed"], what + " packed")
-    if double_quant:
-        assert_bits_equal(np.array([g["offset"]]), np.array([ref["offset"]]), what + " offset")
-        assert_bits_equal(g["scale2"], ref["scale2"], what + " scale2")
-        assert_bits_equal(g["absmax_q"], ref["absmax_q"], what + " absmax_q")
-    w_hat = o.dequantize(ref["packed"], ref["scales"], CODE_ID[code])
-    assert_bits_equal(bf16_bits(what_gpu).reshape(-1), w_hat, what + " w_hat")
-    return qw, w_hat.reshape(w.shape)
+    return full_check(w, code, double_quant, what)
 
 
 SMALL_SHAPES = [(1, 64), (3, 64), (5, 192), (37, 320), (64, 1024), (129, 4160), (300, 2048)]
@@ -237,13 +224,27 @@ def test_gemv_small(M, shape):
 
 
 def test_gemv_one_hot_column_is_exact():
+    """A one-hot x picks a column of w_hat: bit for bit through the exact
+    GEMV, within the matmul tolerance through the block-scale-folded one
+    (which multiplies by code * s, not by its bf16 rounding)."""
     w = synth.normal_weight(200, 512, 0.02, seed=2)
     qw, w_hat = _full_check(w, "nf4", True, "onehot")
     for k in (0, 63, 64, 300, 511):
         x = torch.zeros(1, 512, dtype=torch.bfloat16)
         x[0, k] = 1.0
-        y = nq.gemv(qw, x.cuda())
+        y = nq.gemv_exact(qw, x.cuda())
         assert np.array_equal(bf16_bits(y)[0], w_hat[:, k])
+        check_matmul(bf16_bits(nq.gemv(qw, x.cuda())), bf16_bits(x), w_hat, f"one-hot {k}")
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 12, 16])
+@pytest.mark.parametrize("shape", [(37, 320), (129, 4160)])
+def test_gemv_exact_small(M, shape):
+    w = synth.normal_weight(*shape, 0.02, seed=M * 5 + shape[0], outlier_frac=1e-3)
+    qw, w_hat = _full_check(w, "nf4", True, "gemv exact")
+    x = synth.activations(M, shape[1], seed=M + 40)
+    check_matmul(bf16_bits(nq.gemv_exact(qw, x.cuda())), bf16_bits(x), w_hat,
+                 f"gemv exact M={M} {shape}")
 
 
 @pytest.mark.parametrize("M", [4, 7])
