@@ -1,24 +1,25 @@
 #!/usr/bin/env python
-"""Benchmark of the NF4 quantize -> double quant -> dequantize -> GEMV path.
+"""Benchmark of the NF4 decode GEMV, with the rest of the path as extras.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One STEP is one pass of the whole decode-side path over the Llama-7B decode
-workload: for each of the three weights [4096x4096], [11008x4096] and
-[4096x11008] (bf16 N(0, 0.02) with 0.1 % outliers, seeds 10-12; x ~ N(0, 1)
-bf16, M = 1): nf4q_quantize_dq (absmax + codes + packing, then the double
-quantization of the scales; one call, two kernels), nf4q_dequantize (bf16
-out) and nf4q_gemv.  Inputs are resident in HBM when
-the timed region starts; L2 is flushed (256 MiB write) before every step,
-outside the step's events.  `value` is the step's algorithmic bytes divided
-by its device time (CUDA events), summed over ranks.
+One STEP is one decode token through the 32-layer Llama-3-8B-shaped stack:
+224 NF4 GEMVs (nf4q_gemv, M = 1) over the weights q [4096x4096], k, v
+[1024x4096], o [4096x4096], gate, up [14336x4096] and down [4096x14336] of
+every layer (bf16 N(0, 0.02), seed 1000 * layer + matrix, quantized once to
+NF4 with double quantization before timing; x ~ N(0, 1) bf16 per matrix).
+The packed weights and scales (3.61 GB) are far larger than L2, so every
+step reads them from HBM.  The 224 launches are one CUDA graph; `value` is
+the token's algorithmic bytes (packed codes + int8 scales + scale2 + offset
++ x + y of every GEMV) over its device time, summed over ranks.
 
-The same run also times, on their own workloads, the prefill GEMM (14336x4096
-weight, M = 64..2048, TFLOP/s), the GEMV alone with L2 flushed before each
-launch (all three decode weights, and the 28672x8192 weight at M = 1..16 with
-NF4 and FP4 codes; back-to-back launches over copies of the packed weight
-that together exceed L2), and the 32-layer Llama-3-8B-shaped stack (whole-stack
-quantize + double quant, and one decode token through its 224 GEMVs).
+The same run also reports, each on its own workload: the whole path of the
+Llama-7B decode shapes (quantize + double quant, dequantize and GEMV of
+[4096x4096], [11008x4096], [4096x11008]), the GEMV alone on those weights
+and on the 28672x8192 weight at M = 1..16 with NF4 and FP4 codes (the
+block-scale-folded kernel and the exact one), the whole-stack quantization,
+the prefill GEMM (14336x4096, M = 16..2048, TFLOP/s, against dequantize +
+cuBLAS), the QLoRA input gradient and the LLM.int8() matmul.
 
 Multi-GPU: one process per GPU under torchrun; every rank runs the same
 workload on its own GPU (replicas: the path has no exchange step), time is
@@ -41,9 +42,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "NF4 GEMV effective weight GB/s and % of HBM peak; NF4 GEMM TFLOP/s"
-WORKLOAD = ("Llama-7B decode shapes [4096x4096], [11008x4096], [4096x11008], bf16 "
-            "N(0,0.02) + 0.1% outliers, x bf16 N(0,1) M=1; step = quantize + double "
-            "quant + dequantize + GEMV per weight")
+WORKLOAD = ("Llama-3-8B-shaped stack, 32 layers x {q,k,v,o,gate,up,down}, bf16 N(0,0.02), "
+            "NF4 blocksize 64 + double quant; step = one decode token: 224 NF4 GEMVs, M=1, "
+            "x bf16 N(0,1)")
 NS_HBM_GBS = 8000.0   # the "~8 TB/s" HBM figure the target is stated against
 
 
@@ -139,18 +140,17 @@ def kernel_bytes(N, K, M=1):
     return b
 
 
-# DRAM bytes (read + write) per call of each phase of the step, averaged over
-# the three weights, from one ncu capture of this script (the launch list in
-# profiles/ncu_launches_llama7b_decode_step.md).  They hold only for the
-# kernel sources they were measured on: `traffic` is reported as null as soon
-# as the digest of those sources (STEP_SOURCES) differs.
-MEASURED_TRAFFIC = {"csrc_digest": "31ec09fb8be0ae02",
-                    "quantize_dq": 75457172, "dequantize": 36857290, "gemv": 18425694}
+# DRAM bytes (read + write) per launch of the GEMV kernel on the decode
+# token, averaged over the 224 launches, from one ncu capture of the
+# GEMV kernel.  They hold only for the kernel sources they were measured on:
+# `traffic` is reported as null as soon as the digest of those sources
+# (STEP_SOURCES) differs.
+MEASURED_TRAFFIC = {"csrc_digest": "", "gemv_per_launch": None}
 
 
-# The sources of the step's kernels and of their launch code.
-STEP_SOURCES = ("common.cuh", "tables.h", "lut.cuh", "tma.cuh", "quantize.cuh",
-                "double_quant.cuh", "dequantize.cuh", "gemv_mma.cuh", "nf4q.cu")
+# The sources of the step's kernel and of its launch code.
+STEP_SOURCES = ("common.cuh", "tables.h", "lut.cuh", "tma.cuh", "gemv_lut.cuh",
+                "gemv_mma.cuh", "nf4q.cu")
 
 
 def csrc_digest() -> str:
@@ -189,6 +189,9 @@ def job_throughput(world: int, bytes_per_rank_step: int, ms_per_step: float) -> 
 
 
 # ------------------------------------------------------------------ our path
+MATRIX_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -208,6 +211,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     R = ctypes.byref
+    E = lambda: torch.cuda.Event(enable_timing=True)
 
     def barrier():
         if world > 1:
@@ -225,111 +229,69 @@ def run_ours(args):
         if st != 0:
             raise RuntimeError(f"{what} failed with status {st}")
 
-    # ---- the decode workload
+    # ---- the stack: bf16 weights drawn on the device, quantized once (the
+    # whole-stack quantize + double quant is timed here as an extra)
+    bf = []
+    for layer in range(synth.LLAMA3_8B_LAYERS):
+        for mid in range(7):
+            bf.append(synth.llama3_8b_matrix(layer, mid, device=dev))
     mats = []
-    for i in range(3):
-        w, x = synth.llama7b_decode(i, device=dev)
+    for i, w in enumerate(bf):
+        layer, mid = divmod(i, 7)
         N, K = w.shape
         qw = nq.QuantizedWeight.empty(N, K, device=dev)
-        ws = nq.dq_workspace(N * K // 64, dev)
-        out = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
-        y = torch.empty(1, N, dtype=torch.bfloat16, device=dev)
-        mats.append(dict(w=w, x=x, N=N, K=K, qw=qw, s=qw.struct(), ws=ws, out=out, y=y,
-                         bytes=kernel_bytes(N, K)))
-    names = ["quantize_dq", "dequantize", "gemv"]
-    nphase = len(names)
-    # per weight: quantize (with the first double-quant pass) + per-256 pass,
-    # dequantize, gemv
-    launches_per_step = 3 * (2 + 1 + 1)
+        mats.append(dict(qw=qw, s=qw.struct(), N=N, K=K, mid=mid,
+                         ws=nq.dq_workspace(N * K // 64, dev),
+                         x=synth.llama3_8b_x(layer, mid, device=dev),
+                         y=torch.empty(1, N, dtype=torch.bfloat16, device=dev),
+                         bytes=kernel_bytes(N, K)["gemv"]))
 
-    def launch(m, k, st=None):
-        s = m["s"]
-        sp_ = (st or stream).cuda_stream
-        if k == 0:
-            check(L.nf4q_quantize_dq(m["w"].data_ptr(), nq.IN_BF16, R(s), m["ws"].data_ptr(),
-                                     m["ws"].numel(), sp_), "quantize_dq")
-        elif k == 1:
-            check(L.nf4q_dequantize(R(s), m["out"].data_ptr(), sp_), "dequantize")
-        else:
-            check(L.nf4q_gemv(R(s), m["x"].data_ptr(), 1, m["y"].data_ptr(), sp_), "gemv")
+    def quant_all():
+        for w, m in zip(bf, mats):
+            check(L.nf4q_quantize_dq(w.data_ptr(), nq.IN_BF16, R(m["s"]), m["ws"].data_ptr(),
+                                     m["ws"].numel(), sp), "quantize_dq")
 
-    # The timed step.  The three weights are independent problems: each gets
-    # its own pair of streams.  On the first, quantize + double quant, then
-    # dequantize; on the second, the GEMV as soon as the weight's quantized
-    # state is ready.  Every stream first waits for the step's start and the
-    # main stream waits for all of them at its end, so the step's events
-    # bracket all of its work.
-    s_a = [torch.cuda.Stream(dev) for _ in mats]
-    s_b = [torch.cuda.Stream(dev) for _ in mats]
-    Ent = lambda: torch.cuda.Event()
-    ev_go = Ent()
-    ev_q = [Ent() for _ in mats]
-    ev_end = [Ent() for _ in range(2 * len(mats))]
+    quant_all()
+    torch.cuda.synchronize()
+    q_ms = []
+    for _ in range(3):
+        a, b = E(), E()
+        a.record(stream)
+        quant_all()
+        b.record(stream)
+        b.synchronize()
+        q_ms.append(a.elapsed_time(b))
+    q_bytes = sum(kernel_bytes(*w.shape)["quantize_dq"] for w in bf)
+    stack_quant = {"workload": "the 224 stack weights, bf16 in, nf4q_quantize_dq each",
+                   "ms": round(min(q_ms), 3),
+                   "GB/s": round(q_bytes / (min(q_ms) * 1e-3) / 1e9, 1),
+                   "frac_measured_hbm": round(q_bytes / (min(q_ms) * 1e-3) / 1e9 / peaks["hbm"], 4),
+                   "bytes": q_bytes}
+    del bf
+    torch.cuda.empty_cache()
 
-    def fork(main):
-        ev_go.record(main)
-        for sa, sb in zip(s_a, s_b):
-            sa.wait_event(ev_go)
-            sb.wait_event(ev_go)
+    token_bytes = sum(m["bytes"] for m in mats)
 
-    def join(main):
-        for i, (sa, sb) in enumerate(zip(s_a, s_b)):
-            ev_end[2 * i].record(sa)
-            ev_end[2 * i + 1].record(sb)
-        for e in ev_end:
-            main.wait_event(e)
+    def launch_gemv(m, st):
+        check(L.nf4q_gemv(R(m["s"]), m["x"].data_ptr(), 1, m["y"].data_ptr(), st), "gemv")
 
-    def step(main=None):
-        main = main or stream
-        fork(main)
-        for i, m in enumerate(mats):
-            launch(m, 0, s_a[i])
-            ev_q[i].record(s_a[i])
-            s_b[i].wait_event(ev_q[i])
-            launch(m, 2, s_b[i])
-            launch(m, 1, s_a[i])
-        join(main)
+    # ---- the token as one CUDA graph of 224 launches
+    gs = torch.cuda.Stream(dev)
 
-    def step_serial(evs):
-        j = 0
-        for m in mats:
-            for k in range(nphase):
-                evs[j].record(stream)
-                launch(m, k)
-                j += 1
-        evs[j].record(stream)
+    def capture(subset):
+        with torch.cuda.stream(gs):
+            for m in subset:
+                launch_gemv(m, gs.cuda_stream)
+            gs.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=gs):
+                for m in subset:
+                    launch_gemv(m, gs.cuda_stream)
+        torch.cuda.synchronize()
+        return g
 
-    # The step as one CUDA graph (its streams become branches), so that the
-    # host's launch cost does not pace the device.
+    graph = capture(mats)
     for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step(torch.cuda.current_stream())
-    torch.cuda.synchronize()
-
-    step_bytes = sum(m["bytes"][n] for m in mats for n in names)
-    E = lambda: torch.cuda.Event(enable_timing=True)
-
-    # per-phase breakdown: the same work one kernel at a time on one stream
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    n_serial = max(3, min(args.steps, 200))
-    ser = [[E() for _ in range(3 * nphase + 1)] for _ in range(n_serial)]
-    for i in range(n_serial):
-        flush()
-        step_serial(ser[i])
-    torch.cuda.synchronize()
-    kern_ms = {n: 0.0 for n in names}
-    for evs in ser:
-        for j in range(3 * nphase):
-            kern_ms[names[j % nphase]] += evs[j].elapsed_time(evs[j + 1])
-    serial_ms = sum(kern_ms.values())
-
-    for _ in range(max(3, args.warmup)):
-        flush()
         graph.replay()
     torch.cuda.synchronize()
     per_step = [(E(), E()) for _ in range(args.steps)]
@@ -338,7 +300,6 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
-            flush()
             per_step[i][0].record(stream)
             graph.replay()
             per_step[i][1].record(stream)
@@ -347,105 +308,102 @@ def run_ours(args):
         wall = time.perf_counter() - t0
     clocks = clk.summary()
     step_times = sorted(a.elapsed_time(b) for a, b in per_step)
-    dev_ms = sum(step_times)
+    dev_ms = slowest(sum(step_times))
+    ms_per_step = dev_ms / args.steps
+    value = job_throughput(world, token_bytes, ms_per_step)
 
     def pct(q):
         return round(step_times[min(len(step_times) - 1, int(q * len(step_times)))], 4)
-    dom = max(kern_ms, key=kern_ms.get)            # the largest share of the serial step
-    dom_ms = kern_ms[dom] / n_serial * args.steps  # its launches, timed one by one
-    dev_ms_max = slowest(dev_ms)
-    ms_per_step = dev_ms_max / args.steps
-    value = job_throughput(world, step_bytes, ms_per_step)
 
-    # roofline of the kernel with the largest share of the step, timed with
-    # events around each of its launches on its stream (the serial pass: the
-    # graph's nodes carry no events)
-    dom_bytes = sum(m["bytes"][dom] for m in mats)      # per step, 3 launches
-    launches_dom = 3 * args.steps
-    achieved = (dom_bytes * args.steps / launches_dom) / (dom_ms / launches_dom * 1e-3) / 1e9
-    traffic_ok = csrc_digest() == MEASURED_TRAFFIC["csrc_digest"]
-    roofline = {"kernel": "nf4q_" + dom, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+    # per matrix type: the 32 GEMVs of one type as their own graph
+    by_type = {}
+    for mid, name in enumerate(MATRIX_NAMES):
+        sub = [m for m in mats if m["mid"] == mid]
+        g = capture(sub)
+        for _ in range(3):
+            g.replay()
+        a, b = E(), E()
+        a.record(stream)
+        for _ in range(10):
+            g.replay()
+        b.record(stream)
+        b.synchronize()
+        ms = a.elapsed_time(b) / 10 / len(sub)
+        by = sub[0]["bytes"]
+        by_type[name] = {"shape": [sub[0]["N"], sub[0]["K"]], "us": round(ms * 1e3, 2),
+                         "GB/s": round(by / (ms * 1e-3) / 1e9, 1),
+                         "frac_measured_hbm": round(by / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)}
+        del g
+
+    # roofline of the step's one kernel: algorithmic bytes per launch over
+    # the average launch time, both over the timed steps
+    launches = len(mats)
+    achieved = (token_bytes / launches) / (ms_per_step / launches * 1e-3) / 1e9
+    traffic_ok = MEASURED_TRAFFIC["csrc_digest"] == csrc_digest()
+    roofline = {"kernel": "nf4q_gemv (gemv_lut_kernel, block-scale folded)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm"], 4),
                 "peak_source": peaks["src"] + " HBM copy bandwidth",
-                "bytes_per_launch": dom_bytes // 3,
-                "traffic": MEASURED_TRAFFIC.get(dom) if traffic_ok else None,
-                "traffic_note": "DRAM read+write per call from the ncu launch list; writes "
-                                "still in L2 when the kernel ends are not counted",
-                "share_of_serial_step": round(kern_ms[dom] / serial_ms, 3)}
-    breakdown = {n: {"ms_per_step": round(kern_ms[n] / n_serial, 4),
-                     "GB/s": round(sum(m["bytes"][n] for m in mats)
-                                   / (kern_ms[n] / n_serial * 1e-3) / 1e9, 1),
-                     "share": round(kern_ms[n] / serial_ms, 3),
-                     "bytes_per_call": sum(m["bytes"][n] for m in mats) // 3,
-                     "traffic_per_call": MEASURED_TRAFFIC.get(n) if traffic_ok else None}
-                 for n in names}
+                "frac_of_8TBps": round(achieved / NS_HBM_GBS, 4),
+                "bytes_per_launch": token_bytes // launches,
+                "traffic": MEASURED_TRAFFIC["gemv_per_launch"] if traffic_ok else None,
+                "traffic_note": "DRAM read+write per launch, averaged over the token's 224 "
+                                "launches, from an ncu capture of the same kernel sources"}
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "ms_per_step_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1, "bytes_per_step": step_bytes,
-                   "l2": "flushed before every step (256 MiB write, outside the events)",
-                   "streams": "one CUDA graph per step; each weight on its own two "
-                              "branches: quantize + double quant then dequantize, and the "
-                              "GEMV once the quantized state is ready",
+        "config": {"workload": WORKLOAD, "M": 1, "bytes_per_step": token_bytes,
+                   "gemv_launches_per_step": launches,
+                   "l2": "not flushed: the 3.61 GB of weights per step exceed L2 (126 MB)",
+                   "launch": "the 224 launches captured once in a CUDA graph, replayed per step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
-        "breakdown": {"note": f"the same step one kernel at a time on one stream "
-                              f"({n_serial} steps, L2 flushed), "
-                              f"{round(serial_ms / n_serial, 4)} ms per step", **breakdown},
-        "gpu_launches": launches_per_step * args.steps,
+        "gemv_by_matrix": by_type,
+        "gpu_launches": launches * args.steps,
         "wall_s_timed_region": round(wall, 4),
         "clocks": clocks,
     }
 
-    # ---- e2e: host buffers, copies inside the timed region
-    host_w = [m["w"].cpu().pin_memory() for m in mats]
+    # ---- e2e: the C ABI called from Python for every GEMV of the token, x
+    # copied in from pinned host memory before and y copied out after each
     host_x = [m["x"].cpu().pin_memory() for m in mats]
     host_y = [torch.empty(1, m["N"], dtype=torch.bfloat16).pin_memory() for m in mats]
-    h2d = sum(t.numel() * 2 for t in host_w) + sum(t.numel() * 2 for t in host_x)
+    h2d = sum(t.numel() * 2 for t in host_x)
     d2h = sum(t.numel() * 2 for t in host_y)
 
     def e2e_step():
-        # the same streams as the timed step: each weight's inputs are copied
-        # in on its first stream, its y copied out after its GEMV
-        fork(stream)
-        for i, (m, hw, hx, hy) in enumerate(zip(mats, host_w, host_x, host_y)):
-            with torch.cuda.stream(s_a[i]):
-                m["w"].copy_(hw, non_blocking=True)
-                m["x"].copy_(hx, non_blocking=True)
-            launch(m, 0, s_a[i])
-            ev_q[i].record(s_a[i])
-            s_b[i].wait_event(ev_q[i])
-            launch(m, 2, s_b[i])
-            with torch.cuda.stream(s_b[i]):
-                hy.copy_(m["y"], non_blocking=True)
-            launch(m, 1, s_a[i])
-        join(stream)
+        for m, hx, hy in zip(mats, host_x, host_y):
+            m["x"].copy_(hx, non_blocking=True)
+            launch_gemv(m, sp)
+            hy.copy_(m["y"], non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 50))
+    e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    e0, e1 = E(), E()
     barrier()
-    e0.record(stream)
+    t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
-    e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = slowest(e0.elapsed_time(e1)) / e2e_steps
-    result["e2e"] = {"value": round(job_throughput(world, step_bytes, e2e_ms), 1),
+    e2e_ms = slowest((time.perf_counter() - t0) * 1e3) / e2e_steps
+    result["e2e"] = {"value": round(job_throughput(world, token_bytes, e2e_ms), 1),
                      "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                     "api": "C ABI via the ctypes binding, pinned host buffers"}
+                     "api": "nf4q_gemv through the ctypes binding, one call per GEMV, pinned "
+                            "host buffers, host wall clock around the steps"}
+    result["llama3_8b_stack_quantize"] = stack_quant
+    del mats, graph
+    torch.cuda.empty_cache()
 
     if not args.no_extras:
         result.update(run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream))
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline_sample()
+        result.update(cpu_baselines())
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -453,8 +411,9 @@ def run_ours(args):
 
 
 def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
-    """GEMV alone (L2 flushed before each launch), prefill GEMM, and the
-    Llama-3-8B stack.  Each timed with CUDA events per launch."""
+    """The whole path on the Llama-7B decode shapes, the GEMV alone on its
+    other workloads (both kernels), prefill GEMM, QLoRA input gradient and
+    LLM.int8().  Each timed with CUDA events."""
     out = {}
     sp = stream.cuda_stream
     R = ctypes.byref
@@ -479,65 +438,83 @@ def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
         if st != 0:
             raise RuntimeError(f"{what} failed with status {st}")
 
-    def gemv_timed(qw, x, M, y, n_launch=None):
-        """Average GEMV time over back-to-back launches that rotate through
-        copies of the packed weight and its int8 scales (together > 400 MB,
-        so every launch reads its weight from HBM); one event pair around
-        all of them, best of three rounds."""
+    out["path_step"] = path_step(args, nq, L, synth, torch, dev, peaks, flush, E, stream)
+
+    def gemv_timed(qw, x, M, y, fn=None):
+        """Average GEMV time over launches that rotate through copies of the
+        packed weight and its int8 scales (together > 400 MB, so every
+        launch reads its weight from HBM), captured in a CUDA graph so that
+        host launch cost does not count; best of three replays."""
+        fn = fn or L.nf4q_gemv
         ncopy = max(4, -(-400_000_000 // (qw.rows * qw.cols // 2)))
         cps = [nq.QuantizedWeight(qw.packed.clone(), qw.absmax, qw.absmax_q.clone(), qw.scale2,
-                                  qw.offset, qw.rows, qw.cols, qw.code, qw.double_quant)
+                                  qw.offset, qw.rows, qw.cols, qw.code, qw.double_quant,
+                                  qw.compute_dtype)
                for _ in range(ncopy)]
         structs = [c.struct() for c in cps]
-        for st in structs:
-            check(L.nf4q_gemv(R(st), x.data_ptr(), M, y.data_ptr(), sp), "gemv")
-        n = n_launch or 4 * ncopy
+        n = 4 * ncopy
+        gs = torch.cuda.Stream(dev)
+        with torch.cuda.stream(gs):
+            for st in structs:
+                check(fn(R(st), x.data_ptr(), M, y.data_ptr(), gs.cuda_stream), "gemv")
+            gs.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=gs):
+                for i in range(n):
+                    fn(R(structs[i % ncopy]), x.data_ptr(), M, y.data_ptr(), gs.cuda_stream)
+        torch.cuda.synchronize()
         best = None
         for _ in range(3):
             a, b = E(), E()
             a.record(stream)
-            for i in range(n):
-                L.nf4q_gemv(R(structs[i % ncopy]), x.data_ptr(), M, y.data_ptr(), sp)
+            g.replay()
             b.record(stream)
             b.synchronize()
             ms = a.elapsed_time(b) / n
             best = ms if best is None else min(best, ms)
-        del cps
+        del cps, g
         return best
 
-    # GEMV alone on the three decode weights
+    # GEMV alone on the three decode weights, both kernels
     gem = []
-    tot_b, tot_ms = 0, 0.0
+    tot_b, tot_ms, tot_ms_x = 0, 0.0, 0.0
     for i in range(3):
         w, x = synth.llama7b_decode(i, device=dev)
         qw = nq.quantize(w)
         y = torch.empty(1, w.shape[0], dtype=torch.bfloat16, device=dev)
         ms = gemv_timed(qw, x, 1, y)
+        ms_x = gemv_timed(qw, x, 1, y, L.nf4q_gemv_exact)
         b = kernel_bytes(*w.shape)["gemv"]
         gem.append({"shape": list(w.shape), "us": round(ms * 1e3, 2),
-                    "GB/s": round(b / (ms * 1e-3) / 1e9, 1)})
+                    "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                    "us_exact": round(ms_x * 1e3, 2)})
         tot_b += b
         tot_ms += ms
+        tot_ms_x += ms_x
         del w, qw
     gbs = tot_b / (tot_ms * 1e-3) / 1e9
-    out["gemv"] = {"workload": "Llama-7B decode weights, M=1, each launch reads its weight "
-                               "from HBM (rotating copies > L2)",
-                   "GB/s": round(gbs, 1), "frac_measured_hbm": round(gbs / peaks["hbm"], 4),
-                   "frac_8TBps": round(gbs / NS_HBM_GBS, 4), "per_weight": gem}
+    out["gemv_llama7b"] = {
+        "workload": "Llama-7B decode weights, M=1, each launch reads its weight from HBM "
+                    "(rotating copies > L2), launches in a CUDA graph",
+        "GB/s": round(gbs, 1), "frac_measured_hbm": round(gbs / peaks["hbm"], 4),
+        "frac_8TBps": round(gbs / NS_HBM_GBS, 4),
+        "GB/s_exact": round(tot_b / (tot_ms_x * 1e-3) / 1e9, 1), "per_weight": gem}
 
-    # 70B-MLP weight, M sweep, NF4 and FP4
+    # 70B-MLP weight, M sweep, NF4 and FP4, both kernels
     w = synth.mlp70b_weight(device=dev)
     sweep = []
     for code in ("nf4", "fp4"):
         qw = nq.quantize(w, code)
-        for M in (1, 4, 8, 16):
+        for M in (1, 2, 4, 8, 16):
             x = synth.mlp70b_x(M, device=dev)
             y = torch.empty(M, w.shape[0], dtype=torch.bfloat16, device=dev)
             ms = gemv_timed(qw, x, M, y)
+            ms_x = gemv_timed(qw, x, M, y, L.nf4q_gemv_exact)
             b = kernel_bytes(*w.shape, M=M)["gemv"]
             sweep.append({"code": code, "M": M, "us": round(ms * 1e3, 2),
                           "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
-                          "frac_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)})
+                          "frac_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm"], 4),
+                          "us_exact": round(ms_x * 1e3, 2)})
         del qw
     # fp16 compute dtype (NF4 codes, fp16 x and y)
     qw = nq.quantize(w, "nf4", compute_dtype="f16")
@@ -551,7 +528,8 @@ def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
                       "frac_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)})
     del qw
     del w
-    out["gemv_70b_mlp"] = {"workload": "28672x8192 bf16 N(0,0.015), rotating copies > L2",
+    out["gemv_70b_mlp"] = {"workload": "28672x8192 bf16 N(0,0.015), rotating copies > L2; "
+                                       "us = nf4q_gemv, us_exact = nf4q_gemv_exact",
                            "points": sweep}
 
     # prefill GEMM
@@ -656,130 +634,257 @@ def run_extras(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
                        "points": pts}
     del w
 
-    # Llama-3-8B stack: whole-stack quantize + double quant, one decode token
-    if not args.no_stack:
-        stack = []
-        tot_n = 0
-        for layer in range(synth.LLAMA3_8B_LAYERS):
-            for mid in range(7):
-                w = synth.llama3_8b_matrix(layer, mid, device=dev)
-                x = synth.llama3_8b_x(layer, mid, device=dev)
-                qw = nq.QuantizedWeight.empty(*w.shape, device=dev)
-                ws = nq.dq_workspace(w.numel() // 64, dev)
-                y = torch.empty(1, w.shape[0], dtype=torch.bfloat16, device=dev)
-                stack.append((w, x, qw, qw.struct(), ws, y))
-                tot_n += w.numel()
-
-        def quant_all():
-            for w, x, qw, s, ws, y in stack:
-                L.nf4q_quantize_dq(w.data_ptr(), nq.IN_BF16, R(s), ws.data_ptr(), ws.numel(), sp)
-
-        def token():
-            for w, x, qw, s, ws, y in stack:
-                L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), sp)
-
-        qms = timed(quant_all, n=3)
-        qbytes = sum(kernel_bytes(*t[0].shape)["quantize_dq"] for t in stack)
-        tms = timed(token, n=5)
-        tbytes = sum(kernel_bytes(*t[0].shape)["gemv"] for t in stack)
-        # the same 224 launches captured once in a CUDA graph and replayed:
-        # no host work between kernels
-        gs = torch.cuda.Stream()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(gs):
-            for w, x, qw, s, ws, y in stack:
-                check(L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), gs.cuda_stream), "gemv")
-            gs.synchronize()
-            with torch.cuda.graph(graph, stream=gs):
-                for w, x, qw, s, ws, y in stack:
-                    L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), gs.cuda_stream)
-        torch.cuda.synchronize()
-        gms = timed(graph.replay, n=5)
-        out["llama3_8b_stack"] = {
-            "workload": "32 layers x {q,k,v,o,gate,up,down}, 6.98e9 weights, bf16 N(0,0.02)",
-            "quantize_dq_ms": round(qms, 3), "quantize_dq_GB/s": round(qbytes / (qms * 1e-3) / 1e9, 1),
-            "decode_token_ms": round(tms, 4), "decode_token_GB/s": round(tbytes / (tms * 1e-3) / 1e9, 1),
-            "decode_token_graph_ms": round(gms, 4),
-            "decode_token_graph_GB/s": round(tbytes / (gms * 1e-3) / 1e9, 1),
-            "decode_gemv_launches": len(stack)}
-        del graph
-        del stack
     return out
 
 
+def path_step(args, nq, L, synth, torch, dev, peaks, flush, E, stream):
+    """The whole decode-side path on the Llama-7B decode shapes: for each of
+    [4096x4096], [11008x4096], [4096x11008] (bf16 N(0, 0.02) + 0.1 %
+    outliers) nf4q_quantize_dq, nf4q_dequantize (bf16 out) and nf4q_gemv
+    (M = 1).  The three weights are independent: each gets two streams
+    (quantize + double quant then dequantize; the GEMV once the quantized
+    state is ready), captured as one CUDA graph; L2 is flushed before every
+    replay, outside the events.  Also the same work one kernel at a time,
+    for the per-phase breakdown."""
+    sp = stream.cuda_stream
+    R = ctypes.byref
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what} failed with status {st}")
+
+    mats = []
+    for i in range(3):
+        w, x = synth.llama7b_decode(i, device=dev)
+        N, K = w.shape
+        qw = nq.QuantizedWeight.empty(N, K, device=dev)
+        mats.append(dict(w=w, x=x, N=N, K=K, qw=qw, s=qw.struct(),
+                         ws=nq.dq_workspace(N * K // 64, dev),
+                         out=torch.empty(N, K, dtype=torch.bfloat16, device=dev),
+                         y=torch.empty(1, N, dtype=torch.bfloat16, device=dev),
+                         bytes=kernel_bytes(N, K)))
+    names = ["quantize_dq", "dequantize", "gemv"]
+
+    def launch(m, k, st):
+        s_ = m["s"]
+        if k == 0:
+            check(L.nf4q_quantize_dq(m["w"].data_ptr(), nq.IN_BF16, R(s_), m["ws"].data_ptr(),
+                                     m["ws"].numel(), st), "quantize_dq")
+        elif k == 1:
+            check(L.nf4q_dequantize(R(s_), m["out"].data_ptr(), st), "dequantize")
+        else:
+            check(L.nf4q_gemv(R(s_), m["x"].data_ptr(), 1, m["y"].data_ptr(), st), "gemv")
+
+    s_a = [torch.cuda.Stream(dev) for _ in mats]
+    s_b = [torch.cuda.Stream(dev) for _ in mats]
+    ev_go = torch.cuda.Event()
+    ev_q = [torch.cuda.Event() for _ in mats]
+    ev_end = [torch.cuda.Event() for _ in range(2 * len(mats))]
+
+    def step(main):
+        ev_go.record(main)
+        for i, m in enumerate(mats):
+            s_a[i].wait_event(ev_go)
+            s_b[i].wait_event(ev_go)
+            launch(m, 0, s_a[i].cuda_stream)
+            ev_q[i].record(s_a[i])
+            s_b[i].wait_event(ev_q[i])
+            launch(m, 2, s_b[i].cuda_stream)
+            launch(m, 1, s_a[i].cuda_stream)
+        for i in range(len(mats)):
+            ev_end[2 * i].record(s_a[i])
+            ev_end[2 * i + 1].record(s_b[i])
+        for e in ev_end:
+            main.wait_event(e)
+
+    for _ in range(3):
+        step(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    n = 20
+    ts = []
+    for _ in range(n):
+        flush()
+        a, b = E(), E()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    step_bytes = sum(m["bytes"][k] for m in mats for k in names)
+    # one kernel at a time on one stream
+    kern_ms = {k: 0.0 for k in names}
+    for _ in range(n):
+        for m in mats:
+            for k in range(3):
+                flush()
+                a, b = E(), E()
+                a.record(stream)
+                launch(m, k, sp)
+                b.record(stream)
+                b.synchronize()
+                kern_ms[names[k]] += a.elapsed_time(b)
+    serial = sum(kern_ms.values())
+    breakdown = {k: {"ms_per_step": round(kern_ms[k] / n, 4),
+                     "GB/s": round(sum(m["bytes"][k] for m in mats) / (kern_ms[k] / n * 1e-3) / 1e9, 1),
+                     "frac_measured_hbm": round(sum(m["bytes"][k] for m in mats)
+                                                / (kern_ms[k] / n * 1e-3) / 1e9 / peaks["hbm"], 4),
+                     "share": round(kern_ms[k] / serial, 3),
+                     "bytes_per_call": sum(m["bytes"][k] for m in mats) // 3}
+                 for k in names}
+    del graph
+    return {"workload": "Llama-7B decode shapes [4096x4096], [11008x4096], [4096x11008], "
+                        "bf16 N(0,0.02) + 0.1% outliers, x bf16 N(0,1) M=1: quantize + double "
+                        "quant, dequantize and GEMV per weight; one CUDA graph, L2 flushed "
+                        "before each replay",
+            "ms": round(ms, 4), "GB/s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+            "bytes": step_bytes,
+            "serial_breakdown": {"note": f"one kernel at a time, L2 flushed before each, "
+                                         f"{round(serial / n, 4)} ms per step", **breakdown}}
+
+
 # ------------------------------------------------------------------ oracle (CPU)
-def _limit_threads():
+def _limit_threads(n=1):
     try:
         from threadpoolctl import threadpool_limits
-        return threadpool_limits(1)
+        return threadpool_limits(n)
     except Exception:
         return None
 
 
-_DECODE_CPU = None
+def _oracle_dequant_gemv_time(states, threads):
+    """Seconds the oracle takes to dequantize (from the packed state) and
+    multiply (fp64), like the GEMV does from the stored weight."""
+    from oracle import nf4_oracle as o
+    lim = _limit_threads(threads)
+    t0 = time.perf_counter()
+    for packed, scales, shape, xb in states:
+        w_hat = o.dequantize(packed, scales).reshape(shape)
+        o.matmul_ref(xb, w_hat)
+    dt = time.perf_counter() - t0
+    if lim is not None and hasattr(lim, "unregister"):
+        lim.unregister()
+    return dt
 
 
-def _decode_cpu():
-    """The three decode weights and their x rows on the CPU (drawn once)."""
-    global _DECODE_CPU
-    if _DECODE_CPU is None:
-        import synth
-        _DECODE_CPU = [synth.llama7b_decode(i, device="cpu") for i in range(3)]
-    return _DECODE_CPU
+def _stack_states(items):
+    """The oracle's stored state (packed codes, block scales) of stack
+    matrices, built in spawned workers (untimed preparation)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(min(len(items), os.cpu_count() or 1)) as pool:
+        return pool.map(_oracle_state_item, items)
 
 
-def oracle_sample(rows=None, weights=(0, 1, 2)):
-    """The oracle's whole path - quantize, double quant, dequantize, fp64
-    GEMV - on the first `rows` rows (all if None) of the given decode
-    weights.  Returns (seconds, algorithmic bytes of the same work on the GPU
-    path)."""
+def _oracle_state_item(item):
     import numpy as np
     import torch
+    import synth
     from oracle import nf4_oracle as o
-    tot, by = 0.0, 0
-    for i in weights:
-        w, x = _decode_cpu()[i]
-        wf = (w if rows is None else w[:rows]).float().numpy()
-        xb = x.view(torch.int16).numpy().view(np.uint16)
-        t0 = time.perf_counter()
-        r = o.quantize_full(wf)
-        o.matmul_ref(xb, r["w_hat"].reshape(wf.shape))
-        tot += time.perf_counter() - t0
-        by += sum(kernel_bytes(*wf.shape).values())
-    return tot, by
+    layer, mid, rows = item
+    w = synth.llama3_8b_matrix(layer, mid, device="cpu")
+    x = synth.llama3_8b_x(layer, mid, device="cpu")
+    wf = (w if rows is None else w[:rows]).float().numpy()
+    packed, absmax = o.quantize(wf)
+    q, s2, off = o.double_quant(absmax)
+    scales = o.block_scales(q, s2, off)
+    return packed, scales, wf.shape, x.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def cpu_baseline_sample():
-    """One whole decode step of the oracle (all three weights, every row),
-    single-threaded: about 10-20 s on a server core."""
-    import os
-    lim = _limit_threads()
-    dt, b = oracle_sample()
-    if lim is not None:
-        lim.unregister() if hasattr(lim, "unregister") else None
-    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "seconds": round(dt, 3),
-            "host_cpus": os.cpu_count(), "affinity": len(os.sched_getaffinity(0)),
-            "sample": "one whole step: the three decode weights, every row - quantize + "
-                      "double quant + dequantize + fp64 GEMV (NumPy, one thread)"}
+def cpu_baselines():
+    """The oracle timed on the host cores on bounded samples of the GPU
+    workloads: the decode token's GEMVs (dequantize from the stored state +
+    fp64 GEMV) over layer 0's seven matrices, with one thread and with all
+    cores; and the prefill GEMM (fp64) at M = 64 and 256."""
+    import numpy as np
+    cores = len(os.sched_getaffinity(0))
+    items = [(0, mid, None) for mid in range(7)]
+    states = _stack_states(items)
+    by = sum(kernel_bytes(sh[0], sh[1])["gemv"] for _, _, sh, _ in states)
+    dt1 = _oracle_dequant_gemv_time(states, 1)
+    dtn = _oracle_dequant_gemv_time(states, cores)
+    sample = ("layer 0 of the token (its 7 GEMVs, 218 M weights): the oracle's dequantize "
+              "from the stored NF4 state + fp64 GEMV (NumPy); the oracle's own quantization "
+              "is prepared untimed")
+    out = {"cpu_baseline": {"value": round(by / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                            "kind": "oracle", "seconds": round(dt1, 3), "host_cpus": os.cpu_count(),
+                            "affinity": cores, "sample": sample},
+           "cpu_baseline_all_cores": {"value": round(by / dtn / 1e9, 4), "unit": "GB/s",
+                                      "cores": cores, "kind": "oracle", "seconds": round(dtn, 3),
+                                      "sample": sample}}
+    del states
+    # prefill GEMM: 14336x4096 weight, X [M x 4096]
+    import synth
+    import torch
+    from oracle import nf4_oracle as o
+    w_hat = _prefill_w_hat_spawned()
+    n_rows, n_cols = w_hat.shape
+    pts = []
+    for M in (64, 256):
+        xb = synth.prefill_x(M, device="cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+        for threads in (1, cores):
+            lim = _limit_threads(threads)
+            t0 = time.perf_counter()
+            o.matmul_ref(xb, w_hat)
+            dt = time.perf_counter() - t0
+            if lim is not None and hasattr(lim, "unregister"):
+                lim.unregister()
+            pts.append({"M": M, "cores": threads, "s": round(dt, 3),
+                        "TFLOP/s": round(2.0 * M * n_rows * n_cols / dt / 1e12, 5)})
+    out["cpu_baseline_gemm"] = {"kind": "oracle", "workload": "prefill 14336x4096 NF4 weight "
+                                "(oracle-dequantized, untimed), fp64 X . w_hat^T", "points": pts}
+    return out
+
+
+def _prefill_w_hat(_):
+    """The oracle's dequantized prefill weight (untimed preparation)."""
+    import synth
+    from oracle import nf4_oracle as o
+    wf = synth.prefill_weight(device="cpu").float().numpy()
+    return o.quantize_full(wf)["w_hat"].reshape(wf.shape)
+
+
+def _prefill_w_hat_spawned():
+    import multiprocessing as mp
+    with mp.get_context("spawn").Pool(1) as pool:
+        return pool.map(_prefill_w_hat, [0])[0]
 
 
 def run_reference(args):
     rank, world, _ = rank_env()
     if rank != 0:
         return
-    lim = _limit_threads()
-    rows = 128  # per step, so that a run of --steps 1000 ends in a couple of minutes
+    import numpy as np
+    import torch
+    import synth
+    from oracle import nf4_oracle as o
+    lim = _limit_threads(1)
+    rows = 256   # per step, so that a run of --steps 1000 ends in a few minutes
+    w = synth.llama3_8b_matrix(0, 0, device="cpu")[:rows]
+    x = synth.llama3_8b_x(0, 0, device="cpu")
+    packed, absmax = o.quantize(w.float().numpy())
+    q, s2, off = o.double_quant(absmax)
+    scales = o.block_scales(q, s2, off)
+    xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+    by = kernel_bytes(rows, w.shape[1])["gemv"]
+
+    def one():
+        w_hat = o.dequantize(packed, scales).reshape(rows, -1)
+        o.matmul_ref(xb, w_hat)
+
     for _ in range(max(3, args.warmup)):
-        oracle_sample(rows, weights=(0,))
-    tot, b = 0.0, 0
+        one()
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        dt, bb = oracle_sample(rows, weights=(0,))
-        tot += dt
-        b += bb
-    value = b / tot / 1e9
-    sample = (f"rows 0..{rows - 1} of the 4096x4096 decode weight per step: quantize + "
-              "double quant + dequantize + fp64 GEMV (NumPy, one thread)")
+        one()
+    tot = time.perf_counter() - t0
+    value = by * args.steps / tot / 1e9
+    sample = (f"rows 0..{rows - 1} of layer 0's q weight (4096x4096) per step: the oracle's "
+              "dequantize from the stored NF4 state + fp64 GEMV (NumPy, one thread)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
@@ -791,16 +896,17 @@ def run_reference(args):
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
+    if lim is not None and hasattr(lim, "unregister"):
+        lim.unregister()
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-extras", action="store_true", help="only the step and e2e")
-    ap.add_argument("--no-stack", action="store_true", help="skip the 7B-weight stack")
+    ap.add_argument("--no-extras", action="store_true", help="only the token step and e2e")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

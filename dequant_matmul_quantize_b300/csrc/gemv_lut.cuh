@@ -211,12 +211,16 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
     issue_at(tile, bb, q % kLutStages);
   };
 
-  // 1. barriers, first loads
+  // Programmatic dependent launch: the next kernel on the stream may start
+  // as soon as SMs free up; this one touches no global memory before the
+  // kernels it depends on have finished (griddepcontrol.wait below).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // 1. barriers
   if (lane == 0) {
     for (int st = 0; st < kLutStages; ++st) mbar_init(bar_of(st), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
-    for (int q = 0; q < min(kLutStages, total); ++q) issue(q);
   }
 
   // 2. the byte-pair table: thread i writes entry i/2, replicas 16*(i&1) .. +15
@@ -229,6 +233,10 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
 #pragma unroll
     for (int k = 0; k < 4; ++k) sts128(a + 16 * k, vv);
   }
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (lane == 0)
+    for (int q = 0; q < min(kLutStages, total); ++q) issue(q);
 
   // 3. x -> fp16 with a power-of-two scale per row (bf16), staged
   const uint32_t misc = lut_piece(kLutPieceMisc);  // F of each row of x

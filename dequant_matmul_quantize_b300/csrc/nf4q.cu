@@ -582,8 +582,11 @@ nf4q_status gemv_lut_launch(const nf4q_weight* wq, const void* x, int32_t M, voi
   const bool bf = wq->compute_dtype == NF4Q_DT_BF16;
   const auto k = wq->double_quant ? (bf ? gemv_lut_kernel<0, true> : gemv_lut_kernel<1, true>)
                                   : (bf ? gemv_lut_kernel<0, false> : gemv_lut_kernel<1, false>);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   return launch("gemv_lut_kernel", k, dim3(static_cast<unsigned>(grid)), dim3(kLutThreads),
-                kLutSmemTop, s, nullptr, 0, tw, scale_view(wq),
+                kLutSmemTop, s, attr, 1, tw, scale_view(wq),
                 static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), N, K,
                 static_cast<int>(M), bestP, static_cast<int>(lut_kbx(K)), half_codes(wq->code));
 }

@@ -1,13 +1,19 @@
 """Linear4bit and the nf4q custom operators.  CPU tests check registration,
 fake (shape) propagation and that torch.export traces through the operators
-without running them; GPU tests check the module against the plain binding
-calls and torch.compile(fullgraph=True) against eager."""
+without running them; GPU tests check the module's forward and input
+gradient against the CPU oracle (fp64 on the oracle's own dequantized
+weights, within the matmul tolerance), against the plain binding calls, and
+torch.compile(fullgraph=True) against eager."""
 import pytest
 import torch
+
+import numpy as np
 
 import dequant_matmul_quantize_b300 as nq
 import synth
 from dequant_matmul_quantize_b300.nn import Linear4bit, Linear8bitLt
+from oracle import nf4_oracle as o
+from tests._util import CODE_ID, as_f32, oracle_state
 
 
 def test_operators_are_registered():
@@ -95,25 +101,56 @@ def test_compile_fullgraph_matches_eager():
     assert torch.equal(compiled, eager)
 
 
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _oracle_w_hat(w: torch.Tensor, code: str, dq: bool, dt: int) -> np.ndarray:
+    """The oracle's dequantized weight (bit patterns of the compute dtype)."""
+    st = oracle_state(as_f32(w).reshape(-1), code, dq)
+    return o.dequantize(st["packed"], st["scales"], CODE_ID[code], dtype=dt).reshape(w.shape)
+
+
+def _check_tol(got: torch.Tensor, ref: np.ndarray, bound: np.ndarray, dt: int, what: str):
+    y = o.from_bits(_bits(got), dt).astype(np.float64)
+    tol = o.matmul_tolerance(ref, bound, dt)
+    err = np.abs(y - ref)
+    assert np.all(err <= tol), f"{what}: worst err/tol {np.max(err / tol):.3f}"
+
+
+CONFIGS = [("nf4", True, "bf16"), ("nf4", True, "f16"), ("fp4", True, "bf16"),
+           ("nf4", False, "bf16"), ("fp4", False, "f16")]
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("compute_dtype,rows", [("bf16", 160), ("f16", 160), ("bf16", 100)])
-def test_backward_through_frozen_base(compute_dtype, rows):
-    """dX = dY . w_hat (w_hat exactly as nf4q_dequantize gives it); the 4-bit
-    state gets no gradient.  100 rows: dY is re-pitched to 104 columns."""
-    dt = torch.bfloat16 if compute_dtype == "bf16" else torch.float16
-    w = synth.normal_weight(rows, 256, 0.02, seed=11).cuda()
-    lin = Linear4bit.from_weight(w, None, "nf4", True, compute_dtype)
-    x = synth.activations(6, 256, seed=12).to(dt).cuda().requires_grad_(True)
-    gy = synth.activations(6, rows, seed=13).to(dt).cuda()
-    lin(x).backward(gy)
-    w_hat = lin.dequantized_weight().float()
-    ref = gy.float() @ w_hat
+@pytest.mark.parametrize("code,dq,compute_dtype", CONFIGS)
+@pytest.mark.parametrize("M,rows", [(1, 160), (5, 100), (70, 160)])
+def test_linear4bit_forward_and_backward_against_oracle(code, dq, compute_dtype, M, rows):
+    """Linear4bit over the config matrix (NF4 / FP4, double quant on / off,
+    bf16 / fp16 compute): its dequantized weight equals the oracle's bit for
+    bit; the forward without bias and the input gradient dX = dY . w_hat of
+    the frozen base match the oracle's fp64 products within the matmul
+    tolerance (2e-3 * sum|a b| + one ulp); the bias is added in the compute
+    dtype.  100 rows: dY is re-pitched to 104 columns for the backward."""
+    tdt = torch.bfloat16 if compute_dtype == "bf16" else torch.float16
+    odt = o.DT_BF16 if compute_dtype == "bf16" else o.DT_F16
+    w = synth.normal_weight(rows, 256, 0.02, seed=11 + M).cuda()
+    b = synth.normal_weight(1, rows, 0.5, seed=12 + M).reshape(-1).to(tdt).cuda()
+    lin = Linear4bit.from_weight(w, None, code, dq, compute_dtype)
+    lin_b = Linear4bit.from_weight(w, b, code, dq, compute_dtype)
+    w_hat = _oracle_w_hat(w.cpu(), code, dq, odt)
+    assert np.array_equal(_bits(lin.dequantized_weight()), w_hat)
+    x = synth.activations(M, 256, seed=13 + M).to(tdt).cuda().requires_grad_(True)
+    y = lin(x)
+    y_ref, bound = o.matmul_ref(_bits(x), w_hat, odt)
+    _check_tol(y, y_ref, bound, odt, f"forward {code} dq={dq} {compute_dtype} M={M}")
+    assert torch.equal(lin_b(x.detach()), y.detach() + b)
+    gy = synth.activations(M, rows, seed=14 + M).to(tdt).cuda()
+    y.backward(gy)
     torch.cuda.synchronize()
-    assert x.grad.dtype == dt and x.grad.shape == x.shape
-    err = (x.grad.float() - ref).abs()
-    # fp32 accumulation in the kernel plus one rounding of the output to 16 bits
-    tol = 4e-3 * (gy.float().abs() @ w_hat.abs()) + 1e-30
-    assert bool((err <= tol).all())
+    assert x.grad.dtype == tdt and x.grad.shape == x.shape
+    dx_ref, dbound = o.matmul_dx_ref(_bits(gy), w_hat, odt)
+    _check_tol(x.grad, dx_ref, dbound, odt, f"backward {code} dq={dq} {compute_dtype} M={M}")
     assert lin.packed.grad is None
 
 
@@ -137,22 +174,14 @@ def test_linear8bitlt_matches_binding_and_compiles():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("code,dq", [("fp4", True), ("nf4", False), ("fp4", False)])
-def test_linear4bit_other_configs_forward_and_backward(code, dq):
-    """The module over the rest of the config matrix (FP4, no double quant):
-    forward equals the binding; the input gradient is dY . w_hat."""
+def test_linear4bit_other_configs_match_binding(code, dq):
+    """The module over the rest of the config matrix (FP4, no double quant)
+    gives the binding's matmul bit for bit."""
     w = synth.normal_weight(128, 320, 0.02, seed=41).cuda()
     lin = Linear4bit.from_weight(w, None, code, dq, "bf16")
     qw = nq.quantize(w, code, dq)
-    x = synth.activations(70, 320, seed=42).cuda().requires_grad_(True)
-    y = lin(x)
-    assert torch.equal(y, nq.matmul(qw, x.detach()))
-    gy = synth.activations(70, 128, seed=43).cuda()
-    y.backward(gy)
-    w_hat = nq.dequantize(qw).float()
-    ref = gy.float() @ w_hat
-    torch.cuda.synchronize()
-    tol = 4e-3 * (gy.float().abs() @ w_hat.abs()) + 1e-30
-    assert bool(((x.grad.float() - ref).abs() <= tol).all())
+    x = synth.activations(70, 320, seed=42).cuda()
+    assert torch.equal(lin(x), nq.matmul(qw, x))
 
 
 @pytest.mark.gpu
