@@ -43,8 +43,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NF4 GEMV effective weight GB/s and % of HBM peak; NF4 GEMM TFLOP/s"
 WORKLOAD = ("Llama-3-8B-shaped stack, 32 layers x {q,k,v,o,gate,up,down}, bf16 N(0,0.02), "
-            "NF4 blocksize 64 + double quant; step = one decode token: 224 NF4 GEMVs, M=1, "
-            "x bf16 N(0,1)")
+            "NF4 blocksize 64 + double quant; step = one decode token: 224 NF4 GEMVs in 128 "
+            "launches (q/k/v and gate/up share their x), M=1, x bf16 N(0,1)")
 NS_HBM_GBS = 8000.0   # the "~8 TB/s" HBM figure the target is stated against
 
 
@@ -189,7 +189,8 @@ def job_throughput(world: int, bytes_per_rank_step: int, ms_per_step: float) -> 
 
 
 # ------------------------------------------------------------------ our path
-MATRIX_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+# the launches of one layer: (name, matrix ids of LLAMA3_8B_LAYER sharing x)
+GROUPS = (("qkv", (0, 1, 2)), ("o", (3,)), ("gate_up", (4, 5)), ("down", (6,)))
 
 
 def run_ours(args):
@@ -237,14 +238,11 @@ def run_ours(args):
             bf.append(synth.llama3_8b_matrix(layer, mid, device=dev))
     mats = []
     for i, w in enumerate(bf):
-        layer, mid = divmod(i, 7)
         N, K = w.shape
         qw = nq.QuantizedWeight.empty(N, K, device=dev)
-        mats.append(dict(qw=qw, s=qw.struct(), N=N, K=K, mid=mid,
+        mats.append(dict(qw=qw, s=qw.struct(), N=N, K=K, mid=i % 7, layer=i // 7,
                          ws=nq.dq_workspace(N * K // 64, dev),
-                         x=synth.llama3_8b_x(layer, mid, device=dev),
-                         y=torch.empty(1, N, dtype=torch.bfloat16, device=dev),
-                         bytes=kernel_bytes(N, K)["gemv"]))
+                         y=torch.empty(1, N, dtype=torch.bfloat16, device=dev)))
 
     def quant_all():
         for w, m in zip(bf, mats):
@@ -270,27 +268,47 @@ def run_ours(args):
     del bf
     torch.cuda.empty_cache()
 
-    token_bytes = sum(m["bytes"] for m in mats)
+    # the token's launches: per layer q/k/v (one x), o, gate/up (one x) and
+    # down, the groups through nf4q_gemv_multi
+    groups = []
+    for layer in range(synth.LLAMA3_8B_LAYERS):
+        for name, mids in GROUPS:
+            ms_ = [mats[layer * 7 + mid] for mid in mids]
+            x = synth.llama3_8b_x(layer, mids[0], device=dev)
+            grp = dict(name=name, mats=ms_, x=x, K=ms_[0]["K"],
+                       bytes=sum(nbytes_state(m["N"] * m["K"]) + 2 * m["N"] for m in ms_)
+                       + 2 * ms_[0]["K"])
+            if len(ms_) > 1:
+                grp["wp"] = (ctypes.POINTER(nq.NF4QWeight) * len(ms_))(
+                    *[ctypes.pointer(m["s"]) for m in ms_])
+                grp["yp"] = (ctypes.c_void_p * len(ms_))(*[m["y"].data_ptr() for m in ms_])
+            groups.append(grp)
+    token_bytes = sum(g_["bytes"] for g_ in groups)
 
-    def launch_gemv(m, st):
-        check(L.nf4q_gemv(R(m["s"]), m["x"].data_ptr(), 1, m["y"].data_ptr(), st), "gemv")
+    def launch_group(g_, st):
+        if len(g_["mats"]) == 1:
+            m = g_["mats"][0]
+            check(L.nf4q_gemv(R(m["s"]), g_["x"].data_ptr(), 1, m["y"].data_ptr(), st), "gemv")
+        else:
+            check(L.nf4q_gemv_multi(g_["wp"], len(g_["mats"]), g_["x"].data_ptr(), 1, g_["yp"],
+                                    st), "gemv_multi")
 
-    # ---- the token as one CUDA graph of 224 launches
+    # ---- the token as one CUDA graph of its 128 launches
     gs = torch.cuda.Stream(dev)
 
     def capture(subset):
         with torch.cuda.stream(gs):
-            for m in subset:
-                launch_gemv(m, gs.cuda_stream)
+            for g_ in subset:
+                launch_group(g_, gs.cuda_stream)
             gs.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=gs):
-                for m in subset:
-                    launch_gemv(m, gs.cuda_stream)
+                for g_ in subset:
+                    launch_group(g_, gs.cuda_stream)
         torch.cuda.synchronize()
         return g
 
-    graph = capture(mats)
+    graph = capture(groups)
     for _ in range(max(3, args.warmup)):
         graph.replay()
     torch.cuda.synchronize()
@@ -315,10 +333,10 @@ def run_ours(args):
     def pct(q):
         return round(step_times[min(len(step_times) - 1, int(q * len(step_times)))], 4)
 
-    # per matrix type: the 32 GEMVs of one type as their own graph
+    # per group kind: the 32 launches of one kind as their own graph
     by_type = {}
-    for mid, name in enumerate(MATRIX_NAMES):
-        sub = [m for m in mats if m["mid"] == mid]
+    for name, mids in GROUPS:
+        sub = [g_ for g_ in groups if g_["name"] == name]
         g = capture(sub)
         for _ in range(3):
             g.replay()
@@ -330,14 +348,14 @@ def run_ours(args):
         b.synchronize()
         ms = a.elapsed_time(b) / 10 / len(sub)
         by = sub[0]["bytes"]
-        by_type[name] = {"shape": [sub[0]["N"], sub[0]["K"]], "us": round(ms * 1e3, 2),
-                         "GB/s": round(by / (ms * 1e-3) / 1e9, 1),
+        by_type[name] = {"shapes": [[m["N"], m["K"]] for m in sub[0]["mats"]],
+                         "us": round(ms * 1e3, 2), "GB/s": round(by / (ms * 1e-3) / 1e9, 1),
                          "frac_measured_hbm": round(by / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)}
         del g
 
     # roofline of the step's one kernel: algorithmic bytes per launch over
     # the average launch time, both over the timed steps
-    launches = len(mats)
+    launches = len(groups)
     achieved = (token_bytes / launches) / (ms_per_step / launches * 1e-3) / 1e9
     traffic_ok = MEASURED_TRAFFIC["csrc_digest"] == csrc_digest()
     roofline = {"kernel": "nf4q_gemv (gemv_lut_kernel, block-scale folded)", "bound": "hbm",
@@ -347,7 +365,7 @@ def run_ours(args):
                 "frac_of_8TBps": round(achieved / NS_HBM_GBS, 4),
                 "bytes_per_launch": token_bytes // launches,
                 "traffic": MEASURED_TRAFFIC["gemv_per_launch"] if traffic_ok else None,
-                "traffic_note": "DRAM read+write per launch, averaged over the token's 224 "
+                "traffic_note": "DRAM read+write per launch, averaged over the token's "
                                 "launches, from an ncu capture of the same kernel sources"}
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -357,28 +375,33 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "bytes_per_step": token_bytes,
                    "gemv_launches_per_step": launches,
+                   "groups": "per layer: q/k/v sharing one x (nf4q_gemv_multi), o, gate/up "
+                             "sharing one x (nf4q_gemv_multi), down",
                    "l2": "not flushed: the 3.61 GB of weights per step exceed L2 (126 MB)",
-                   "launch": "the 224 launches captured once in a CUDA graph, replayed per step",
+                   "launch": "the launches captured once in a CUDA graph, replayed per step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
-        "gemv_by_matrix": by_type,
+        "gemv_by_group": by_type,
         "gpu_launches": launches * args.steps,
         "wall_s_timed_region": round(wall, 4),
         "clocks": clocks,
     }
 
-    # ---- e2e: the C ABI called from Python for every GEMV of the token, x
-    # copied in from pinned host memory before and y copied out after each
-    host_x = [m["x"].cpu().pin_memory() for m in mats]
-    host_y = [torch.empty(1, m["N"], dtype=torch.bfloat16).pin_memory() for m in mats]
+    # ---- e2e: the C ABI called from Python for every launch of the token,
+    # each x copied in from pinned host memory before and its y copied out
+    # after
+    host_x = [g_["x"].cpu().pin_memory() for g_ in groups]
+    host_y = [[torch.empty(1, m["N"], dtype=torch.bfloat16).pin_memory() for m in g_["mats"]]
+              for g_ in groups]
     h2d = sum(t.numel() * 2 for t in host_x)
-    d2h = sum(t.numel() * 2 for t in host_y)
+    d2h = sum(t.numel() * 2 for hy in host_y for t in hy)
 
     def e2e_step():
-        for m, hx, hy in zip(mats, host_x, host_y):
-            m["x"].copy_(hx, non_blocking=True)
-            launch_gemv(m, sp)
-            hy.copy_(m["y"], non_blocking=True)
+        for g_, hx, hy in zip(groups, host_x, host_y):
+            g_["x"].copy_(hx, non_blocking=True)
+            launch_group(g_, sp)
+            for m, t in zip(g_["mats"], hy):
+                t.copy_(m["y"], non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
@@ -393,10 +416,10 @@ def run_ours(args):
     result["e2e"] = {"value": round(job_throughput(world, token_bytes, e2e_ms), 1),
                      "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                     "api": "nf4q_gemv through the ctypes binding, one call per GEMV, pinned "
-                            "host buffers, host wall clock around the steps"}
+                     "api": "nf4q_gemv / nf4q_gemv_multi through the ctypes binding, one call "
+                            "per launch, pinned host buffers, host wall clock around the steps"}
     result["llama3_8b_stack_quantize"] = stack_quant
-    del mats, graph
+    del mats, groups, graph
     torch.cuda.empty_cache()
 
     if not args.no_extras:

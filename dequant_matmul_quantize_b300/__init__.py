@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
         "nf4q_dequantize": (i32, [W, vp, vp]),
         "nf4q_gemv": (i32, [W, vp, i32, vp, vp]),
         "nf4q_gemv_exact": (i32, [W, vp, i32, vp, vp]),
+        "nf4q_gemv_multi": (i32, [ctypes.POINTER(W), i32, vp, i32,
+                                  ctypes.POINTER(vp), vp]),
         "nf4q_gemm": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul_dx": (i32, [W, vp, i64, i64, vp, vp]),
@@ -301,6 +303,24 @@ def gemv(qw, x, out=None, stream=None):
     """y = x . w_hat^T for 1 <= M <= 16 (decode); for M <= 8 the block scale
     is folded after an fp16 contraction with the code values (see nf4q.h)."""
     return _mm("nf4q_gemv", qw, x, out, stream)
+
+
+def gemv_multi(qws, x, outs=None, stream=None):
+    """y_i = x . w_hat_i^T for a group of 1..4 weights sharing x (same cols,
+    code, double quant and compute dtype), in one launch where possible."""
+    _require(1 <= len(qws) <= 4, "a group has 1 to 4 weights")
+    _require(x.is_cuda and x.dtype == qws[0].torch_dtype and x.is_contiguous() and x.dim() == 2,
+             "x must be a contiguous 2-D CUDA tensor of the compute dtype")
+    _require(all(q.cols == x.shape[-1] for q in qws), "x must have the weights' columns")
+    M = x.shape[0]
+    if outs is None:
+        outs = [torch.empty(M, q.rows, dtype=q.torch_dtype, device=x.device) for q in qws]
+    structs = [q.struct() for q in qws]
+    ptrs = (ctypes.POINTER(NF4QWeight) * len(qws))(*[ctypes.pointer(st) for st in structs])
+    ys = (ctypes.c_void_p * len(qws))(*[_ptr(o) for o in outs])
+    _check("nf4q_gemv_multi", lib().nf4q_gemv_multi(ptrs, len(qws), _ptr(x), M, ys,
+                                                     _stream(stream)))
+    return outs
 
 
 def gemv_exact(qw, x, out=None, stream=None):

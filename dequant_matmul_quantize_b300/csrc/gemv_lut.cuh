@@ -29,15 +29,18 @@
 // the NF4 and FP4 values, 2^-11 at most for any value).  Per term the
 // difference is at most 2^-8 + 2^-11 of |x * w_hat| for bf16 and 2^-10 for
 // fp16; it has the sign of the rounding of each w_hat and so averages out
-// over a dot product.  (The bit-faithful variant, which rebuilds w_hat exactly inside
-// the contraction, is gemv_mma.cuh.)
+// over a dot product.  (The bit-faithful variant, which rebuilds w_hat
+// exactly inside the contraction, is gemv_mma.cuh.)
 //
 // Work split.  One CTA per SM (the table takes 64 KB), 16 warps, each with
-// its own three-stage TMA ring of 16-row x 256-column boxes of packed codes
-// (2 KB, 128-byte swizzle).  A warp owns one 16-row tile at a time and one
-// of P parts of the K range; the P warps of a tile add their partial sums
-// in a fixed order in shared memory, so y is deterministic.  Tiles go to the
-// CTAs round robin.
+// its own TMA ring of boxes of 16 rows x BB 64-blocks of packed codes (BB = 8:
+// two 2 KB boxes per stage, two stages; BB = 4: one box, three stages; the
+// 128-byte swizzle).  A warp owns one 16-row tile at a time and one of P
+// parts of the K range; the P warps of a tile add their partial sums in a
+// fixed order in shared memory, so y is deterministic.  Tiles go to the CTAs
+// round robin.  One launch may cover up to four weights that share x and
+// K (a group: q, k and v of an attention block; gate and up of an MLP):
+// their tiles are numbered one after the other.
 #pragma once
 
 #include "common.cuh"
@@ -47,27 +50,53 @@ namespace nf4q {
 
 constexpr int kLutWarps = 16;
 constexpr int kLutThreads = kLutWarps * 32;
-constexpr int kLutStages = 3;                 // per warp
-constexpr uint32_t kLutBoxBytes = 16 * 128;   // 16 rows x 256 packed columns
+constexpr uint32_t kLutBoxBytes = 16 * 128;   // one TMA box: 16 rows x 256 packed columns
 constexpr uint32_t kLutTable = 0x10000;       // shared address of the table
 constexpr uint32_t kLutRing = 0x20000;        // shared address of the rings
-constexpr uint32_t kLutSmemTop = kLutRing + kLutWarps * kLutStages * kLutBoxBytes;  // 0x38000
+constexpr uint32_t kLutSmemTop = 0x38000;     // end of the layout
 constexpr uint32_t kLutMaxBase = 0x1000;      // dynamic shared memory must start below
-// Shared memory below the table available to x: [kLutMaxBase, kLutTable).
-constexpr uint32_t kLutXBytes = kLutTable - kLutMaxBase;
+constexpr uint32_t kLutRing8Low = 0x8000;     // BB = 8: the rings' last 32 KB
+// Shared memory for staged x: [kLutMaxBase, kLutTable) with BB = 4,
+// [kLutMaxBase, kLutRing8Low) with BB = 8.
+constexpr uint32_t kLutXBytes4 = kLutTable - kLutMaxBase;
+constexpr uint32_t kLutXBytes8 = kLutRing8Low - kLutMaxBase;
 constexpr int kLutMaxM = 8;
+constexpr int kLutMaxGroup = 4;
+
+template <int BB>
+struct LutCfg {
+  static constexpr int kStages = BB == 8 ? 2 : 3;
+  static constexpr uint32_t kStageBytes = (BB / 4) * kLutBoxBytes;
+  static_assert(BB == 4 || BB == 8, "4 or 8 blocks per box");
+  static_assert(kLutWarps * kStages * kStageBytes ==
+                    (BB == 8 ? (kLutSmemTop - kLutRing) + (kLutTable - kLutRing8Low)
+                             : kLutSmemTop - kLutRing),
+                "ring layout");
+};
 
 // The unused upper half of each 256-byte table row is a 128-byte "piece";
 // pieces hold the control data.
 __device__ __forceinline__ uint32_t lut_piece(int p) { return kLutTable + 256u * p + 128u; }
-constexpr int kLutPieceBars = 0;    // 16 warps x 32 B (3 stages x 8 B)  (4 pieces)
-constexpr int kLutPieceScale = 4;   // per warp 2 x 256 B          (64 pieces)
-constexpr int kLutPieceRed = 68;    // per warp 2 x 512 B          (128 pieces)
-constexpr int kLutPieceMisc = 196;  // F factors, reduction scratch (8 pieces)
+constexpr int kLutPieceBars = 0;    // per warp 32 B (up to 3 stages x 8 B)     (4 pieces)
+constexpr int kLutPieceScale = 4;   // per warp BB * 16 floats (BB / 2 pieces)  (<= 64)
+constexpr int kLutPieceRed = 68;    // per warp 2 x 512 B                       (128 pieces)
+constexpr int kLutPieceMisc = 196;  // F factors, reduction scratch             (5 pieces)
 
 // fp16 bits of the 16 code values, built on the host.
 struct __align__(16) HalfCodes {
   uint16_t h[16];
+};
+
+// The weights of one launch (1 .. 4, same K, code, double quant and compute
+// dtype): their tensor maps, scale state, outputs, rows, and the first tile
+// of each (16-row tiles numbered over the group; off[count] = all tiles).
+struct __align__(64) LutGroup {
+  CUtensorMap tmap[kLutMaxGroup];
+  ScaleView sv[kLutMaxGroup];
+  uint16_t* y[kLutMaxGroup];
+  int N[kLutMaxGroup];
+  int off[kLutMaxGroup + 1];
+  int count;
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -89,9 +118,6 @@ __device__ __forceinline__ uint4 lds128_lut(uint32_t addr) {
 }
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void sts64(uint32_t addr, float a, float b) {
-  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -159,16 +185,18 @@ __device__ __forceinline__ uint32_t lut_x_addr(uint32_t xbase, int kbx, int m, i
          static_cast<uint32_t>((byte + 16 * m) & 127);
 }
 
-// Launch: grid <= SM count, 512 threads, 0x38000 bytes of dynamic shared
-// memory (minus nothing: the layout uses absolute shared addresses and
-// checks that the dynamic area starts below kLutMaxBase).  P = parts of K
-// (1, 2, 4, 8 or 16), kbx = 64-blocks of staged x per row (a multiple of 4,
-// >= K/64).  Requires M <= 8 and M * kbx * 128 <= kLutXBytes.
-template <int DT, bool DQ>
+// Launch: grid <= SM count, 512 threads, kLutSmemTop bytes of dynamic shared
+// memory (the layout uses absolute shared addresses and checks that the
+// dynamic area starts below kLutMaxBase).  P = parts of K (1, 2, 4, 8 or 16,
+// at most the boxes of a row), kbx = 64-blocks of staged x per row (a
+// multiple of BB, >= K/64).  Requires M <= 8 and M * kbx * 128 <= the x room
+// of BB.  Launched as a programmatic dependent of the previous kernel.
+template <int DT, bool DQ, int BB>
 __global__ void __launch_bounds__(kLutThreads, 1)
-gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
-                const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int N, int K, int M,
+gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__ x, int K, int M,
                 int P, int kbx, const __grid_constant__ HalfCodes hc) {
+  using Cfg = LutCfg<BB>;
+  constexpr int NS = Cfg::kStages;
   extern __shared__ __align__(1024) uint8_t lsm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -179,36 +207,43 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
   }
   const uint32_t xbase = kLutMaxBase;
   const int KB = K / kBlock;
-  const int nbox = (KB + 3) / 4;
+  const int nbox = (KB + BB - 1) / BB;
   const int SL = kLutWarps / P;
   const int slot = warp / P, part = warp % P;
   const int pb0 = part * nbox / P, pb1 = (part + 1) * nbox / P;
   const int nmy = pb1 - pb0;
-  const int T = (N + 15) / 16;
+  const int T = G.off[G.count];
   const int tile_stride = static_cast<int>(gridDim.x) * SL;
   const int tile0 = static_cast<int>(blockIdx.x) * SL + slot;
   const int nunits = (tile0 < T && nmy > 0) ? (T - tile0 + tile_stride - 1) / tile_stride : 0;
   const int total = nunits * nmy;
+  // the weight a (group-wide) tile belongs to
+  auto mat_of = [&](int tile) {
+    int m = 0;
+#pragma unroll
+    for (int i = 1; i < kLutMaxGroup; ++i) m += (i < G.count && tile >= G.off[i]) ? 1 : 0;
+    return m;
+  };
 
   const uint32_t barw = lut_piece(kLutPieceBars + warp / 4) + 32u * (warp % 4);
   auto bar_of = [&](int st) { return barw + 8u * st; };
-  const uint32_t ring = kLutRing + static_cast<uint32_t>(warp * kLutStages) * kLutBoxBytes;
+  auto stage_addr = [&](int st) -> uint32_t {
+    const int i = warp * NS + st;
+    if (BB == 4) return kLutRing + static_cast<uint32_t>(i) * Cfg::kStageBytes;
+    return i < 24 ? kLutRing + static_cast<uint32_t>(i) * Cfg::kStageBytes
+                  : kLutRing8Low + static_cast<uint32_t>(i - 24) * Cfg::kStageBytes;
+  };
 
-  // box q of this warp's stream: (tile, box index along K)
-  auto box_coords = [&](int q, int& tile, int& bb) {
-    const int u = q / nmy;
-    tile = tile0 + u * tile_stride;
-    bb = pb0 + (q - u * nmy);
-  };
+  // stage st <- box bb (BB blocks) of tile `tile`
   auto issue_at = [&](int tile, int bb, int st) {
+    const int m = mat_of(tile);
+    const int row0 = (tile - G.off[m]) * 16;
     const uint32_t bar = bar_of(st);
-    mbar_arrive_expect_tx(bar, kLutBoxBytes);
-    tma_load_2d(ring + st * kLutBoxBytes, &tmap_w, bb * 128, tile * 16, bar);
-  };
-  auto issue = [&](int q) {
-    int tile, bb;
-    box_coords(q, tile, bb);
-    issue_at(tile, bb, q % kLutStages);
+    const uint32_t dst = stage_addr(st);
+    mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+#pragma unroll
+    for (int h = 0; h < BB / 4; ++h)
+      tma_load_2d(dst + h * kLutBoxBytes, &G.tmap[m], (bb * (BB / 4) + h) * 128, row0, bar);
   };
 
   // Programmatic dependent launch: the next kernel on the stream may start
@@ -218,7 +253,7 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
 
   // 1. barriers
   if (lane == 0) {
-    for (int st = 0; st < kLutStages; ++st) mbar_init(bar_of(st), 1);
+    for (int st = 0; st < NS; ++st) mbar_init(bar_of(st), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -235,8 +270,22 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
   }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (lane == 0)
-    for (int q = 0; q < min(kLutStages, total); ++q) issue(q);
+
+  // stream positions: consumer, scale loader (two boxes ahead), producer
+  // (NS boxes ahead, lane 0); each advances one box at a time
+  auto advance = [&](int& tile, int& bi) {
+    if (++bi == nmy) {
+      bi = 0;
+      tile += tile_stride;
+    }
+  };
+  int p_tile = tile0, p_bi = 0;
+  if (lane == 0) {
+    for (int q = 0; q < min(NS, total); ++q) {
+      issue_at(p_tile, pb0 + p_bi, q);
+      advance(p_tile, p_bi);
+    }
+  }
 
   // 3. x -> fp16 with a power-of-two scale per row (bf16), staged
   const uint32_t misc = lut_piece(kLutPieceMisc);  // F of each row of x
@@ -314,74 +363,88 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
   }
   __syncthreads();  // table and x are complete
 
-  // 4. block scales.  Lane l computes rows l & 15, blocks 2 (l >> 4) + {0, 1}
-  //    of a box and keeps them in the warp's scale slot: float (j, r) (block
-  //    j, tile row r) at index 16 j + r, indices 32.. rotated by 16 floats so
-  //    that the two half-warps store to different banks.  With M = 1 the
-  //    slot holds s * 2^F of the single row of x.
-  const float off = DQ ? __ldg(sv.offset) : 0.f;
-  // Raw scale data of one box: lane l takes tile row l & 15 and blocks
-  // 2 (l >> 4) and 2 (l >> 4) + 1 of the box.  With K / 64 even the two int8
-  // codes are one aligned 16-bit word and share their scale2 (the pair never
-  // straddles a multiple of 256); otherwise two byte loads and two scale2.
-  // The loads run two boxes ahead of their use.
-  const int srow = lane & 15, sjb = 2 * (lane >> 4);
-  const bool kb_even = (KB & 1) == 0;
+  // 4. block scales.  Lane l computes tile row l & 15 and the BB / 2 blocks
+  //    from (BB / 2) (l >> 4) of a box and keeps them in the warp's scale
+  //    slot: float (j, r) (block j, tile row r) at word 16 j + r, the half of
+  //    the slot written by lanes 16..31 rotated by 16 words so that the two
+  //    half-warps store to different banks.  With M = 1 the slot holds
+  //    s * 2^F of the single row of x.  With K / 64 a multiple of 4 the codes
+  //    of a lane's blocks are one aligned 16- or 32-bit word and share their
+  //    scale2 (they never straddle a multiple of 256); otherwise byte loads.
+  //    The loads run two boxes ahead of their use.
+  constexpr int NBL = BB / 2;
+  const int srow = lane & 15, sjb = NBL * (lane >> 4);
+  const bool kb4 = (KB & 3) == 0;
   struct Raw {
-    uint32_t q2;     // the two int8 codes (bytes 0, 1)
-    float a, b;      // scale2 of the two blocks (DQ), or their fp32 absmax
-    uint32_t okm;    // bit h: block h exists
+    uint32_t q;       // NBL int8 codes (block j in byte j)
+    float s[NBL];     // scale2 of each block (double quant) or its fp32 absmax
+    uint32_t okm;     // bit j: block j exists
+    float off;        // the weight's double-quant offset
   };
   auto scale_load = [&](int tile, int bb, Raw& r) {
-    const int row = tile * 16 + srow;
-    const int jb = bb * 4 + sjb;
-    r.q2 = 0;
-    r.a = r.b = 0.f;
-    r.okm = row < N ? (jb + 1 < KB ? 3u : (jb < KB ? 1u : 0u)) : 0u;
+    const int m = mat_of(tile);
+    const ScaleView& sv = G.sv[m];
+    const int row = (tile - G.off[m]) * 16 + srow;
+    const int jb = bb * BB + sjb;
+    r.q = 0;
+    r.off = 0.f;
+#pragma unroll
+    for (int j = 0; j < NBL; ++j) r.s[j] = 0.f;
+    r.okm = 0;
+    if (row < G.N[m]) {
+      const int nj = max(0, min(NBL, KB - jb));
+      r.okm = (1u << nj) - 1u;
+    }
     if (r.okm) {
       const int64_t b0 = static_cast<int64_t>(row) * KB + jb;
       if (DQ) {
-        if (kb_even) {
-          r.q2 = __ldg(reinterpret_cast<const uint16_t*>(sv.absmax_q + b0));
-          r.a = r.b = __ldg(sv.scale2 + (b0 >> 8));
+        r.off = __ldg(sv.offset);
+        if (kb4) {
+          if (NBL == 4)
+            r.q = __ldg(reinterpret_cast<const uint32_t*>(sv.absmax_q + b0));
+          else
+            r.q = __ldg(reinterpret_cast<const uint16_t*>(sv.absmax_q + b0));
+          const float s2 = __ldg(sv.scale2 + (b0 >> 8));
+#pragma unroll
+          for (int j = 0; j < NBL; ++j) r.s[j] = s2;
         } else {
-          r.q2 = static_cast<uint8_t>(__ldg(sv.absmax_q + b0));
-          r.a = __ldg(sv.scale2 + (b0 >> 8));
-          if (r.okm & 2u) {
-            r.q2 |= static_cast<uint32_t>(static_cast<uint8_t>(__ldg(sv.absmax_q + b0 + 1))) << 8;
-            r.b = __ldg(sv.scale2 + ((b0 + 1) >> 8));
-          }
+#pragma unroll
+          for (int j = 0; j < NBL; ++j)
+            if ((r.okm >> j) & 1u) {
+              r.q |= static_cast<uint32_t>(static_cast<uint8_t>(__ldg(sv.absmax_q + b0 + j)))
+                     << (8 * j);
+              r.s[j] = __ldg(sv.scale2 + ((b0 + j) >> 8));
+            }
         }
       } else {
-        r.a = __ldg(sv.absmax + b0);
-        if (r.okm & 2u) r.b = __ldg(sv.absmax + b0 + 1);
+#pragma unroll
+        for (int j = 0; j < NBL; ++j)
+          if ((r.okm >> j) & 1u) r.s[j] = __ldg(sv.absmax + b0 + j);
       }
     }
   };
-  auto slot_off = [](int idx) -> uint32_t {
-    return idx < 32 ? 4u * idx : 256u + 4u * ((idx + 16) & 31);
+  // word offset of float (j, r) in the slot
+  auto slot_word = [](int j, int r) -> uint32_t {
+    const int idx = 16 * j + r;
+    return static_cast<uint32_t>((idx & ~31) + (((idx & 31) + 16 * (j / NBL)) & 31));
   };
-  const uint32_t slot0 = lut_piece(kLutPieceScale + 4 * warp);
+  const uint32_t slot0 = lut_piece(kLutPieceScale + (BB / 2) * warp);
+  auto slot_addr = [&](uint32_t word) { return slot0 + 256u * (word >> 5) + 4u * (word & 31); };
   // with M = 1 the slot holds s * 2^F of row 0 of x (the same for every lane)
   const float fs =
       M != 1 ? 1.f
              : (DT == 0 ? __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(lds32(misc))) << 23)
                         : 1.f);
-  const uint32_t soff0 = slot_off(sjb * 16 + srow), soff1 = slot_off((sjb + 1) * 16 + srow);
-  auto scale_store = [&](int buf, const Raw& r) {
-    // rows past N and blocks past K get scale 0
-    float s0, s1;
-    if (DQ) {
-      s0 = __fmaf_rn(static_cast<float>(static_cast<int8_t>(r.q2 & 0xFFu)), r.a, off);
-      s1 = __fmaf_rn(static_cast<float>(static_cast<int8_t>((r.q2 >> 8) & 0xFFu)), r.b, off);
-    } else {
-      s0 = r.a;
-      s1 = r.b;
+  auto scale_store = [&](const Raw& r) {
+#pragma unroll
+    for (int j = 0; j < NBL; ++j) {
+      float sc = 0.f;  // rows past N and blocks past K get scale 0
+      if ((r.okm >> j) & 1u)
+        sc = DQ ? __fmaf_rn(static_cast<float>(static_cast<int8_t>((r.q >> (8 * j)) & 0xFFu)),
+                            r.s[j], r.off)
+                : r.s[j];
+      sts32(slot_addr(slot_word(sjb + j, srow)), __float_as_uint(sc * fs));
     }
-    s0 = (r.okm & 1u) ? s0 * fs : 0.f;
-    s1 = (r.okm & 2u) ? s1 * fs : 0.f;
-    sts32(slot0 + 512u * buf + soff0, __float_as_uint(s0));
-    sts32(slot0 + 512u * buf + soff1, __float_as_uint(s1));
   };
 
   // 5. per-lane constants.  MMA row g is tile row 2g, MMA row g + 8 is tile
@@ -398,20 +461,12 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
   // table address = [lane * 4, code byte, 0x01, 0]: the table sits at 0x10000
   const uint32_t L = kLutTable | (static_cast<uint32_t>(lane) << 2);
 
-  // stream positions: consumer, scale loader (two boxes ahead), producer
-  // (kLutStages ahead, lane 0); each advances one box at a time
-  auto advance = [&](int& tile, int& bi) {
-    if (++bi == nmy) {
-      bi = 0;
-      tile += tile_stride;
-    }
-  };
   // raw scales: box q + 1 in rA, box q + 2 in rB while box q is consumed
   Raw rA, rB;
   int s_tile = tile0, s_bi = 0;
   if (total > 0) {
     scale_load(s_tile, pb0 + s_bi, rA);
-    scale_store(0, rA);
+    scale_store(rA);
     advance(s_tile, s_bi);
   }
   if (total > 1) {
@@ -422,13 +477,11 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
     scale_load(s_tile, pb0 + s_bi, rB);
     advance(s_tile, s_bi);
   }
-  int p_tile = tile0, p_bi = 0;
-  for (int i = 0; i < min(kLutStages, total); ++i) advance(p_tile, p_bi);
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   bool dead = false;
   int waited_q = -1;  // last box whose stage wait succeeded (waits go in order)
-  int issued_n = min(kLutStages, total);
+  int issued_n = min(NS, total);
   int c_tile = tile0, c_bi = 0, u = 0;
   int st = 0;
   uint32_t ph = 0;
@@ -440,14 +493,14 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
       if (!ok) dead = true;
       else waited_q = q;
     }
-    const uint32_t stage = ring + st * kLutBoxBytes;
+    const uint32_t stage = stage_addr(st);
     const uint32_t w0 = stage + SB0, w1 = stage + SB1;
-    const uint32_t xbox = xrow + static_cast<uint32_t>((pb0 + c_bi) * 512);
-    const uint32_t sl = slot0 + 512u * (q & 1) + 8u * g;
+    const uint32_t xbox = xrow + static_cast<uint32_t>((pb0 + c_bi) * BB * 128);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint2 wg = lds64(w0 ^ (32u * j));
-      const uint2 wh = lds64(w1 ^ (32u * j));
+    for (int j = 0; j < BB; ++j) {
+      const uint32_t hb = kLutBoxBytes * (j >> 2);  // second TMA box of an 8-block stage
+      const uint2 wg = lds64((w0 + hb) ^ (32u * (j & 3)));
+      const uint2 wh = lds64((w1 + hb) ^ (32u * (j & 3)));
       // x: values 16t .. 16t+15 of block j of row g; lanes whose column
       // g is past M load nothing (their outputs are never stored), so a
       // load moves only the M rows' bytes
@@ -473,8 +526,8 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
         else
           mma_f16_acc(d, a0, a1, a2, a3, xr[2 * i], xr[2 * i + 1]);
       }
-      // (s of tile row 2g, of row 2g + 1) for block j
-      const uint2 sg = lds64(sl + (j < 2 ? 64u * j : 256u + 64u * ((j + 1) & 1)));
+      // (s of tile row 2g, of row 2g + 1) for block j: adjacent words
+      const uint2 sg = lds64(slot_addr(slot_word(j, 0) + 2u * g));
       const float sa = __uint_as_float(sg.x), sb = __uint_as_float(sg.y);
       if (M == 1) {
         acc[0] = __fmaf_rn(d[0], sa, acc[0]);
@@ -487,37 +540,41 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
       }
     }
     __syncwarp();
-    if (lane == 0 && !dead && q + kLutStages < total) {
+    if (lane == 0 && !dead && q + NS < total) {
       fence_proxy_async_smem();
       issue_at(p_tile, pb0 + p_bi, st);
       advance(p_tile, p_bi);
       ++issued_n;
     }
-    // scales of the next box into the other slot; raw loads for box q + 3
+    // scales of the next box into the slot (every lane is done with this
+    // box's); raw loads for box q + 3
     if (q + 1 < total) {
-      scale_store((q + 1) & 1, rA);
+      scale_store(rA);
       rA = rB;
       if (q + 3 < total) {
         scale_load(s_tile, pb0 + s_bi, rB);
         advance(s_tile, s_bi);
       }
     }
-    if (++st == kLutStages) {
+    if (++st == NS) {
       st = 0;
       ph ^= 1u;
     }
     // end of a unit (tile, part): reduce over the P parts and store y
     if (++c_bi == nmy) {
-      const int row = c_tile * 16 + 2 * g;
+      const int m = mat_of(c_tile);
+      const int Nm = G.N[m];
+      uint16_t* __restrict__ ym = G.y[m];
+      const int row = (c_tile - G.off[m]) * 16 + 2 * g;
       auto store = [&](const float (&v)[4]) {
         const int c0 = 2 * t, c1 = 2 * t + 1;
-        if (row < N) {
-          if (c0 < M) y[static_cast<int64_t>(c0) * N + row] = round_to_dt<DT>(v[0]);
-          if (c1 < M) y[static_cast<int64_t>(c1) * N + row] = round_to_dt<DT>(v[1]);
+        if (row < Nm) {
+          if (c0 < M) ym[static_cast<int64_t>(c0) * Nm + row] = round_to_dt<DT>(v[0]);
+          if (c1 < M) ym[static_cast<int64_t>(c1) * Nm + row] = round_to_dt<DT>(v[1]);
         }
-        if (row + 1 < N) {
-          if (c0 < M) y[static_cast<int64_t>(c0) * N + row + 1] = round_to_dt<DT>(v[2]);
-          if (c1 < M) y[static_cast<int64_t>(c1) * N + row + 1] = round_to_dt<DT>(v[3]);
+        if (row + 1 < Nm) {
+          if (c0 < M) ym[static_cast<int64_t>(c0) * Nm + row + 1] = round_to_dt<DT>(v[2]);
+          if (c1 < M) ym[static_cast<int64_t>(c1) * Nm + row + 1] = round_to_dt<DT>(v[3]);
         }
       };
       if (P == 1) {
@@ -550,9 +607,9 @@ gemv_lut_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
   }
   // drain copies still landing (only after a wait gave up)
   if (lane == 0 && dead) {
-    for (int s2 = 0; s2 < kLutStages; ++s2) {
-      const int n_st = issued_n > s2 ? (issued_n - s2 + kLutStages - 1) / kLutStages : 0;
-      const int w_st = waited_q >= s2 ? (waited_q - s2) / kLutStages + 1 : 0;
+    for (int s2 = 0; s2 < NS; ++s2) {
+      const int n_st = issued_n > s2 ? (issued_n - s2 + NS - 1) / NS : 0;
+      const int w_st = waited_q >= s2 ? (waited_q - s2) / NS + 1 : 0;
       if (n_st > w_st) mbar_wait_drain(bar_of(s2), static_cast<uint32_t>((n_st - 1) & 1));
     }
   }

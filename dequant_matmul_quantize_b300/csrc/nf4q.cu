@@ -136,6 +136,18 @@ nf4q_status gemv_attr_ready() {
 
 // Opt the block-scale-folded GEMV kernels in to their shared memory (once
 // per device).
+using LutKernelFn = void (*)(LutGroup, const uint16_t*, int, int, int, int, HalfCodes);
+
+// The folded-GEMV instantiation for a compute dtype, double quant and box size.
+template <int DT, bool DQ>
+LutKernelFn gemv_lut_kernel_dq(int bb) {
+  return bb == 8 ? gemv_lut_kernel<DT, DQ, 8> : gemv_lut_kernel<DT, DQ, 4>;
+}
+LutKernelFn gemv_lut_kernel_for(int dt, bool dq, int bb) {
+  if (dt == 0) return dq ? gemv_lut_kernel_dq<0, true>(bb) : gemv_lut_kernel_dq<0, false>(bb);
+  return dq ? gemv_lut_kernel_dq<1, true>(bb) : gemv_lut_kernel_dq<1, false>(bb);
+}
+
 nf4q_status gemv_lut_attr_ready() {
   static bool done[kMaxDevices] = {false};
   static std::mutex mu;
@@ -146,12 +158,12 @@ nf4q_status gemv_lut_attr_ready() {
   if (done[dev]) return NF4Q_OK;
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
   const int b = static_cast<int>(kLutSmemTop);
-  const char* what = "cudaFuncSetAttribute (GEMV, folded)";
-  if ((st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<0, true>, A, b), what)) != NF4Q_OK ||
-      (st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<1, true>, A, b), what)) != NF4Q_OK ||
-      (st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<0, false>, A, b), what)) != NF4Q_OK ||
-      (st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel<1, false>, A, b), what)) != NF4Q_OK)
-    return st;
+  for (int dt = 0; dt < 2; ++dt)
+    for (int dq = 0; dq < 2; ++dq)
+      for (int bb = 4; bb <= 8; bb += 4)
+        if ((st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel_for(dt, dq != 0, bb), A, b),
+                             "cudaFuncSetAttribute (GEMV, folded)")) != NF4Q_OK)
+          return st;
   done[dev] = true;
   return NF4Q_OK;
 }
@@ -541,24 +553,44 @@ nf4q_status gemv_weight_map(const nf4q_weight* wq, int box_rows, CUtensorMap* tw
                   "cuTensorMapEncodeTiled (GEMV weight)");
 }
 
-// Staged x of the folded GEMV: 64-blocks per row, a multiple of four.
-int64_t lut_kbx(int64_t K) { return (K / kBlock + 3) / 4 * 4; }
+// Staged x of the folded GEMV: 64-blocks per row, a multiple of the box.
+int64_t lut_kbx(int64_t K, int bb) { return (K / kBlock + bb - 1) / bb * bb; }
 
-// Whether the folded GEMV takes this call (M <= 8 and x fits its staging).
-bool lut_fits(int64_t K, int32_t M) {
-  return M <= kLutMaxM && static_cast<int64_t>(M) * lut_kbx(K) * 128 <= kLutXBytes;
+// Box size of the folded GEMV for this call: 8 blocks when x fits the room
+// that layout leaves it, else 4; 0 when the folded GEMV does not take the
+// call (M > 8, or x does not fit at all).
+int lut_box(int64_t K, int32_t M) {
+  if (M > kLutMaxM) return 0;
+  if (static_cast<int64_t>(M) * lut_kbx(K, 8) * 128 <= kLutXBytes8) return 8;
+  if (static_cast<int64_t>(M) * lut_kbx(K, 4) * 128 <= kLutXBytes4) return 4;
+  return 0;
 }
 
-// The block-scale-folded GEMV (gemv_lut.cuh).  Chooses the number of K
-// parts P a tile is split into (over P warps of a CTA) by the modelled
-// efficiency: tiles per round of the grid times boxes per part.
-nf4q_status gemv_lut_launch(const nf4q_weight* wq, const void* x, int32_t M, void* y,
-                            cudaStream_t s) {
+// The block-scale-folded GEMV (gemv_lut.cuh) over a group of 1..4 weights
+// with the same cols, code, double quant and compute dtype, sharing x.
+// Chooses the number of K parts P a tile is split into (over P warps of a
+// CTA) by the modelled efficiency: tiles per round of the grid times boxes
+// per part.
+nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void* x, int32_t M,
+                            void* const* y, cudaStream_t s) {
   nf4q_status st = gemv_lut_attr_ready();
   if (st != NF4Q_OK) return st;
-  const int N = static_cast<int>(wq->rows), K = static_cast<int>(wq->cols);
-  const int64_t T = (N + 15) / 16;
-  const int64_t nbox = (K / kBlock + 3) / 4;
+  const int K = static_cast<int>(wq[0]->cols);
+  const int bb = lut_box(K, M);
+  LutGroup G;
+  std::memset(&G, 0, sizeof(G));
+  G.count = count;
+  int64_t T = 0;
+  for (int i = 0; i < count; ++i) {
+    G.off[i] = static_cast<int>(T);
+    G.N[i] = static_cast<int>(wq[i]->rows);
+    G.sv[i] = scale_view(wq[i]);
+    G.y[i] = static_cast<uint16_t*>(y[i]);
+    if ((st = gemv_weight_map(wq[i], 16, &G.tmap[i])) != NF4Q_OK) return st;
+    T += (wq[i]->rows + 15) / 16;
+  }
+  for (int i = count; i <= kLutMaxGroup; ++i) G.off[i] = static_cast<int>(T);
+  const int64_t nbox = (K / kBlock + bb - 1) / bb;
   const int64_t sms = sm_count();
   int bestP = 1;
   double best = -1.0;
@@ -577,18 +609,15 @@ nf4q_status gemv_lut_launch(const nf4q_weight* wq, const void* x, int32_t M, voi
   }
   const int64_t SL = kLutWarps / bestP;
   const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
-  CUtensorMap tw;
-  if ((st = gemv_weight_map(wq, 16, &tw)) != NF4Q_OK) return st;
-  const bool bf = wq->compute_dtype == NF4Q_DT_BF16;
-  const auto k = wq->double_quant ? (bf ? gemv_lut_kernel<0, true> : gemv_lut_kernel<1, true>)
-                                  : (bf ? gemv_lut_kernel<0, false> : gemv_lut_kernel<1, false>);
+  const auto k = gemv_lut_kernel_for(wq[0]->compute_dtype == NF4Q_DT_BF16 ? 0 : 1,
+                                     wq[0]->double_quant != 0, bb);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   return launch("gemv_lut_kernel", k, dim3(static_cast<unsigned>(grid)), dim3(kLutThreads),
-                kLutSmemTop, s, attr, 1, tw, scale_view(wq),
-                static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), N, K,
-                static_cast<int>(M), bestP, static_cast<int>(lut_kbx(K)), half_codes(wq->code));
+                kLutSmemTop, s, attr, 1, G, static_cast<const uint16_t*>(x), K,
+                static_cast<int>(M), bestP, static_cast<int>(lut_kbx(K, bb)),
+                half_codes(wq[0]->code));
 }
 
 // The bit-faithful GEMV (gemv_mma.cuh): w_hat rebuilt exactly inside the
@@ -651,8 +680,43 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   bool done = false;
   nf4q_status st = gemv_checks(wq, x, M, y, s, &done);
   if (st != NF4Q_OK || done) return st;
-  if (lut_fits(wq->cols, M)) return gemv_lut_launch(wq, x, M, y, s);
+  if (lut_box(wq->cols, M)) return gemv_lut_launch(&wq, 1, x, M, &y, s);
   return gemv_exact_launch(wq, x, M, y, s);
+}
+
+nf4q_status nf4q_gemv_multi(const nf4q_weight* const* wq, int32_t count, const void* x,
+                            int32_t M, void* const* y, void* stream) {
+  if (!wq || !y || count < 1 || count > kLutMaxGroup) return NF4Q_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    if (!wq[i]) return NF4Q_ERR_INVALID_ARG;
+    nf4q_status st = check_shape(wq[i]);
+    if (st != NF4Q_OK) return st;
+    if (wq[i]->cols != wq[0]->cols || wq[i]->code != wq[0]->code ||
+        wq[i]->double_quant != wq[0]->double_quant ||
+        wq[i]->compute_dtype != wq[0]->compute_dtype)
+      return NF4Q_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // one launch when the folded GEMV takes the call and every weight is
+  // non-empty; else the weights one by one
+  bool one = lut_box(wq[0]->cols, M) != 0 && wq[0]->cols > 0;
+  for (int i = 0; i < count && one; ++i) {
+    bool done = false;
+    nf4q_status st = gemv_checks(wq[i], x, M, y[i], s, &done);
+    if (st != NF4Q_OK) return st;
+    one = !done;
+  }
+  if (!one) {
+    for (int i = 0; i < count; ++i) {
+      nf4q_status st = nf4q_gemv(wq[i], x, M, y[i], stream);
+      if (st != NF4Q_OK) return st;
+    }
+    return NF4Q_OK;
+  }
+  int64_t tiles = 0;
+  for (int i = 0; i < count; ++i) tiles += (wq[i]->rows + 15) / 16;
+  if (tiles > 0x7FFFFFFF) return NF4Q_ERR_UNSUPPORTED;
+  return gemv_lut_launch(wq, count, x, M, y, s);
 }
 
 nf4q_status nf4q_gemv_exact(const nf4q_weight* wq, const void* x, int32_t M, void* y,

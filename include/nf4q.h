@@ -207,6 +207,17 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream);
 nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M,
                       void* y, void* stream);
 
+/* nf4q_gemv over a group of 1..4 weights that share x (q, k and v of an
+ * attention block, gate and up of an MLP): y[i] = x . w_hat_i^T for each,
+ * in one launch when the block-scale-folded GEMV takes the call (then the
+ * same numerics as nf4q_gemv; else the weights go one by one through
+ * nf4q_gemv).  wq: host array of `count` weight pointers, all with the same
+ * cols, code, double_quant and compute_dtype (NF4Q_ERR_INVALID_ARG
+ * otherwise); y: host array of `count` device outputs [M x rows_i].  Other
+ * arguments and errors as nf4q_gemv. */
+nf4q_status nf4q_gemv_multi(const nf4q_weight* const* wq, int32_t count, const void* x,
+                            int32_t M, void* const* y, void* stream);
+
 /* nf4q_gemv with w_hat rebuilt bit for bit inside the contraction: y =
  * x . w_hat^T with w_hat exactly as nf4q_dequantize produces it, fp32
  * accumulation (only the order of the additions differs from an exact

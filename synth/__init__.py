@@ -120,9 +120,17 @@ def llama3_8b_matrix(layer: int, mid: int, device="cpu"):
     return normal_weight(n, k, 0.02, 1000 * layer + mid, device=device)
 
 
+# Matrices of a block that read the same activation row in a decoder layer:
+# q, k and v read the normalized hidden state, gate and up the normalized
+# attention output; o and down read their own inputs.
+LLAMA3_8B_X_GROUP = (0, 0, 0, 3, 4, 4, 6)
+
+
 def llama3_8b_x(layer: int, mid: int, device="cpu"):
+    """x [1 x K] ~ N(0, 1) bf16 of a stack matrix, shared within a group
+    (q/k/v, gate/up): seed 500000 + 1000 * layer + the group's first id."""
     _, n, k = LLAMA3_8B_LAYER[mid]
-    return activations(1, k, 500000 + 1000 * layer + mid, device=device)
+    return activations(1, k, 500000 + 1000 * layer + LLAMA3_8B_X_GROUP[mid], device=device)
 
 
 # ---------------------------------------------------------------- LLM.int8()

@@ -148,3 +148,32 @@ def test_folded_gemv_error_analysis(code):
     err = abs(ya - y_ref[0, 0])
     analytic = (2.0 ** -8 + 2.0 ** -11 + 2.0 ** -20) * bound[0, 0] + o.ulp_bf16(y_ref[0, 0])
     assert err <= analytic, (err, analytic)
+
+
+def test_grouped_gemv_matches_the_oracle_per_weight():
+    """nf4q_gemv_multi: three weights sharing x (q, k, v shaped, rows not
+    multiples of 16) in one launch; every output against the oracle, and
+    each equal to its own nf4q_gemv within the tolerance."""
+    shapes = [(300, 1024), (70, 1024), (64, 1024)]
+    ws = [synth.normal_weight(n, k, 0.02, seed=60 + i) for i, (n, k) in enumerate(shapes)]
+    checked = [full_check(w, "nf4", True, f"group {i}") for i, w in enumerate(ws)]
+    for M in (1, 3):
+        x = synth.activations(M, 1024, seed=63 + M)
+        ys = nq.gemv_multi([q for q, _ in checked], x.cuda())
+        for (qw, w_hat), y in zip(checked, ys):
+            assert y.shape == (M, qw.rows)
+            check_matmul(bf16_bits(y), bf16_bits(x), w_hat, f"grouped M={M}")
+            check_matmul(bf16_bits(nq.gemv(qw, x.cuda())), bf16_bits(x), w_hat, "single")
+
+
+def test_grouped_gemv_refuses_mixed_groups():
+    a = nq.quantize(synth.normal_weight(64, 256, 0.02, seed=70).cuda())
+    b = nq.quantize(synth.normal_weight(64, 320, 0.02, seed=71).cuda())
+    c = nq.quantize(synth.normal_weight(64, 256, 0.02, seed=72).cuda(), "fp4")
+    x = synth.activations(1, 256, seed=73).cuda()
+    with pytest.raises(nq.Nf4qError):          # codes differ: refused by the C ABI
+        nq.gemv_multi([a, c], x)
+    with pytest.raises(ValueError):            # columns differ: refused by the binding
+        nq.gemv_multi([a, b], x)
+    with pytest.raises(ValueError):
+        nq.gemv_multi([a] * 5, x)
