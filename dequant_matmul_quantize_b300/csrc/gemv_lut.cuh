@@ -191,10 +191,11 @@ __device__ __forceinline__ uint32_t lut_x_addr(uint32_t xbase, int kbx, int m, i
 // at most the boxes of a row), kbx = 64-blocks of staged x per row (a
 // multiple of BB, >= K/64).  Requires M <= 8 and M * kbx * 128 <= the x room
 // of BB.  Launched as a programmatic dependent of the previous kernel.
-template <int DT, bool DQ, int BB>
+template <int DT, bool DQ, int BB, bool EP, bool M1>
 __global__ void __launch_bounds__(kLutThreads, 1)
-gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__ x, int K, int M,
-                int P, int kbx, const __grid_constant__ HalfCodes hc) {
+gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__ x, int K,
+                int M_arg, int P, int kbx, const __grid_constant__ HalfCodes hc) {
+  const int M = M1 ? 1 : M_arg;  // M1: compiled for a single row of x
   using Cfg = LutCfg<BB>;
   constexpr int NS = Cfg::kStages;
   extern __shared__ __align__(1024) uint8_t lsm[];
@@ -269,8 +270,6 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     for (int k = 0; k < 4; ++k) sts128(a + 16 * k, vv);
   }
 
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
   // stream positions: consumer, scale loader (two boxes ahead), producer
   // (NS boxes ahead, lane 0); each advances one box at a time
   auto advance = [&](int& tile, int& bi) {
@@ -279,6 +278,22 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       tile += tile_stride;
     }
   };
+
+  // The first NS boxes of each warp go to L2 while the kernels this one
+  // depends on finish: the weights are read-only here, and an L2 prefetch
+  // is safe even if they were still being written.
+  if (lane == 0) {
+    int f_tile = tile0, f_bi = 0;
+    for (int q = 0; q < min(NS, total); ++q) {
+      const int m = mat_of(f_tile);
+#pragma unroll
+      for (int h = 0; h < BB / 4; ++h)
+        tma_prefetch_2d(&G.tmap[m], ((pb0 + f_bi) * (BB / 4) + h) * 128, (f_tile - G.off[m]) * 16);
+      advance(f_tile, f_bi);
+    }
+  }
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int p_tile = tile0, p_bi = 0;
   if (lane == 0) {
     for (int q = 0; q < min(NS, total); ++q) {
@@ -295,7 +310,54 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     return lut_piece(kLutPieceMisc + 1 + i / 32) + 4u * (i % 32);
   };
   const int n8 = K / 8;  // 16-byte groups per row
-  if (DT == 0) {
+  // M = 1 and at most 16384 staged columns: one read of x, kept in
+  // registers (4 x 16 bytes per thread) from the maximum to the conversion
+  const bool x1 = M1 && kbx * 8 <= 4 * kLutThreads;
+  int F1 = 0;  // the F of the single row (x1)
+  if (x1) {
+    uint4 xv[4];
+    float mx = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = threadIdx.x + r * kLutThreads;
+      xv[r] = i < n8 ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
+      const uint32_t wv[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mx = fmaxf(mx, fmaxf(fabsf(bf16lo_to_f32(wv[k])), fabsf(bf16hi_to_f32(wv[k]))));
+    }
+    if (DT == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      if (lane == 0) sts32(fscr_addr(warp, 0), __float_as_uint(mx));
+      __syncthreads();
+      mx = 0.f;
+      for (int w = 0; w < kLutWarps; ++w)
+        mx = fmaxf(mx, __uint_as_float(lds32(fscr_addr(w, 0))));
+      // F = exponent of mx minus 14: mx * 2^-F lies in [2^14, 2^15)
+      if (mx > 0.f && mx == mx) {
+        const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+        F1 = max(-126, min(127, e - 14));
+      }
+      if (threadIdx.x == 0) sts32(misc, static_cast<uint32_t>(F1));
+    }
+    const float sc = __uint_as_float(static_cast<uint32_t>(127 - F1) << 23);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = threadIdx.x + r * kLutThreads;
+      if (i < kbx * 8) {  // 16-byte groups of staged x; past K they are 0
+        uint4 out = xv[r];
+        if (DT == 0) {
+          out.x = pack_f16x2(bf16lo_to_f32(xv[r].x) * sc, bf16hi_to_f32(xv[r].x) * sc);
+          out.y = pack_f16x2(bf16lo_to_f32(xv[r].y) * sc, bf16hi_to_f32(xv[r].y) * sc);
+          out.z = pack_f16x2(bf16lo_to_f32(xv[r].z) * sc, bf16hi_to_f32(xv[r].z) * sc);
+          out.w = pack_f16x2(bf16lo_to_f32(xv[r].w) * sc, bf16hi_to_f32(xv[r].w) * sc);
+        }
+        sts128(lut_x_addr(xbase, kbx, 0, i >> 3, 16 * (i & 7)), out);
+      }
+    }
+  }
+  if (DT == 0 && !x1) {
     for (int m = 0; m < M; ++m) {
       float mx = 0.f;
       for (int i = threadIdx.x; i < n8; i += kLutThreads) {
@@ -310,8 +372,8 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       if (lane == 0) sts32(fscr_addr(warp, m), __float_as_uint(mx));
     }
   }
-  __syncthreads();
-  if (DT == 0 && threadIdx.x < M) {
+  if (!x1) __syncthreads();
+  if (DT == 0 && !x1 && threadIdx.x < M) {
     float mx = 0.f;
     for (int w = 0; w < kLutWarps; ++w)
       mx = fmaxf(mx, __uint_as_float(lds32(fscr_addr(w, threadIdx.x))));
@@ -323,8 +385,8 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     }
     sts32(misc + 4u * threadIdx.x, static_cast<uint32_t>(F));
   }
-  __syncthreads();
-  {
+  if (!x1) __syncthreads();
+  if (!x1) {
     // convert / copy: thread -> 8 consecutive values of one row
     const int groups = M * kbx * 8;  // 16-byte groups of staged x
     for (int i = threadIdx.x; i < groups; i += kLutThreads) {
@@ -353,7 +415,9 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   float f0 = 0.f, f1 = 0.f;
   {
     const int m0 = 2 * t, m1 = 2 * t + 1;
-    if (DT == 0) {
+    if (DT == 0 && x1) {
+      if (m0 < M) f0 = __uint_as_float(static_cast<uint32_t>(127 + F1) << 23);
+    } else if (DT == 0) {
       if (m0 < M) f0 = __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(lds32(misc + 4u * m0))) << 23);
       if (m1 < M) f1 = __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(lds32(misc + 4u * m1))) << 23);
     } else {
@@ -447,6 +511,79 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     }
   };
 
+  // Chunked scale loads (EP: double quant with K / 64 a multiple of 16).  A
+  // chunk is 16 blocks of the tile's 16 rows: lanes 0..15 hold the 16 int8
+  // scale codes of row `lane` (one 16-byte load), lanes 16..31 the scale2 of
+  // row `lane - 16` (16 blocks aligned to 16 never straddle a 256-block
+  // group).  Chunks are loaded two ahead of the one in use, in the order the
+  // warp meets them: its units' chunks c0 .. c0 + nch - 1 of each tile.
+  const int c0 = (pb0 * BB) / 16;
+  const int nch = nmy > 0 ? (pb1 * BB - 1) / 16 - c0 + 1 : 0;
+  float offs[kLutMaxGroup];
+#pragma unroll
+  for (int i = 0; i < kLutMaxGroup; ++i)
+    offs[i] = (EP && i < G.count) ? __ldg(G.sv[i].offset) : 0.f;
+  auto chunk_load = [&](int tile, int ci) -> uint4 {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (EP && tile < T) {
+      const int m = mat_of(tile);
+      const int row = (tile - G.off[m]) * 16 + (lane & 15);
+      if (row < G.N[m]) {
+        const int64_t b0 = static_cast<int64_t>(row) * KB + 16 * (c0 + ci);
+        if (lane < 16)
+          v = __ldg(reinterpret_cast<const uint4*>(G.sv[m].absmax_q + b0));
+        else
+          v.x = __float_as_uint(__ldg(G.sv[m].scale2 + (b0 >> 8)));
+      }
+    }
+    return v;
+  };
+  auto chunk_next = [&](int& tile, int& ci) {
+    if (++ci == nch) {
+      ci = 0;
+      tile += tile_stride;
+    }
+  };
+  uint4 E0 = make_uint4(0, 0, 0, 0), E1 = E0, E2 = E0;
+  int k_tile = tile0, k_ci = 0;  // chunk held in E0
+  int e_tile = tile0, e_ci = 0;  // next chunk to load
+  if (EP && total > 0) {
+    E0 = chunk_load(e_tile, e_ci);
+    chunk_next(e_tile, e_ci);
+    E1 = chunk_load(e_tile, e_ci);
+    chunk_next(e_tile, e_ci);
+    E2 = chunk_load(e_tile, e_ci);
+    chunk_next(e_tile, e_ci);
+  }
+  auto word_of = [](const uint4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+  };
+  // scales of box bb of `tile` into the slot, from the chunk registers
+  auto scale_store_ep = [&](int tile, int bb) {
+    const int ci = (bb * BB) / 16 - c0;
+    while (tile != k_tile || ci != k_ci) {
+      E0 = E1;
+      E1 = E2;
+      E2 = chunk_load(e_tile, e_ci);
+      chunk_next(e_tile, e_ci);
+      chunk_next(k_tile, k_ci);
+    }
+    const int o = (bb * BB) & 15;  // first block of the box in the chunk
+    const float s2 = __uint_as_float(__shfl_sync(0xFFFFFFFFu, E0.x, 16 + (lane & 15)));
+    const uint32_t other = __shfl_sync(0xFFFFFFFFu, word_of(E0, (o + NBL) >> 2), lane & 15);
+    const uint32_t qw = lane < 16 ? word_of(E0, o >> 2) : other;
+    const int sh = 8 * ((o + sjb) & 3);
+    float off = offs[0];
+#pragma unroll
+    for (int i = 1; i < kLutMaxGroup; ++i)
+      if (i < G.count && tile >= G.off[i]) off = offs[i];
+#pragma unroll
+    for (int j = 0; j < NBL; ++j) {
+      const float qv = static_cast<float>(static_cast<int8_t>((qw >> (sh + 8 * j)) & 0xFFu));
+      sts32(slot_addr(slot_word(sjb + j, srow)), __float_as_uint(__fmaf_rn(qv, s2, off) * fs));
+    }
+  };
+
   // 5. per-lane constants.  MMA row g is tile row 2g, MMA row g + 8 is tile
   //    row 2g + 1, so that the four rows a half-warp reads in one load sit
   //    on distinct banks under the 128-byte swizzle: row r's 16-byte chunk c
@@ -461,21 +598,29 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   // table address = [lane * 4, code byte, 0x01, 0]: the table sits at 0x10000
   const uint32_t L = kLutTable | (static_cast<uint32_t>(lane) << 2);
 
-  // raw scales: box q + 1 in rA, box q + 2 in rB while box q is consumed
+  // raw scales (without EP): box q + 1 in rA, box q + 2 in rB while box q
+  // is consumed
   Raw rA, rB;
   int s_tile = tile0, s_bi = 0;
-  if (total > 0) {
-    scale_load(s_tile, pb0 + s_bi, rA);
-    scale_store(rA);
-    advance(s_tile, s_bi);
-  }
-  if (total > 1) {
-    scale_load(s_tile, pb0 + s_bi, rA);
-    advance(s_tile, s_bi);
-  }
-  if (total > 2) {
-    scale_load(s_tile, pb0 + s_bi, rB);
-    advance(s_tile, s_bi);
+  if (EP) {
+    if (total > 0) {
+      scale_store_ep(s_tile, pb0 + s_bi);
+      advance(s_tile, s_bi);
+    }
+  } else {
+    if (total > 0) {
+      scale_load(s_tile, pb0 + s_bi, rA);
+      scale_store(rA);
+      advance(s_tile, s_bi);
+    }
+    if (total > 1) {
+      scale_load(s_tile, pb0 + s_bi, rA);
+      advance(s_tile, s_bi);
+    }
+    if (total > 2) {
+      scale_load(s_tile, pb0 + s_bi, rB);
+      advance(s_tile, s_bi);
+    }
   }
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -549,11 +694,16 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     // scales of the next box into the slot (every lane is done with this
     // box's); raw loads for box q + 3
     if (q + 1 < total) {
-      scale_store(rA);
-      rA = rB;
-      if (q + 3 < total) {
-        scale_load(s_tile, pb0 + s_bi, rB);
+      if (EP) {
+        scale_store_ep(s_tile, pb0 + s_bi);
         advance(s_tile, s_bi);
+      } else {
+        scale_store(rA);
+        rA = rB;
+        if (q + 3 < total) {
+          scale_load(s_tile, pb0 + s_bi, rB);
+          advance(s_tile, s_bi);
+        }
       }
     }
     if (++st == NS) {

@@ -138,14 +138,23 @@ nf4q_status gemv_attr_ready() {
 // per device).
 using LutKernelFn = void (*)(LutGroup, const uint16_t*, int, int, int, int, HalfCodes);
 
-// The folded-GEMV instantiation for a compute dtype, double quant and box size.
-template <int DT, bool DQ>
-LutKernelFn gemv_lut_kernel_dq(int bb) {
-  return bb == 8 ? gemv_lut_kernel<DT, DQ, 8> : gemv_lut_kernel<DT, DQ, 4>;
+// The folded-GEMV instantiation for a compute dtype, double quant, box size,
+// whether the scales are read in 16-block chunks (double quant with K / 64
+// a multiple of 16) and whether x has a single row.
+template <int DT, bool DQ, int BB>
+LutKernelFn gemv_lut_kernel_bb(bool ep, bool m1) {
+  if (DQ && ep)
+    return m1 ? gemv_lut_kernel<DT, DQ, BB, DQ, true> : gemv_lut_kernel<DT, DQ, BB, DQ, false>;
+  return m1 ? gemv_lut_kernel<DT, DQ, BB, false, true> : gemv_lut_kernel<DT, DQ, BB, false, false>;
 }
-LutKernelFn gemv_lut_kernel_for(int dt, bool dq, int bb) {
-  if (dt == 0) return dq ? gemv_lut_kernel_dq<0, true>(bb) : gemv_lut_kernel_dq<0, false>(bb);
-  return dq ? gemv_lut_kernel_dq<1, true>(bb) : gemv_lut_kernel_dq<1, false>(bb);
+template <int DT, bool DQ>
+LutKernelFn gemv_lut_kernel_dq(int bb, bool ep, bool m1) {
+  return bb == 8 ? gemv_lut_kernel_bb<DT, DQ, 8>(ep, m1) : gemv_lut_kernel_bb<DT, DQ, 4>(ep, m1);
+}
+LutKernelFn gemv_lut_kernel_for(int dt, bool dq, int bb, bool ep, bool m1) {
+  if (dt == 0)
+    return dq ? gemv_lut_kernel_dq<0, true>(bb, ep, m1) : gemv_lut_kernel_dq<0, false>(bb, ep, m1);
+  return dq ? gemv_lut_kernel_dq<1, true>(bb, ep, m1) : gemv_lut_kernel_dq<1, false>(bb, ep, m1);
 }
 
 nf4q_status gemv_lut_attr_ready() {
@@ -161,9 +170,11 @@ nf4q_status gemv_lut_attr_ready() {
   for (int dt = 0; dt < 2; ++dt)
     for (int dq = 0; dq < 2; ++dq)
       for (int bb = 4; bb <= 8; bb += 4)
-        if ((st = cuda_check(cudaFuncSetAttribute(gemv_lut_kernel_for(dt, dq != 0, bb), A, b),
-                             "cudaFuncSetAttribute (GEMV, folded)")) != NF4Q_OK)
-          return st;
+        for (int v = 0; v < 4; ++v)
+          if ((st = cuda_check(cudaFuncSetAttribute(
+                   gemv_lut_kernel_for(dt, dq != 0, bb, (v & 1) != 0, (v & 2) != 0), A, b),
+                   "cudaFuncSetAttribute (GEMV, folded)")) != NF4Q_OK)
+            return st;
   done[dev] = true;
   return NF4Q_OK;
 }
@@ -610,7 +621,8 @@ nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void*
   const int64_t SL = kLutWarps / bestP;
   const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
   const auto k = gemv_lut_kernel_for(wq[0]->compute_dtype == NF4Q_DT_BF16 ? 0 : 1,
-                                     wq[0]->double_quant != 0, bb);
+                                     wq[0]->double_quant != 0, bb, (K / kBlock) % 16 == 0,
+                                     M == 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
