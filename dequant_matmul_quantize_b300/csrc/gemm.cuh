@@ -26,6 +26,15 @@
 // sets bit 0 of the device error word and the CTA winds down: its other
 // waits stop, its TMA copies and MMAs are drained (bounded), its TMEM freed.
 // No multicast: every CTA loads its own tiles.
+//
+// Split K (M <= 128 with fewer 128 x 128 tiles than SMs): a thread-block
+// cluster of S <= 4 CTAs shares one tile, CTA r taking k-steps
+// [r KT / S, (r + 1) KT / S).  After a cluster barrier (every CTA's main
+// loop has finished, so rank 0's rings are idle) ranks 1 .. S-1 write their
+// fp32 accumulators into rank 0's shared memory (distributed shared memory,
+// 128 x 128 floats each, 16-byte chunks swizzled by row); after a second
+// barrier rank 0 adds them in rank order to its own and stores Y, so the
+// result is deterministic.
 #pragma once
 
 #include <mutex>
@@ -166,6 +175,94 @@ __device__ __forceinline__ void store_accumulators(uint32_t tmem, int warp, int 
   }
 }
 
+// Split-K partials: rank p (1 .. S-1) of a cluster writes its 128 x BN fp32
+// accumulator to rank 0's shared memory at base + (p - 1) * 128 * BN * 4,
+// row-major, the 16-byte chunk c of row r at chunk c ^ (r & 7).  Warp w
+// (2 .. 17) takes TMEM lane quarter w % 4 (the one it may access) and the
+// 32-column chunks from ((w - 2) / 8) * 32 in steps of 64; warps with
+// ((w - 2) / 4) odd have no second accumulator to drain (one per CTA here).
+__device__ __forceinline__ uint32_t split_partial_addr(uint32_t base, int bn, int p, int r,
+                                                       int col) {
+  return base + static_cast<uint32_t>((p - 1) * 128 * bn * 4 + r * bn * 4) +
+         static_cast<uint32_t>((((col >> 2) ^ (r & 7)) << 4) + (col & 3) * 4);
+}
+
+template <int BN>
+__device__ __forceinline__ void send_partials(uint32_t tmem, int warp, int lane, uint32_t base,
+                                              uint32_t rank) {
+  const int q = warp & 3;
+  if ((((warp - 2) >> 2) & 1) != 0) return;
+  const int cc = ((warp - 2) >> 3) * 32;
+  const int r = q * 32 + lane;
+#pragma unroll 1
+  for (int col = cc; col < BN; col += 64) {
+    uint32_t v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col, v);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t local = split_partial_addr(base, BN, static_cast<int>(rank), r, col + 4 * c);
+      uint32_t remote;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(local));
+      asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(remote),
+                   "r"(v[4 * c]), "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
+                   : "memory");
+    }
+  }
+}
+
+// Rank 0: its accumulator plus ranks 1 .. S-1 in order, rounded and stored
+// as store_accumulators does for rows m0 .. m0 + 127.
+template <int BN, int DT>
+__device__ __forceinline__ void store_split_sum(uint32_t tmem, int warp, int lane, uint32_t base,
+                                                int S, uint16_t* __restrict__ Y, int M, int ncols,
+                                                int m0, int c0) {
+  const int q = warp & 3;
+  if ((((warp - 2) >> 2) & 1) != 0) return;
+  const int cc = ((warp - 2) >> 3) * 32;
+  const int r = q * 32 + lane;
+  const int m = m0 + r;
+  uint16_t* yrow = Y + static_cast<int64_t>(m) * ncols + c0;
+  const bool vec = (ncols & 7) == 0;
+#pragma unroll 1
+  for (int col = cc; col < BN; col += 64) {
+    uint32_t v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col, v);
+    for (int p = 1; p < S; ++p) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 w;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                     : "r"(split_partial_addr(base, BN, p, r, col + 4 * c))
+                     : "memory");
+        v[4 * c] = __float_as_uint(__uint_as_float(v[4 * c]) + __uint_as_float(w.x));
+        v[4 * c + 1] = __float_as_uint(__uint_as_float(v[4 * c + 1]) + __uint_as_float(w.y));
+        v[4 * c + 2] = __float_as_uint(__uint_as_float(v[4 * c + 2]) + __uint_as_float(w.z));
+        v[4 * c + 3] = __float_as_uint(__uint_as_float(v[4 * c + 3]) + __uint_as_float(w.w));
+      }
+    }
+    if (m < M) {
+      const int n = min(32, ncols - (c0 + col));
+      if (n == 32 && vec) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 o;
+          o.x = pack_x2<DT>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+          o.y = pack_x2<DT>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+          o.z = pack_x2<DT>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+          o.w = pack_x2<DT>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+          *reinterpret_cast<uint4*>(yrow + col + 8 * j) = o;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < n) yrow[col + j] = round_to_dt<DT>(__uint_as_float(v[j]));
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ the kernel
 template <int CODE, int BN, int DT, int MT>
 __global__ void __launch_bounds__(GemmCfg<BN, MT>::kThreads, 1)
@@ -196,6 +293,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (MT * kGemmBM);
   const int KT = K / kGemmBK;
+  // split K: this CTA's k-steps kb .. kb + KTl - 1 (the whole range without a split)
+  const int S = static_cast<int>(gridDim.z);
+  uint32_t rank = 0;
+  if (S > 1) asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int kb = static_cast<int>(rank) * KT / S;
+  const int KTl = (static_cast<int>(rank) + 1) * KT / S - kb;
 
   if (threadIdx.x == 0) {
     *abort = 0u;
@@ -228,32 +331,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
       int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % SA;
-        const uint32_t ph = (kt / SA) & 1;
+      for (int i = 0; i < KTl; ++i) {
+        const int kt = kb + i;
+        const int s = i % SA;
+        const uint32_t ph = (i / SA) & 1;
         if (!mbar_wait(aempty_bar(s), ph ^ 1, abort)) break;
         mbar_arrive_expect_tx(full_bar(s), MT * kGemmATile + Cfg::kPTile);
         tma_load_2d(sA(s, 0), &tmap_x, kt * kGemmBK, m0, full_bar(s));
         if (MT == 2) tma_load_2d(sA(s, 1), &tmap_x, kt * kGemmBK, m0 + kGemmBM, full_bar(s));
         tma_load_2d(sP(s), &tmap_w, kt * (kGemmBK / 2), n0, full_bar(s));
-        issued = kt + 1;
+        issued = i + 1;
       }
       // wind-down: make sure no copy is still landing in this CTA's smem
-      for (int kt = (issued > SA ? issued - SA : 0); kt < issued; ++kt)
-        mbar_wait_drain(full_bar(kt % SA), (kt / SA) & 1);
+      for (int i = (issued > SA ? issued - SA : 0); i < issued; ++i)
+        mbar_wait_drain(full_bar(i % SA), (i / SA) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc<DT>(kGemmBM, BN);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int sa = kt % SA, sb = kt % SB;
-        if (!mbar_wait(full_bar(sa), (kt / SA) & 1, abort)) break;
-        if (!mbar_wait(bfull_bar(sb), (kt / SB) & 1, abort)) break;
+      for (int i = 0; i < KTl; ++i) {
+        const int sa = i % SA, sb = i % SB;
+        if (!mbar_wait(full_bar(sa), (i / SA) & 1, abort)) break;
+        if (!mbar_wait(bfull_bar(sb), (i / SB) & 1, abort)) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kGemmBK / 16; ++k) {
           const uint64_t bdesc = smem_desc_sw128(sB(sb) + 32 * k);
-          const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
+          const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
           mma_bf16(tmem, smem_desc_sw128(sA(sa, 0) + 32 * k), bdesc, idesc, acc);
           if (MT == 2) mma_bf16(tmem + 256, smem_desc_sw128(sA(sa, 1) + 32 * k), bdesc, idesc, acc);
         }
@@ -301,14 +405,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
     };
     const float off = sv.double_quant ? __ldg(sv.offset) : 0.f;
     ScaleGroup gcur, gnext;
-    load_group(gcur, 0);
-    load_group(gnext, 16);
-    for (int kt = grp; kt < KT; kt += Cfg::kGroups) {
-      const int sa = kt % SA, sb = kt % SB;
+    int g16 = kb & ~15;  // first k-step of the group of 16 in gcur
+    load_group(gcur, g16);
+    load_group(gnext, g16 + 16);
+    for (int i = grp; i < KTl; i += Cfg::kGroups) {
+      const int kt = kb + i;
+      const int sa = i % SA, sb = i % SB;
       const int j = kt & 15;
-      if (kt >= 16 && j < Cfg::kGroups) {  // first k-step of this thread in a new group of 16
+      if ((kt & ~15) != g16) {  // first k-step of this thread in a new group of 16
+        g16 += 16;
         gcur = gnext;
-        load_group(gnext, kt - j + 16);
+        load_group(gnext, g16 + 16);
       }
       float sc;
       if (sv.double_quant) {
@@ -321,8 +428,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       RowTable<CODE> T;
       build_table<CODE, DT>(T, sc, C);
       // B slot sb is free once the MMAs of the previous round on it are done
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bempty_bar(sb), ((kt / SB) & 1) ^ 1, abort) &&
-                                       mbar_wait(full_bar(sa), (kt / SA) & 1, abort)))
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bempty_bar(sb), ((i / SB) & 1) ^ 1, abort) &&
+                                       mbar_wait(full_bar(sa), (i / SA) & 1, abort)))
         break;
       if (active) {
         const uint8_t* prow = gbase + (sP(sa) - base) + r * 32;
@@ -343,9 +450,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       if (lane == 0) mbar_arrive(bfull_bar(sb));
     }
     // ---------------- epilogue: TMEM -> bf16 -> Y
-    if (warp < 18 && __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
+    if (S == 1 && warp < 18 && __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
       tc_fence_after();
       store_accumulators<BN, DT, MT>(tmem, warp, lane, Y, M, N, m0, n0);
+    }
+  }
+  if (MT == 1 && S > 1) {
+    // split K: every thread of the cluster passes both barriers
+    __syncwarp();
+    const bool epi = warp >= 2 && warp < 18;
+    bool ok = true;
+    if (epi) ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort));
+    tc_fence_before();
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (epi && ok && rank > 0) {
+      tc_fence_after();
+      send_partials<BN>(tmem, warp, lane, base, rank);
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (epi && ok && rank == 0) {
+      tc_fence_after();
+      store_split_sum<BN, DT>(tmem, warp, lane, base, S, Y, M, N, m0, n0);
     }
   }
   tc_fence_before();
@@ -383,9 +510,19 @@ inline int gemm_pick_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
+// K split of a one-accumulator launch (M <= 128): the largest S <= 4 with
+// S x tiles CTAs in one wave and at least 8 k-steps per CTA.  The partials
+// of ranks 1 .. 3 (64 KB each) fit in rank 0's idle TMA and B rings.
+inline int gemm_split_k(int64_t tiles, int64_t kt, int sms) {
+  int S = 1;
+  while (S < 4 && tiles * (S + 1) <= sms && kt / (S + 1) >= 8) ++S;
+  return S;
+}
+
 template <int CODE, int BN, int DT, int MT = 2>
 inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, const ScaleView& sv,
-                                  const CodeValues& C, int64_t M, void* Y, cudaStream_t stream) {
+                                  const CodeValues& C, int64_t M, void* Y, cudaStream_t stream,
+                                  int sms) {
   using Cfg = GemmCfg<BN, MT>;
   const int64_t N = wq->rows, K = wq->cols;
   EncodeTiledFn enc = encode_tiled_fn();
@@ -417,26 +554,34 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
       attr_set[dev] = true;
     }
   }
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + MT * kGemmBM - 1) / (MT * kGemmBM));
+  const int S = MT == 1 ? gemm_split_k(tiles, K / kGemmBK, sms) : 1;
   dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
-            static_cast<unsigned>((M + MT * kGemmBM - 1) / (MT * kGemmBM)));
+            static_cast<unsigned>((M + MT * kGemmBM - 1) / (MT * kGemmBM)),
+            static_cast<unsigned>(S));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = static_cast<unsigned>(S);
   return launch("gemm_kernel", gemm_kernel<CODE, BN, DT, MT>, grid, dim3(Cfg::kThreads), Cfg::kSmem,
-                stream, nullptr, 0, tx, tw, sv, static_cast<uint16_t*>(Y), static_cast<int>(M),
-                static_cast<int>(N), static_cast<int>(K), C);
+                stream, attr, S > 1 ? 1u : 0u, tx, tw, sv, static_cast<uint16_t*>(Y),
+                static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), C);
 }
 
 template <int CODE, int DT>
 inline nf4q_status gemm_launch_code(const CUtensorMap& tx, const nf4q_weight* wq,
                                     const ScaleView& sv, const CodeValues& C, int64_t M, void* Y,
-                                    cudaStream_t stream, int bn) {
+                                    cudaStream_t stream, int bn, int sms) {
   // M <= 128: one accumulator per CTA and 128-row W tiles, with the deeper
   // TMA ring the smaller stages allow
-  if (M <= kGemmBM) return gemm_launch_bn<CODE, 128, DT, 1>(tx, wq, sv, C, M, Y, stream);
+  if (M <= kGemmBM) return gemm_launch_bn<CODE, 128, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
   switch (bn) {
-    case 224: return gemm_launch_bn<CODE, 224, DT>(tx, wq, sv, C, M, Y, stream);
-    case 192: return gemm_launch_bn<CODE, 192, DT>(tx, wq, sv, C, M, Y, stream);
-    case 160: return gemm_launch_bn<CODE, 160, DT>(tx, wq, sv, C, M, Y, stream);
-    case 128: return gemm_launch_bn<CODE, 128, DT>(tx, wq, sv, C, M, Y, stream);
-    default: return gemm_launch_bn<CODE, 256, DT>(tx, wq, sv, C, M, Y, stream);
+    case 224: return gemm_launch_bn<CODE, 224, DT>(tx, wq, sv, C, M, Y, stream, sms);
+    case 192: return gemm_launch_bn<CODE, 192, DT>(tx, wq, sv, C, M, Y, stream, sms);
+    case 160: return gemm_launch_bn<CODE, 160, DT>(tx, wq, sv, C, M, Y, stream, sms);
+    case 128: return gemm_launch_bn<CODE, 128, DT>(tx, wq, sv, C, M, Y, stream, sms);
+    default: return gemm_launch_bn<CODE, 256, DT>(tx, wq, sv, C, M, Y, stream, sms);
   }
 }
 
@@ -464,10 +609,10 @@ inline nf4q_status gemm_launch(const nf4q_weight* wq, const ScaleView& sv,
   if (st != NF4Q_OK) return st;
   const int bn = gemm_pick_bn(M, N, sms);
   if (dt == 0)
-    return wq->code == 0 ? gemm_launch_code<0, 0>(tx, wq, sv, C, M, Y, stream, bn)
-                         : gemm_launch_code<1, 0>(tx, wq, sv, C, M, Y, stream, bn);
-  return wq->code == 0 ? gemm_launch_code<0, 1>(tx, wq, sv, C, M, Y, stream, bn)
-                       : gemm_launch_code<1, 1>(tx, wq, sv, C, M, Y, stream, bn);
+    return wq->code == 0 ? gemm_launch_code<0, 0>(tx, wq, sv, C, M, Y, stream, bn, sms)
+                         : gemm_launch_code<1, 0>(tx, wq, sv, C, M, Y, stream, bn, sms);
+  return wq->code == 0 ? gemm_launch_code<0, 1>(tx, wq, sv, C, M, Y, stream, bn, sms)
+                       : gemm_launch_code<1, 1>(tx, wq, sv, C, M, Y, stream, bn, sms);
 }
 
 }  // namespace nf4q

@@ -32,7 +32,10 @@ def _oracle_what(w, code):
     (1, 256, 64), (64, 256, 256), (128, 512, 512), (200, 300, 320), (129, 257, 192),
     (256, 1000, 1024), (383, 768, 2048), (512, 256, 4096),
     # one-accumulator CTAs (M <= 128) with ragged N and K
-    (100, 300, 320), (128, 200, 4160), (1, 129, 64), (77, 1000, 192)])
+    (100, 300, 320), (128, 200, 4160), (1, 129, 64), (77, 1000, 192),
+    # K split over a cluster: S = 4 with k ranges not aligned to 16 k-steps
+    # (37 k-steps), S = 2 (17 k-steps), S = 4 on a ragged 130-row weight
+    (33, 700, 2368), (128, 1000, 1088), (5, 130, 4096)])
 def test_gemm_small(M, N, K):
     w = synth.normal_weight(N, K, 0.02, seed=N + K, outlier_frac=1e-3)
     x = synth.activations(M, K, seed=M)
@@ -52,6 +55,29 @@ def test_gemm_fp4_and_no_dq():
             ref = oracle_state(as_f32(w).reshape(-1), code, dq)
             what = o.dequantize(ref["packed"], ref["scales"], CODE_ID[code]).reshape(w.shape)
             check_matmul(bf16_bits(y), bf16_bits(x), what, f"{code} dq={dq}")
+
+
+@pytest.mark.parametrize("code,dq,dt", [("nf4", True, "f16"), ("fp4", True, "bf16"),
+                                        ("nf4", False, "bf16"), ("fp4", False, "f16")])
+def test_gemm_split_k_configs(code, dq, dt):
+    """Split K (2 tiles, 32 k-steps: S = 4) for the other codes, without
+    double quantization and with fp16; two calls give identical bits."""
+    w = synth.normal_weight(200, 2048, 0.02, seed=21)
+    x = synth.activations(40, 2048, seed=22)
+    if dt == "f16":
+        x = x.to(torch.float16)
+    qw = nq.quantize(w.cuda(), code, dq, compute_dtype=dt)
+    y1 = nq.gemm(qw, x.cuda())
+    y2 = nq.gemm(qw, x.cuda())
+    assert torch.equal(y1, y2)
+    ref = oracle_state(as_f32(w).reshape(-1), code, dq)
+    dt_id = o.DT_F16 if dt == "f16" else o.DT_BF16
+    what = o.dequantize(ref["packed"], ref["scales"], CODE_ID[code], dtype=dt_id).reshape(w.shape)
+    if dt == "f16":
+        check_matmul(y1.cpu().view(torch.int16).numpy().view(np.uint16),
+                     x.view(torch.int16).numpy().view(np.uint16), what, f"split {code}", o.DT_F16)
+    else:
+        check_matmul(bf16_bits(y1), bf16_bits(x), what, f"split {code} dq={dq}")
 
 
 def test_gemm_matches_gemv_and_cublas():
