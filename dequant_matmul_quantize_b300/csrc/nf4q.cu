@@ -692,7 +692,7 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   bool done = false;
   nf4q_status st = gemv_checks(wq, x, M, y, s, &done);
   if (st != NF4Q_OK || done) return st;
-  if (lut_box(wq->cols, M)) return gemv_lut_launch(&wq, 1, x, M, &y, s);
+  if (M <= NF4Q_GEMV_FOLD_MAX_M && lut_box(wq->cols, M)) return gemv_lut_launch(&wq, 1, x, M, &y, s);
   return gemv_exact_launch(wq, x, M, y, s);
 }
 

@@ -195,23 +195,26 @@ nf4q_status nf4q_dequantize(const nf4q_weight* wq, void* out, void* stream);
  * accumulation, output rounded to the compute dtype.
  *   x: device [M x cols], y: device [M x rows], both of wq->compute_dtype
  *   (bf16 or fp16) and 16-byte aligned.
- * For M <= 8 (when M * cols <= 30720, the staging room for x) the block
- * scale is folded: y = sum_b s_b * sum_{k in b} x_k * code_value[code_k],
+ * For M <= NF4Q_GEMV_FOLD_MAX_M (when M * cols <= 30720, the staging room
+ * for x) the block scale is folded:
+ * y = sum_b s_b * sum_{k in b} x_k * code_value[code_k],
  * with the code values rounded to fp16 and x converted to fp16 after a
  * power-of-two scaling per row (exact for every bf16 x within 2^31 of its
  * row's largest |x|).  This differs from x . w_hat^T only by the rounding of
  * w_hat = bf16(code_value * s_b) and of the code values: at most 2^-8 + 2^-11
  * of |x_k w_hat_k| per term (fp16 compute dtype: 2^-10), signed like those
  * roundings.
- * Other calls, and nf4q_gemv_exact always, use w_hat itself. */
+ * Other calls, and nf4q_gemv_exact always, use w_hat itself (measured on a
+ * B300: from M = 3 on, the exact kernel is as fast or faster). */
+#define NF4Q_GEMV_FOLD_MAX_M 2
 nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M,
                       void* y, void* stream);
 
 /* nf4q_gemv over a group of 1..4 weights that share x (q, k and v of an
  * attention block, gate and up of an MLP): y[i] = x . w_hat_i^T for each,
- * in one launch when the block-scale-folded GEMV takes the call (then the
- * same numerics as nf4q_gemv; else the weights go one by one through
- * nf4q_gemv).  wq: host array of `count` weight pointers, all with the same
+ * in one launch of the block-scale-folded GEMV when M <= 8 and x fits its
+ * staging room (numerics as the folded nf4q_gemv above, for any such M);
+ * else the weights go one by one through nf4q_gemv.  wq: host array of `count` weight pointers, all with the same
  * cols, code, double_quant and compute_dtype (NF4Q_ERR_INVALID_ARG
  * otherwise); y: host array of `count` device outputs [M x rows_i].  Other
  * arguments and errors as nf4q_gemv. */

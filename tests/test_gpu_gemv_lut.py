@@ -1,4 +1,6 @@
-"""The block-scale-folded GEMV (nf4q_gemv for M <= 8) against the oracle.
+"""The block-scale-folded GEMV against the oracle.  nf4q_gemv takes it for
+M <= 2; nf4q_gemv_multi (here with a single weight) for M <= 8, which is
+how the tests reach it at every M.
 
 The folded kernel multiplies x by code_value * s_b (code values rounded to
 fp16) instead of by w_hat = bf16(code_value * s_b); it is held to the same
@@ -36,6 +38,11 @@ def _setup():
     assert nq.device_error() == 0
 
 
+def folded(qw, x):
+    """The folded kernel for any M <= 8: a one-weight group."""
+    return nq.gemv_multi([qw], x)[0]
+
+
 # (rows, cols) -> the split the launch picks: (37, 320) P=2, (256, 1024) P=4,
 # (129, 4160) P=16, (4000, 256) P=1, (2400, 1024) P=4, (700, 2112) P=8
 SHAPES = [(37, 320), (256, 1024), (129, 4160), (4000, 256), (2400, 1024), (700, 2112)]
@@ -48,7 +55,7 @@ def test_folded_gemv_parity(code, M, shape):
     w = synth.normal_weight(*shape, 0.02, seed=shape[0] + M, outlier_frac=1e-3)
     qw, w_hat = full_check(w, code, True, f"{code} {shape}")
     x = synth.activations(M, shape[1], seed=100 + M)
-    y = nq.gemv(qw, x.cuda())
+    y = folded(qw, x.cuda())
     check_matmul(bf16_bits(y), bf16_bits(x), w_hat, f"folded {code} M={M} {shape}")
 
 
@@ -63,13 +70,13 @@ def test_folded_gemv_fp16_and_no_double_quant(M):
     scales = o.block_scales(st["absmax_q"], st["scale2"], st["offset"])
     w_hat16 = o.dequantize(st["packed"], scales, o.CODE_NF4, dtype=o.DT_F16).reshape(300, 1088)
     x = synth.activations(M, 1088, seed=8).to(torch.float16)
-    y = nq.gemv(qw, x.cuda())
+    y = folded(qw, x.cuda())
     check_matmul(y.cpu().view(torch.int16).numpy().view(np.uint16),
                  x.view(torch.int16).numpy().view(np.uint16), w_hat16, "folded fp16", o.DT_F16)
     # no double quantization: the fp32 absmax is the scale
     qn, w_hat_n = full_check(w, "fp4", False, "no-dq")
     xb = synth.activations(M, 1088, seed=9)
-    check_matmul(bf16_bits(nq.gemv(qn, xb.cuda())), bf16_bits(xb), w_hat_n, "folded no-dq")
+    check_matmul(bf16_bits(folded(qn, xb.cuda())), bf16_bits(xb), w_hat_n, "folded no-dq")
 
 
 def test_folded_gemv_rows_of_x_far_apart_in_magnitude():
@@ -85,7 +92,7 @@ def test_folded_gemv_rows_of_x_far_apart_in_magnitude():
     g = torch.Generator().manual_seed(13)
     x[6] = x[6] * torch.exp2(-30.0 * torch.rand(K, generator=g))
     x = x.to(torch.bfloat16)
-    y = nq.gemv(qw, x.cuda())
+    y = folded(qw, x.cuda())
     assert torch.all(y[5] == 0)
     check_matmul(bf16_bits(y), bf16_bits(x), w_hat, "x row scales")
 
@@ -94,8 +101,8 @@ def test_folded_gemv_is_deterministic_and_near_the_exact_kernel():
     w = synth.normal_weight(1500, 2048, 0.02, seed=14, outlier_frac=1e-3)
     qw, w_hat = full_check(w, "nf4", True, "determinism")
     x = synth.activations(3, 2048, seed=15).cuda()
-    y1 = nq.gemv(qw, x)
-    y2 = nq.gemv(qw, x)
+    y1 = folded(qw, x)
+    y2 = folded(qw, x)
     assert torch.equal(y1, y2)
     ye = nq.gemv_exact(qw, x)
     check_matmul(bf16_bits(y1), bf16_bits(x), w_hat, "folded")
@@ -148,6 +155,16 @@ def test_folded_gemv_error_analysis(code):
     err = abs(ya - y_ref[0, 0])
     analytic = (2.0 ** -8 + 2.0 ** -11 + 2.0 ** -20) * bound[0, 0] + o.ulp_bf16(y_ref[0, 0])
     assert err <= analytic, (err, analytic)
+
+
+def test_gemv_dispatch_by_m():
+    """nf4q_gemv: the folded kernel for M <= 2, the exact one from M = 3."""
+    w = synth.normal_weight(300, 1024, 0.02, seed=31)
+    qw = nq.quantize(w.cuda())
+    for M in (1, 2, 3, 8, 16):
+        x = synth.activations(M, 1024, seed=32 + M).cuda()
+        want = folded(qw, x) if M <= 2 else nq.gemv_exact(qw, x)
+        assert torch.equal(nq.gemv(qw, x), want), M
 
 
 def test_grouped_gemv_matches_the_oracle_per_weight():
