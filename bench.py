@@ -4,14 +4,17 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One STEP is one decode token through the 32-layer Llama-3-8B-shaped stack:
-224 NF4 GEMVs (nf4q_gemv, M = 1) over the weights q [4096x4096], k, v
-[1024x4096], o [4096x4096], gate, up [14336x4096] and down [4096x14336] of
-every layer (bf16 N(0, 0.02), seed 1000 * layer + matrix, quantized once to
-NF4 with double quantization before timing; x ~ N(0, 1) bf16 per matrix).
-The packed weights and scales (3.61 GB) are far larger than L2, so every
-step reads them from HBM.  The 224 launches are one CUDA graph; `value` is
-the token's algorithmic bytes (packed codes + int8 scales + scale2 + offset
-+ x + y of every GEMV) over its device time, summed over ranks.
+224 NF4 GEMVs (M = 1) over the weights q [4096x4096], k, v [1024x4096],
+o [4096x4096], gate, up [14336x4096] and down [4096x14336] of every layer
+(bf16 N(0, 0.02), seed 1000 * layer + matrix, quantized once to NF4 with
+double quantization before timing; x ~ N(0, 1) bf16, one per layer input:
+q, k and v share theirs, as do gate and up).  They run as 128 launches, as a
+decoder issues them: per layer nf4q_gemv_multi(q, k, v), nf4q_gemv(o),
+nf4q_gemv_multi(gate, up), nf4q_gemv(down).  The packed weights and scales
+(3.61 GB) are far larger than L2, so every step reads them from HBM.  The
+launches are one CUDA graph; `value` is the token's algorithmic bytes
+(packed codes + int8 scales + scale2 + offset + x + y of every GEMV) over
+its device time, summed over ranks.
 
 The same run also reports, each on its own workload: the whole path of the
 Llama-7B decode shapes (quantize + double quant, dequantize and GEMV of
@@ -141,11 +144,13 @@ def kernel_bytes(N, K, M=1):
 
 
 # DRAM bytes (read + write) per launch of the GEMV kernel on the decode
-# token, averaged over the 224 launches, from one ncu capture of the
-# GEMV kernel.  They hold only for the kernel sources they were measured on:
-# `traffic` is reported as null as soon as the digest of those sources
-# (STEP_SOURCES) differs.
-MEASURED_TRAFFIC = {"csrc_digest": "", "gemv_per_launch": None}
+# token: the mean over layer 0's four launches (every layer has the same
+# shapes), from one ncu capture of dram__bytes_read.sum and
+# dram__bytes_write.sum (`python profile_cases.py layer`, the second pass's
+# four gemv_lut_kernel launches).  They hold only for the kernel sources they
+# were measured on: `traffic` is reported as null as soon as the digest of
+# those sources (STEP_SOURCES) differs.
+MEASURED_TRAFFIC = {"csrc_digest": "95e497925148a017", "gemv_per_launch": 28181824}
 
 
 # The sources of the step's kernel and of its launch code.

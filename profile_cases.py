@@ -8,6 +8,12 @@ Each case builds its seeded synthetic input, runs the library call twice
     quant11008   nf4q_quantize_dq then nf4q_dequantize, 11008x4096 decode weight
     gemv70b      nf4q_gemv M=1 on the 28672x8192 weight (NF4)
     gemv70b_exact  nf4q_gemv_exact M=1 on the same weight
+    token        one Llama-3-8B decode token twice over the 224-weight stack:
+                 per layer nf4q_gemv_multi(q, k, v), nf4q_gemv(o),
+                 nf4q_gemv_multi(gate, up), nf4q_gemv(down) - 128 launches
+                 per token, as the benchmark step issues them
+    layer        the same four launches for layer 0 only, twice
+    gateup       nf4q_gemv_multi(gate, up) of layer 0, twice
     gemv4096     nf4q_gemv M=1 on the 4096x4096 decode weight
     gemv11008    nf4q_gemv M=1 on the 11008x4096 decode weight
     gemv70b_m16  nf4q_gemv M=16 on the 28672x8192 weight (NF4)
@@ -41,7 +47,24 @@ def _run(case: str, torch, nq, synth) -> None:
         if st != 0:
             raise RuntimeError(f"{what}: status {st}")
 
-    if case == "quant11008":
+    if case in ("token", "layer", "gateup"):
+        groups = ((0, 1, 2), (3,), (4, 5), (6,)) if case != "gateup" else ((4, 5),)
+        layers = synth.LLAMA3_8B_LAYERS if case == "token" else 1
+        launches = []
+        for layer in range(layers):
+            for mids in groups:
+                qws = [nq.quantize(synth.llama3_8b_matrix(layer, mid, device=dev)) for mid in mids]
+                x = synth.llama3_8b_x(layer, mids[0], device=dev)
+                ys = [torch.empty(1, q.rows, dtype=torch.bfloat16, device=dev) for q in qws]
+                launches.append((qws, x, ys))
+        torch.cuda.synchronize()
+        for _ in range(2):
+            for qws, x, ys in launches:
+                if len(qws) == 1:
+                    nq.gemv(qws[0], x, out=ys[0])
+                else:
+                    nq.gemv_multi(qws, x, outs=ys)
+    elif case == "quant11008":
         w, _ = synth.llama7b_decode(1, device=dev)
         N, K = w.shape
         qw = nq.QuantizedWeight.empty(N, K, device=dev)
