@@ -17,12 +17,14 @@
 // the signed value), so at most one point T is in reach, and
 // code = lo(bin) + [wn > T] * dl(bin) (dl = 1 for NF4).  A second FMA forms
 // e = (v r - T) 2^19 from the table's -T 2^19; if |e| <= 1 (v r within about
-// 2^-19 of T) the two sides of T could disagree and the unit is recomputed
-// with the exact division and a plain count over all T_j; so are blocks
+// 2^-19 of T) the two sides of T could disagree and that element's compare
+// is redone on the exact quotient (IEEE division) at the same T - frequent
+// for bf16 FP4 input, whose quotients often land exactly on 1/8; blocks
 // whose absmax is zero, below 2^-100 (2^19 / absmax would overflow) or above
-// 2^126 (1/absmax not a normal number) or not finite.  Otherwise sat(e) is the compare bit exactly, and
-// lo + bit (one add on the table's float 2^23 + lo) is the code in the low
-// mantissa bits.  The result is therefore exactly the rule; the fast path
+// 2^126 (1/absmax not a normal number) or not finite take the exact rule
+// (division and a plain count over all T_j) for every element.  Otherwise
+// sat(e) is the compare bit exactly, and lo + bit (one add on the table's
+// float 2^23 + lo) is the code in the low mantissa bits.  The result is therefore exactly the rule; the fast path
 // only saves work.  The eight codes of a word are packed by a multiply-add
 // chain (Horner) on those float bit patterns, and one addition removes the
 // 2^23 terms.  The tables are replicated once per lane in shared memory, so
@@ -88,6 +90,34 @@ __device__ __forceinline__ uint32_t code_fast(float v, float r128, float r19, ui
     c = __fmaf_rn(bit, dl, lof);
   }
   return __float_as_uint(c);
+}
+
+// The code of v (bits of 2^23 + code, as code_fast) with the comparison at
+// the bin's decision point T made on the exact quotient q = fp32(v / a) when
+// v r is within reach of T (|e| <= 1); otherwise the fast compare bit, which
+// is exact there.  The bins carry a quarter-bin margin and v r is within
+// 2^-21 of the quotient, so T is also the only decision point that can
+// separate q from the bin's lower code: lo + [q beyond T] dl is the rule,
+// with "beyond" q > T for NF4 and for FP4's positive points, and q >= T for
+// FP4's negative points -T_j (the FP4 rule compares |q| > T_j, so a tie
+// keeps the smaller magnitude).
+template <int CODE>
+__device__ __forceinline__ uint32_t code_fixed(float v, float a, float r128, float r19,
+                                               uint32_t lane_tab, uint32_t lane_dl) {
+  const float y = __fmaf_rn(v, r128, 129.0f + kMagic);
+  const uint32_t yb = __float_as_uint(y);
+  float ntp, lof;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(ntp), "=f"(lof) : "r"(yb * 256u + lane_tab));
+  const float e = __fmaf_rn(v, r19, ntp);
+  float bit = sat_add0(e);
+  if (fabsf(e) <= 1.0f) {
+    const float q = __fdiv_rn(v, a), t = -ntp * (1.0f / kTwo19);  // t exact: a power-of-two scaling
+    bit = (CODE == 1 && t < 0.f) ? (q >= t ? 1.0f : 0.0f) : (q > t ? 1.0f : 0.0f);
+  }
+  if (CODE == 0) return __float_as_uint(__fadd_rn(lof, bit));
+  float dl;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(dl) : "r"(yb * 128u + lane_dl));
+  return __float_as_uint(__fmaf_rn(bit, dl, lof));
 }
 
 template <int CODE>
@@ -260,13 +290,41 @@ quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
           const int i = (6 - 2 * (k >> 1)) + (k & 1);
           wd = wd * 16u + code_fast<CODE>(vh[i], r128, r19, lane_tab, lane_dl, near[h]);
         }
+        if (IN != 0 && near[h] <= 1.0f) {
+          // a value within reach of a decision point: the word again, with
+          // the exact quotient at that point (16-bit inputs: the values are
+          // still in registers; fp32 inputs are read again below, which
+          // costs their register-heavier loop less)
+          wd = 0;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = (6 - 2 * (k >> 1)) + (k & 1);
+            wd = wd * 16u + code_fixed<CODE>(vh[i], a, r128, r19, lane_tab, lane_dl);
+          }
+        }
         word[h] = wd + kCodeMagicFix;
       }
     }
     if (live) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (near[h] <= 1.0f || !ok) word[h] = encode_word_exact<CODE, IN>(w, 2 * unit + h, a, P);
+      for (int h = 0; h < 2; ++h) {
+        if (!ok) {
+          word[h] = encode_word_exact<CODE, IN>(w, 2 * unit + h, a, P);
+        } else if (IN == 0 && near[h] <= 1.0f) {
+          float r;
+          asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+          const float r128 = r * 128.0f, r19 = r * kTwo19;
+          float vh[8];
+          load_unit<IN>(w, 2 * unit + h, vh);
+          uint32_t wd = 0;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = (6 - 2 * (k >> 1)) + (k & 1);
+            wd = wd * 16u + code_fixed<CODE>(vh[i], a, r128, r19, lane_tab, lane_dl);
+          }
+          word[h] = wd + kCodeMagicFix;
+        }
+      }
       packed[unit] = make_uint2(word[0], word[1]);
       if ((lane & 3u) == 0u) {
         absmax[unit >> 2] = a;
