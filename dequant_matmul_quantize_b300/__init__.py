@@ -335,7 +335,8 @@ def gemm(qw, x, out=None, stream=None):
 
 
 def matmul(qw, x, out=None, stream=None):
-    """Dispatch on M: gemv for M <= 16, gemm above."""
+    """Dispatch on M: gemv for M <= 16 (gemm for M = 9..16 on weights of at
+    least 20000 rows), gemm above."""
     return _mm("nf4q_matmul", qw, x, out, stream)
 
 

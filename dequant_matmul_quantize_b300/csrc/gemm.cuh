@@ -56,10 +56,11 @@ constexpr int kGemmTmemCols = 512;
 template <int BN, int MT = 2>
 struct GemmCfg {
   static constexpr int kBTile = BN * kGemmBK * 2;     // bf16 W tile
-  static constexpr int kPTile = BN * kGemmBK / 2;     // packed W tile
+  static constexpr int kPTile = BN * kGemmBK / 2;     // packed W tile (bytes the TMA moves)
+  static constexpr int kPSlot = (kPTile + 1023) / 1024 * 1024;  // its room in a stage
   static constexpr int kAStages =                     // TMA stages: MT X tiles + packed W
       MT == 2 ? 4 : (BN <= 128 ? 8 : 6);
-  static constexpr int kAStage = MT * kGemmATile + kPTile;
+  static constexpr int kAStage = MT * kGemmATile + kPSlot;
   static constexpr int kBStages =                     // dequantized W stages
       (kAStages * kAStage + 3 * kBTile + 2048 <= 232448 - 1024) ? 3 : 2;
   static constexpr size_t kSmem = 1024 + kAStages * kAStage + kBStages * kBTile + 1024;
@@ -68,7 +69,8 @@ struct GemmCfg {
   // one mbarrier phase ahead of the MMA on its stage.
   static constexpr int kGroups = kBStages;
   static constexpr int kThreads = 64 + kGroups * 256;   // + TMA warp and MMA warp
-  static_assert(kPTile % 1024 == 0 && kBTile % 1024 == 0, "1 KB alignment of tiles");
+  static_assert(kPTile % 256 == 0 && kBTile % 1024 == 0, "tile alignment (swizzle atoms)");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(MT == 1 || MT == 2, "one or two accumulators");
 };
@@ -154,7 +156,7 @@ __device__ __forceinline__ void store_accumulators(uint32_t tmem, int warp, int 
     uint32_t v[32];
     tmem_ld32(tmem + h * 256 + (static_cast<uint32_t>(q * 32) << 16) + col, v);
     if (m < M) {
-      const int n = min(32, ncols - (c0 + col));
+      const int n = min(min(32, BN - col), ncols - (c0 + col));
       if (n == 32 && vec) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -190,6 +192,7 @@ __device__ __forceinline__ uint32_t split_partial_addr(uint32_t base, int bn, in
 template <int BN>
 __device__ __forceinline__ void send_partials(uint32_t tmem, int warp, int lane, uint32_t base,
                                               uint32_t rank) {
+  static_assert(BN % 32 == 0, "split K runs with whole 32-column chunks");
   const int q = warp & 3;
   if ((((warp - 2) >> 2) & 1) != 0) return;
   const int cc = ((warp - 2) >> 3) * 32;
@@ -455,7 +458,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       store_accumulators<BN, DT, MT>(tmem, warp, lane, Y, M, N, m0, n0);
     }
   }
-  if (MT == 1 && S > 1) {
+  if constexpr (MT == 1 && BN % 32 == 0) if (S > 1) {
     // split K: every thread of the cluster passes both barriers
     __syncwarp();
     const bool epi = warp >= 2 && warp < 18;
@@ -555,7 +558,7 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
     }
   }
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + MT * kGemmBM - 1) / (MT * kGemmBM));
-  const int S = MT == 1 ? gemm_split_k(tiles, K / kGemmBK, sms) : 1;
+  const int S = (MT == 1 && BN % 32 == 0) ? gemm_split_k(tiles, K / kGemmBK, sms) : 1;
   dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
             static_cast<unsigned>((M + MT * kGemmBM - 1) / (MT * kGemmBM)),
             static_cast<unsigned>(S));
@@ -569,13 +572,34 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
                 static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), C);
 }
 
+// BN of a one-accumulator launch (M <= 128).  Each CTA rebuilds BN weight
+// rows per k-step, so within one wave the time grows with BN: the smallest
+// candidate whose tiles fit the SMs.  Weights narrow enough for the K split
+// (at most half the SMs' worth of 128-wide tiles) keep BN = 128 and split.
+inline int gemm_pick_bn1(int64_t N, int sms) {
+  if ((N + 127) / 128 * 2 <= sms) return 128;
+  const int cands[6] = {80, 112, 128, 160, 208, 256};
+  for (int bn : cands)
+    if ((N + bn - 1) / bn <= sms) return bn;
+  return 128;
+}
+
 template <int CODE, int DT>
 inline nf4q_status gemm_launch_code(const CUtensorMap& tx, const nf4q_weight* wq,
                                     const ScaleView& sv, const CodeValues& C, int64_t M, void* Y,
                                     cudaStream_t stream, int bn, int sms) {
-  // M <= 128: one accumulator per CTA and 128-row W tiles, with the deeper
-  // TMA ring the smaller stages allow
-  if (M <= kGemmBM) return gemm_launch_bn<CODE, 128, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
+  // M <= 128: one accumulator per CTA, with the deeper TMA ring the smaller
+  // stages allow, and W tiles as narrow as one wave allows
+  if (M <= kGemmBM) {
+    switch (gemm_pick_bn1(wq->rows, sms)) {
+      case 80: return gemm_launch_bn<CODE, 80, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
+      case 112: return gemm_launch_bn<CODE, 112, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
+      case 160: return gemm_launch_bn<CODE, 160, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
+      case 208: return gemm_launch_bn<CODE, 208, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
+      case 256: return gemm_launch_bn<CODE, 256, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
+      default: return gemm_launch_bn<CODE, 128, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
+    }
+  }
   switch (bn) {
     case 224: return gemm_launch_bn<CODE, 224, DT>(tx, wq, sv, C, M, Y, stream, sms);
     case 192: return gemm_launch_bn<CODE, 192, DT>(tx, wq, sv, C, M, Y, stream, sms);

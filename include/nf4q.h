@@ -236,8 +236,11 @@ nf4q_status nf4q_gemv_exact(const nf4q_weight* wq, const void* x, int32_t M,
 nf4q_status nf4q_gemm(const nf4q_weight* wq, const void* X, int64_t M,
                       void* Y, void* stream);
 
-/* Dispatch on M: nf4q_gemv for M <= NF4Q_GEMV_MAX_M, nf4q_gemm above. */
+/* Dispatch on M: nf4q_gemv for M <= NF4Q_GEMV_MAX_M, nf4q_gemm above, and
+ * nf4q_gemm also for M = 9..16 on weights of at least NF4Q_MATMUL_GEMM_ROWS
+ * rows (the crossover measured on a B300). */
 #define NF4Q_GEMV_MAX_M 16
+#define NF4Q_MATMUL_GEMM_ROWS 20000
 nf4q_status nf4q_matmul(const nf4q_weight* wq, const void* X, int64_t M,
                         void* Y, void* stream);
 

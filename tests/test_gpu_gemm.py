@@ -35,7 +35,10 @@ def _oracle_what(w, code):
     (100, 300, 320), (128, 200, 4160), (1, 129, 64), (77, 1000, 192),
     # K split over a cluster: S = 4 with k ranges not aligned to 16 k-steps
     # (37 k-steps), S = 2 (17 k-steps), S = 4 on a ragged 130-row weight
-    (33, 700, 2368), (128, 1000, 1088), (5, 130, 4096)])
+    (33, 700, 2368), (128, 1000, 1088), (5, 130, 4096),
+    # narrower W tiles for M <= 128 (one wave): BN = 80, 112, 208, each with
+    # a ragged last tile and a partial 32-column chunk in the epilogue
+    (33, 11008, 256), (7, 14376, 128), (100, 28600, 192)])
 def test_gemm_small(M, N, K):
     w = synth.normal_weight(N, K, 0.02, seed=N + K, outlier_frac=1e-3)
     x = synth.activations(M, K, seed=M)
@@ -94,6 +97,18 @@ def test_gemm_matches_gemv_and_cublas():
     y_cublas = torch.matmul(x, nq.dequantize(qw).T)
     check_matmul(bf16_bits(y_cublas), bf16_bits(x), what, "cublas")
     check_matmul(bf16_bits(nq.matmul(qw, x)), bf16_bits(x), what, "matmul dispatch")
+
+
+def test_matmul_dispatch():
+    """nf4q_matmul: the GEMV up to M = 16, except M = 9..16 on weights of
+    20000 rows or more, which take the GEMM (bitwise the same call)."""
+    for rows, K in ((300, 256), (20000, 128)):
+        qw = nq.quantize(synth.normal_weight(rows, K, 0.02, seed=rows).cuda())
+        for M in (1, 8, 9, 16, 17):
+            x = synth.activations(M, K, seed=M).cuda()
+            gemm = M > 16 or (M > 8 and rows >= 20000)
+            want = nq.gemm(qw, x) if gemm else nq.gemv(qw, x)
+            assert torch.equal(nq.matmul(qw, x), want), (rows, M)
 
 
 def test_gemm_one_hot_rows_exact():
