@@ -23,6 +23,12 @@
 // Rows n >= N and columns k >= K of the last tiles get scale 0 (w_hat = 0);
 // the TMA zero-fills dY beyond N, so they add nothing.  Every wait is
 // bounded as in the forward kernel.
+//
+// When 128 x 128 tiles (one accumulator, MT = 1) fit one wave, a CTA owns
+// 128 rows of dY, and if the tiles still leave SMs idle the contraction
+// over n is split across a thread-block cluster (S <= 4 CTAs, stages
+// [r NT / S, (r + 1) NT / S) for rank r) whose fp32 partials are summed in
+// rank order in rank 0's shared memory, as in the forward kernel's split K.
 #pragma once
 
 #include "gemm.cuh"
@@ -31,13 +37,13 @@ namespace nf4q {
 
 constexpr int kDxRows = 64;  // contraction rows n per stage
 
-template <int BN>
+template <int BN, int MT = 2>
 struct GemmDxCfg {
   static constexpr int kChunks = BN / 64;              // 64-column chunks (blocks) per row
   static constexpr int kBTile = kDxRows * BN * 2;      // dequantized w_hat tile
   static constexpr int kPTile = kDxRows * BN / 2;      // packed tile
-  static constexpr int kAStages = 4;
-  static constexpr int kAStage = 2 * kGemmATile + kPTile;
+  static constexpr int kAStages = MT == 2 ? 4 : 8;
+  static constexpr int kAStage = MT * kGemmATile + kPTile;
   static constexpr int kBStages =
       (kAStages * kAStage + 3 * kBTile + 2048 <= 232448 - 1024) ? 3 : 2;
   static constexpr size_t kSmem = 1024 + kAStages * kAStage + kBStages * kBTile + 1024;
@@ -46,6 +52,7 @@ struct GemmDxCfg {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: whole 64-blocks, MMA N <= 256");
   static_assert(kPTile % 1024 == 0 && kBTile % 1024 == 0, "1 KB alignment of tiles");
   static_assert(kSmem <= 232448, "shared memory");
+  static_assert(MT == 1 || MT == 2, "one or two accumulators");
 };
 
 // MN-major operand in the 128-byte swizzled layout: the leading byte offset
@@ -59,20 +66,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
-template <int CODE, int BN, int DT>
-__global__ void __launch_bounds__(GemmDxCfg<BN>::kThreads, 1)
+template <int CODE, int BN, int DT, int MT>
+__global__ void __launch_bounds__(GemmDxCfg<BN, MT>::kThreads, 1)
 gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
                const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
                uint16_t* __restrict__ dX, int M, int N, int K,
                const __grid_constant__ CodeValues C) {
-  using Cfg = GemmDxCfg<BN>;
+  using Cfg = GemmDxCfg<BN, MT>;
   constexpr int SA = Cfg::kAStages, SB = Cfg::kBStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   auto sA = [&](int s, int h) { return base + s * Cfg::kAStage + h * kGemmATile; };
-  auto sP = [&](int s) { return base + s * Cfg::kAStage + 2 * kGemmATile; };
+  auto sP = [&](int s) { return base + s * Cfg::kAStage + MT * kGemmATile; };
   auto sB = [&](int s) { return base + SA * Cfg::kAStage + s * Cfg::kBTile; };
   const uint32_t sBar = base + SA * Cfg::kAStage + SB * Cfg::kBTile;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sBar - base) + 512);
@@ -84,8 +91,14 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
   const uint32_t acc_bar = sBar + 8u * (2 * SA + 2 * SB);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k0 = blockIdx.x * BN, m0 = blockIdx.y * (2 * kGemmBM);
+  const int k0 = blockIdx.x * BN, m0 = blockIdx.y * (MT * kGemmBM);
   const int NT = (N + kDxRows - 1) / kDxRows;  // stages
+  // split of the contraction: this CTA's stages t0 .. t0 + nst - 1
+  const int S = static_cast<int>(gridDim.z);
+  uint32_t rank = 0;
+  if (S > 1) asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int t0 = static_cast<int>(rank) * NT / S;
+  const int nst = (static_cast<int>(rank) + 1) * NT / S - t0;
 
   if (threadIdx.x == 0) {
     *abort = 0u;
@@ -118,33 +131,34 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_dy)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
       int issued = 0;
-      for (int t = 0; t < NT; ++t) {
-        const int s = t % SA;
-        if (!mbar_wait(aempty_bar(s), ((t / SA) & 1) ^ 1, abort)) break;
-        mbar_arrive_expect_tx(full_bar(s), 2 * kGemmATile + Cfg::kPTile);
+      for (int i = 0; i < nst; ++i) {
+        const int t = t0 + i;
+        const int s = i % SA;
+        if (!mbar_wait(aempty_bar(s), ((i / SA) & 1) ^ 1, abort)) break;
+        mbar_arrive_expect_tx(full_bar(s), MT * kGemmATile + Cfg::kPTile);
         tma_load_2d(sA(s, 0), &tmap_dy, t * kDxRows, m0, full_bar(s));
-        tma_load_2d(sA(s, 1), &tmap_dy, t * kDxRows, m0 + kGemmBM, full_bar(s));
+        if (MT == 2) tma_load_2d(sA(s, 1), &tmap_dy, t * kDxRows, m0 + kGemmBM, full_bar(s));
         tma_load_2d(sP(s), &tmap_w, k0 / 2, t * kDxRows, full_bar(s));
-        issued = t + 1;
+        issued = i + 1;
       }
-      for (int t = (issued > SA ? issued - SA : 0); t < issued; ++t)
-        mbar_wait_drain(full_bar(t % SA), (t / SA) & 1);
+      for (int i = (issued > SA ? issued - SA : 0); i < issued; ++i)
+        mbar_wait_drain(full_bar(i % SA), (i / SA) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc<DT>(kGemmBM, BN) | (1u << 16);  // B MN-major
-      for (int t = 0; t < NT; ++t) {
-        const int sa = t % SA, sb = t % SB;
-        if (!mbar_wait(full_bar(sa), (t / SA) & 1, abort)) break;
-        if (!mbar_wait(bfull_bar(sb), (t / SB) & 1, abort)) break;
+      for (int i = 0; i < nst; ++i) {
+        const int sa = i % SA, sb = i % SB;
+        if (!mbar_wait(full_bar(sa), (i / SA) & 1, abort)) break;
+        if (!mbar_wait(bfull_bar(sb), (i / SB) & 1, abort)) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kDxRows / 16; ++k) {
           // rows 16k .. 16k+15 of the stage: two 8-row groups of 1 KB
           const uint64_t bdesc = smem_desc_sw128_mn(sB(sb) + 2048 * k);
-          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+          const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
           mma_bf16(tmem, smem_desc_sw128(sA(sa, 0) + 32 * k), bdesc, idesc, acc);
-          mma_bf16(tmem + 256, smem_desc_sw128(sA(sa, 1) + 32 * k), bdesc, idesc, acc);
+          if (MT == 2) mma_bf16(tmem + 256, smem_desc_sw128(sA(sa, 1) + 32 * k), bdesc, idesc, acc);
         }
         mma_commit(aempty_bar(sa));
         mma_commit(bempty_bar(sb));
@@ -186,17 +200,18 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
       }
       return v;
     };
-    RawScale next = load_scale(grp);
-    for (int t = grp; t < NT; t += Cfg::kGroups) {
-      const int sa = t % SA, sb = t % SB;
+    RawScale next = load_scale(grp < nst ? t0 + grp : NT);
+    for (int i = grp; i < nst; i += Cfg::kGroups) {
+      const int t = t0 + i;
+      const int sa = i % SA, sb = i % SB;
       const RawScale cur = next;
-      next = load_scale(t + Cfg::kGroups);
+      next = load_scale(i + Cfg::kGroups < nst ? t + Cfg::kGroups : NT);
       const float sc = !cur.ok ? 0.f
                      : (sv.double_quant ? __fmaf_rn(static_cast<float>(cur.q), cur.s, off) : cur.s);
       RowTable<CODE> T;
       build_table<CODE, DT>(T, sc, C);
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bempty_bar(sb), ((t / SB) & 1) ^ 1, abort) &&
-                                       mbar_wait(full_bar(sa), (t / SA) & 1, abort)))
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bempty_bar(sb), ((i / SB) & 1) ^ 1, abort) &&
+                                       mbar_wait(full_bar(sa), (i / SA) & 1, abort)))
         break;
       if (active) {
         // packed row r: BN / 2 bytes, of which this block is the 16-byte
@@ -222,9 +237,30 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
       __syncwarp();
       if (lane == 0) mbar_arrive(bfull_bar(sb));
     }
-    if (warp < 18 && __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
+    if (S == 1 && warp < 18 && __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort))) {
       tc_fence_after();
-      store_accumulators<BN, DT>(tmem, warp, lane, dX, M, K, m0, k0);
+      store_accumulators<BN, DT, MT>(tmem, warp, lane, dX, M, K, m0, k0);
+    }
+  }
+  if constexpr (MT == 1 && BN % 32 == 0) if (S > 1) {
+    // split of the contraction: every thread of the cluster passes both
+    // barriers (as in the forward kernel)
+    __syncwarp();
+    const bool epi = warp >= 2 && warp < 18;
+    bool ok = true;
+    if (epi) ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0, abort));
+    tc_fence_before();
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (epi && ok && rank > 0) {
+      tc_fence_after();
+      send_partials<BN>(tmem, warp, lane, base, rank);
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (epi && ok && rank == 0) {
+      tc_fence_after();
+      store_split_sum<BN, DT>(tmem, warp, lane, base, S, dX, M, K, m0, k0);
     }
   }
   tc_fence_before();
@@ -258,11 +294,11 @@ inline int gemm_dx_pick_bn(int64_t M, int64_t K, int sms) {
   return best;
 }
 
-template <int CODE, int BN, int DT>
+template <int CODE, int BN, int DT, int MT = 2>
 inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* wq,
                                      const ScaleView& sv, const CodeValues& C, int64_t M,
-                                     void* dX, cudaStream_t stream) {
-  using Cfg = GemmDxCfg<BN>;
+                                     void* dX, cudaStream_t stream, int sms) {
+  using Cfg = GemmDxCfg<BN, MT>;
   const int64_t N = wq->rows, K = wq->cols;
   EncodeTiledFn enc = encode_tiled_fn();
   CUtensorMap tw;
@@ -289,7 +325,7 @@ inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* 
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(gemm_dx_kernel<CODE, BN, DT>,
+      st = cuda_check(cudaFuncSetAttribute(gemm_dx_kernel<CODE, BN, DT, MT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(Cfg::kSmem)),
                       "cudaFuncSetAttribute (dX GEMM)");
@@ -297,21 +333,35 @@ inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* 
       attr_set[dev] = true;
     }
   }
+  const int64_t tiles = ((K + BN - 1) / BN) * ((M + MT * kGemmBM - 1) / (MT * kGemmBM));
+  const int S = (MT == 1 && BN % 32 == 0)
+                    ? gemm_split_k(tiles, (N + kDxRows - 1) / kDxRows, sms) : 1;
   dim3 grid(static_cast<unsigned>((K + BN - 1) / BN),
-            static_cast<unsigned>((M + 2 * kGemmBM - 1) / (2 * kGemmBM)));
-  return launch("gemm_dx_kernel", gemm_dx_kernel<CODE, BN, DT>, grid, dim3(Cfg::kThreads),
-                Cfg::kSmem, stream, nullptr, 0, tdy, tw, sv, static_cast<uint16_t*>(dX),
-                static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), C);
+            static_cast<unsigned>((M + MT * kGemmBM - 1) / (MT * kGemmBM)),
+            static_cast<unsigned>(S));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = static_cast<unsigned>(S);
+  return launch("gemm_dx_kernel", gemm_dx_kernel<CODE, BN, DT, MT>, grid, dim3(Cfg::kThreads),
+                Cfg::kSmem, stream, attr, S > 1 ? 1u : 0u, tdy, tw, sv,
+                static_cast<uint16_t*>(dX), static_cast<int>(M), static_cast<int>(N),
+                static_cast<int>(K), C);
 }
 
 template <int CODE, int DT>
 inline nf4q_status gemm_dx_launch_code(const CUtensorMap& tdy, const nf4q_weight* wq,
                                        const ScaleView& sv, const CodeValues& C, int64_t M,
-                                       void* dX, cudaStream_t stream, int bn) {
+                                       void* dX, cudaStream_t stream, int bn, int sms) {
+  // 128 x 128 tiles with one accumulator (then the split) when they fit one
+  // wave: at M = 256 on a 4096-column weight 64 CTAs x 2 instead of 16
+  const int64_t t1 = ((M + kGemmBM - 1) / kGemmBM) * ((wq->cols + 127) / 128);
+  if (t1 <= sms) return gemm_dx_launch_bn<CODE, 128, DT, 1>(tdy, wq, sv, C, M, dX, stream, sms);
   switch (bn) {
-    case 192: return gemm_dx_launch_bn<CODE, 192, DT>(tdy, wq, sv, C, M, dX, stream);
-    case 128: return gemm_dx_launch_bn<CODE, 128, DT>(tdy, wq, sv, C, M, dX, stream);
-    default: return gemm_dx_launch_bn<CODE, 256, DT>(tdy, wq, sv, C, M, dX, stream);
+    case 192: return gemm_dx_launch_bn<CODE, 192, DT>(tdy, wq, sv, C, M, dX, stream, sms);
+    case 128: return gemm_dx_launch_bn<CODE, 128, DT>(tdy, wq, sv, C, M, dX, stream, sms);
+    default: return gemm_dx_launch_bn<CODE, 256, DT>(tdy, wq, sv, C, M, dX, stream, sms);
   }
 }
 
@@ -341,10 +391,10 @@ inline nf4q_status gemm_dx_launch(const nf4q_weight* wq, const ScaleView& sv,
   if (st != NF4Q_OK) return st;
   const int bn = gemm_dx_pick_bn(M, K, sms);
   if (dt == 0)
-    return wq->code == 0 ? gemm_dx_launch_code<0, 0>(tdy, wq, sv, C, M, dX, stream, bn)
-                         : gemm_dx_launch_code<1, 0>(tdy, wq, sv, C, M, dX, stream, bn);
-  return wq->code == 0 ? gemm_dx_launch_code<0, 1>(tdy, wq, sv, C, M, dX, stream, bn)
-                       : gemm_dx_launch_code<1, 1>(tdy, wq, sv, C, M, dX, stream, bn);
+    return wq->code == 0 ? gemm_dx_launch_code<0, 0>(tdy, wq, sv, C, M, dX, stream, bn, sms)
+                         : gemm_dx_launch_code<1, 0>(tdy, wq, sv, C, M, dX, stream, bn, sms);
+  return wq->code == 0 ? gemm_dx_launch_code<0, 1>(tdy, wq, sv, C, M, dX, stream, bn, sms)
+                       : gemm_dx_launch_code<1, 1>(tdy, wq, sv, C, M, dX, stream, bn, sms);
 }
 
 }  // namespace nf4q

@@ -44,7 +44,10 @@ def check_dx(dx_bits, dy_bits, what_bits, what="", dtype=o.DT_BF16):
 # each tile width (128 for the small ones, 256 for 2048 x 256 x 4096, 192
 # for 3000 x 136 x 4096).
 SHAPES = [(1, 64, 64), (5, 200, 320), (64, 256, 256), (300, 1000, 1024), (129, 136, 4160),
-          (513, 512, 512), (2048, 256, 4096), (3000, 136, 4096)]
+          (513, 512, 512), (2048, 256, 4096), (3000, 136, 4096),
+          # the contraction split over a cluster: S = 4 over 65 stages (ragged
+          # last stage) and over 37 stages, one-accumulator tiles
+          (200, 4160, 320), (77, 2368, 960)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
