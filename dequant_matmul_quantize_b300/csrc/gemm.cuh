@@ -572,26 +572,32 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
                 static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), C);
 }
 
-// BN of a one-accumulator launch (M <= 128).  Each CTA rebuilds BN weight
-// rows per k-step, so within one wave the time grows with BN: the smallest
-// candidate whose tiles fit the SMs.  Weights narrow enough for the K split
-// (at most half the SMs' worth of 128-wide tiles) keep BN = 128 and split.
-inline int gemm_pick_bn1(int64_t N, int sms) {
-  if ((N + 127) / 128 * 2 <= sms) return 128;
+// BN of a one-accumulator launch (128-row tiles, mt of them along M), or 0
+// when no width fits one wave.  Each CTA rebuilds BN weight rows per
+// k-step, so within one wave the time grows with BN: the smallest candidate
+// whose tiles fit the SMs.  Weights narrow enough for the K split (at most
+// half the SMs' worth of 128-wide tiles) keep BN = 128 and split.
+inline int gemm_pick_bn1(int64_t mt, int64_t N, int sms) {
+  if (mt * ((N + 127) / 128) * 2 <= sms) return 128;
   const int cands[6] = {80, 112, 128, 160, 208, 256};
   for (int bn : cands)
-    if ((N + bn - 1) / bn <= sms) return bn;
-  return 128;
+    if (mt * ((N + bn - 1) / bn) <= sms) return bn;
+  return 0;
 }
 
 template <int CODE, int DT>
 inline nf4q_status gemm_launch_code(const CUtensorMap& tx, const nf4q_weight* wq,
                                     const ScaleView& sv, const CodeValues& C, int64_t M, void* Y,
                                     cudaStream_t stream, int bn, int sms) {
-  // M <= 128: one accumulator per CTA, with the deeper TMA ring the smaller
-  // stages allow, and W tiles as narrow as one wave allows
-  if (M <= kGemmBM) {
-    switch (gemm_pick_bn1(wq->rows, sms)) {
+  // One accumulator per CTA (128-row tiles, with the deeper TMA ring the
+  // smaller stages allow, W tiles as narrow as one wave allows) whenever
+  // such tiles fit one wave: for M <= 128 always (several waves of 128-wide
+  // tiles otherwise), above that while they give more CTAs than 256-row
+  // tiles do (M = 256 on a 14336-row weight: 138 CTAs instead of 64)
+  const int64_t mt1 = (M + kGemmBM - 1) / kGemmBM;
+  const int bn1 = gemm_pick_bn1(mt1, wq->rows, sms);
+  if (M <= kGemmBM || bn1 != 0) {
+    switch (bn1) {
       case 80: return gemm_launch_bn<CODE, 80, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
       case 112: return gemm_launch_bn<CODE, 112, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
       case 160: return gemm_launch_bn<CODE, 160, DT, 1>(tx, wq, sv, C, M, Y, stream, sms);
