@@ -20,6 +20,8 @@ Each case builds its seeded synthetic input, runs the library call twice
     gemm2048     nf4q_gemm M=2048 on the 14336x4096 prefill weight
     gemm64       nf4q_gemm M=64 on the 14336x4096 prefill weight
     dx2048       nf4q_matmul_dx M=2048 on the 14336x4096 prefill weight
+    dx256        nf4q_matmul_dx M=256 on the same weight (128-row tiles, the
+                 contraction split over a 2-CTA cluster)
     int8_m1      nf4q_int8_quantize_weight, then nf4q_int8_matmul M=1 and
                  M=16, on the fp16 28672x8192 weight (LLM.int8())
 
@@ -99,14 +101,15 @@ def _run(case: str, torch, nq, synth) -> None:
         y = torch.empty(M, qw.rows, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
             ok(L.nf4q_gemm(R(s), x.data_ptr(), M, y.data_ptr(), sp), "gemm")
-    elif case == "dx2048":
+    elif case in ("dx2048", "dx256"):
+        Md = 2048 if case == "dx2048" else 256
         qw = nq.quantize(synth.prefill_weight(device=dev))
         s = qw.struct()
         N, K = qw.rows, qw.cols
-        dy = synth.activations(2048, N, seed=2048 + N, device=dev)
-        dx = torch.empty(2048, K, dtype=torch.bfloat16, device=dev)
+        dy = synth.activations(Md, N, seed=Md + N, device=dev)
+        dx = torch.empty(Md, K, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
-            ok(L.nf4q_matmul_dx(R(s), dy.data_ptr(), N, 2048, dx.data_ptr(), sp), "matmul_dx")
+            ok(L.nf4q_matmul_dx(R(s), dy.data_ptr(), N, Md, dx.data_ptr(), sp), "matmul_dx")
     elif case == "int8_m1":
         w = synth.int8_mlp70b_weight(device=dev)
         for _ in range(2):
