@@ -391,13 +391,7 @@ def run_ours(args):
         "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "ms_per_step_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1, "bytes_per_step": token_bytes,
-                   "gemv_launches_per_step": launches,
-                   "groups": "per layer: q/k/v sharing one x (nf4q_gemv_multi), o, gate/up "
-                             "sharing one x (nf4q_gemv_multi), down",
-                   "l2": "not flushed: the 3.61 GB of weights per step exceed L2 (126 MB)",
-                   "launch": "the launches captured once in a CUDA graph, replayed per step",
-                   "parallelism": f"replicas x{world}"},
+        "config": token_config(world),
         "roofline": roofline,
         "gemv_by_group": by_type,
         "gpu_launches": launches * args.steps,
@@ -922,6 +916,31 @@ def _prefill_w_hat_spawned():
         return pool.map(_prefill_w_hat, [0])[0]
 
 
+def token_bytes_per_step() -> int:
+    """Algorithmic bytes of one decode token: per launch the packed codes,
+    int8 scale codes, scale2 and offset of each weight, its y, and x once."""
+    import synth
+    shapes = [(n, k) for _, n, k in synth.LLAMA3_8B_LAYER]
+    per_layer = 0
+    for _, mids in GROUPS:
+        per_layer += sum(nbytes_state(shapes[m][0] * shapes[m][1]) + 2 * shapes[m][0]
+                         for m in mids) + 2 * shapes[mids[0]][1]
+    return per_layer * synth.LLAMA3_8B_LAYERS
+
+
+def token_config(world: int) -> dict:
+    """The workload both arms report (the reference arm times a bounded
+    sample of it, named in its cpu_baseline)."""
+    import synth
+    return {"workload": WORKLOAD, "M": 1, "bytes_per_step": token_bytes_per_step(),
+            "gemv_launches_per_step": len(GROUPS) * synth.LLAMA3_8B_LAYERS,
+            "groups": "per layer: q/k/v sharing one x (nf4q_gemv_multi), o, gate/up "
+                      "sharing one x (nf4q_gemv_multi), down",
+            "l2": "not flushed: the 3.61 GB of weights per step exceed L2 (126 MB)",
+            "launch": "the launches captured once in a CUDA graph, replayed per step",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     rank, world, _ = rank_env()
     if rank != 0:
@@ -958,7 +977,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1, "parallelism": "CPU oracle, rank 0 only"},
+        "config": token_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
