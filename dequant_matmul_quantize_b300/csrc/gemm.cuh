@@ -458,7 +458,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       store_accumulators<BN, DT, MT>(tmem, warp, lane, Y, M, N, m0, n0);
     }
   }
-  if constexpr (MT == 1 && BN % 32 == 0) if (S > 1) {
+  if constexpr (MT == 1 && BN % 32 == 0) {
+   if (S > 1) {
     // split K: every thread of the cluster passes both barriers
     __syncwarp();
     const bool epi = warp >= 2 && warp < 18;
@@ -477,6 +478,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
       tc_fence_after();
       store_split_sum<BN, DT>(tmem, warp, lane, base, S, Y, M, N, m0, n0);
     }
+   }
   }
   tc_fence_before();
   __syncthreads();
@@ -513,12 +515,16 @@ inline int gemm_pick_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-// K split of a one-accumulator launch (M <= 128): the largest S <= 4 with
-// S x tiles CTAs in one wave and at least 8 k-steps per CTA.  The partials
-// of ranks 1 .. 3 (64 KB each) fit in rank 0's idle TMA and B rings.
-inline int gemm_split_k(int64_t tiles, int64_t kt, int sms) {
+// K split of a one-accumulator launch: the largest S <= 4 with S x tiles
+// CTAs in one wave, at least 8 k-steps per CTA, and the fp32 partials of
+// ranks 1 .. S-1 (partial_bytes each) within rank 0's idle rings
+// (room_bytes, everything below the barrier area).
+inline int gemm_split_k(int64_t tiles, int64_t kt, int sms, int64_t partial_bytes,
+                        int64_t room_bytes) {
   int S = 1;
-  while (S < 4 && tiles * (S + 1) <= sms && kt / (S + 1) >= 8) ++S;
+  while (S < 4 && tiles * (S + 1) <= sms && kt / (S + 1) >= 8 &&
+         S * partial_bytes <= room_bytes)
+    ++S;
   return S;
 }
 
@@ -558,7 +564,11 @@ inline nf4q_status gemm_launch_bn(const CUtensorMap& tx, const nf4q_weight* wq, 
     }
   }
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + MT * kGemmBM - 1) / (MT * kGemmBM));
-  const int S = (MT == 1 && BN % 32 == 0) ? gemm_split_k(tiles, K / kGemmBK, sms) : 1;
+  const int S = (MT == 1 && BN % 32 == 0)
+                    ? gemm_split_k(tiles, K / kGemmBK, sms, int64_t{kGemmBM} * BN * 4,
+                                   int64_t{Cfg::kAStages} * Cfg::kAStage +
+                                       int64_t{Cfg::kBStages} * Cfg::kBTile)
+                    : 1;
   dim3 grid(static_cast<unsigned>((N + BN - 1) / BN),
             static_cast<unsigned>((M + MT * kGemmBM - 1) / (MT * kGemmBM)),
             static_cast<unsigned>(S));

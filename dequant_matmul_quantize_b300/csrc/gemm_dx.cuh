@@ -242,7 +242,8 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
       store_accumulators<BN, DT, MT>(tmem, warp, lane, dX, M, K, m0, k0);
     }
   }
-  if constexpr (MT == 1 && BN % 32 == 0) if (S > 1) {
+  if constexpr (MT == 1 && BN % 32 == 0) {
+   if (S > 1) {
     // split of the contraction: every thread of the cluster passes both
     // barriers (as in the forward kernel)
     __syncwarp();
@@ -262,6 +263,7 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
       tc_fence_after();
       store_split_sum<BN, DT>(tmem, warp, lane, base, S, dX, M, K, m0, k0);
     }
+   }
   }
   tc_fence_before();
   __syncthreads();
@@ -335,7 +337,11 @@ inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* 
   }
   const int64_t tiles = ((K + BN - 1) / BN) * ((M + MT * kGemmBM - 1) / (MT * kGemmBM));
   const int S = (MT == 1 && BN % 32 == 0)
-                    ? gemm_split_k(tiles, (N + kDxRows - 1) / kDxRows, sms) : 1;
+                    ? gemm_split_k(tiles, (N + kDxRows - 1) / kDxRows, sms,
+                                   int64_t{kGemmBM} * BN * 4,
+                                   int64_t{Cfg::kAStages} * Cfg::kAStage +
+                                       int64_t{Cfg::kBStages} * Cfg::kBTile)
+                    : 1;
   dim3 grid(static_cast<unsigned>((K + BN - 1) / BN),
             static_cast<unsigned>((M + MT * kGemmBM - 1) / (MT * kGemmBM)),
             static_cast<unsigned>(S));

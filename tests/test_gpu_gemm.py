@@ -83,6 +83,28 @@ def test_gemm_split_k_configs(code, dq, dt):
         check_matmul(bf16_bits(y1), bf16_bits(x), what, f"split {code} dq={dq}")
 
 
+@pytest.mark.parametrize("code,dq,dt", [("fp4", True, "bf16"), ("nf4", False, "f16")])
+def test_gemm_narrow_tiles_configs(code, dq, dt):
+    """One-wave narrow W tiles (BN = 80 for 11008 rows) with FP4, without
+    double quantization and with fp16; and 128-row tiles at M = 200."""
+    w = synth.normal_weight(11008, 128, 0.02, seed=23)
+    qw = nq.quantize(w.cuda(), code, dq, compute_dtype=dt)
+    ref = oracle_state(as_f32(w).reshape(-1), code, dq)
+    dt_id = o.DT_F16 if dt == "f16" else o.DT_BF16
+    what = o.dequantize(ref["packed"], ref["scales"], CODE_ID[code], dtype=dt_id).reshape(w.shape)
+    for M in (9, 200):
+        x = synth.activations(M, 128, seed=24 + M)
+        if dt == "f16":
+            x = x.to(torch.float16)
+        y = nq.gemm(qw, x.cuda())
+        if dt == "f16":
+            check_matmul(y.cpu().view(torch.int16).numpy().view(np.uint16),
+                         x.view(torch.int16).numpy().view(np.uint16), what, f"{code} M={M}",
+                         o.DT_F16)
+        else:
+            check_matmul(bf16_bits(y), bf16_bits(x), what, f"{code} dq={dq} M={M}")
+
+
 def test_gemm_matches_gemv_and_cublas():
     w = synth.normal_weight(512, 1024, 0.02, seed=8)
     qw = nq.quantize(w.cuda())
