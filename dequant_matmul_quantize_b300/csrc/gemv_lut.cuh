@@ -119,6 +119,9 @@ __device__ __forceinline__ uint4 lds128_lut(uint32_t addr) {
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
@@ -427,17 +430,21 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   }
   __syncthreads();  // table and x are complete
 
-  // 4. block scales.  Lane l computes tile row l & 15 and the BB / 2 blocks
-  //    from (BB / 2) (l >> 4) of a box and keeps them in the warp's scale
-  //    slot: float (j, r) (block j, tile row r) at word 16 j + r, the half of
-  //    the slot written by lanes 16..31 rotated by 16 words so that the two
-  //    half-warps store to different banks.  With M = 1 the slot holds
-  //    s * 2^F of the single row of x.  With K / 64 a multiple of 4 the codes
-  //    of a lane's blocks are one aligned 16- or 32-bit word and share their
-  //    scale2 (they never straddle a multiple of 256); otherwise byte loads.
-  //    The loads run two boxes ahead of their use.
+  // 4. block scales.  Lane l computes tile row r = l & 15 and the NBL = BB/2
+  //    blocks from NBL (l >> 4) of a box and keeps them in the warp's scale
+  //    slot (BB / 2 pieces, one per 128-byte line): the scales of 4
+  //    consecutive blocks cb of row r are one 16-byte group, group
+  //    ((r >> 1) + 4 (r & 1)) mod 8 of line (r & 1) + 2 cb.  So a writer
+  //    stores its 4 scales at once (BB = 8; with BB = 4 its 2, the halves of
+  //    an odd row's group swapped), and a reader loads the scales of tile
+  //    rows 2g and 2g + 1 for 4 blocks with two 16-byte loads - the eight
+  //    rows of either parity sit on distinct banks.  With M = 1 the slot
+  //    holds s * 2^F of the single row of x.  With K / 64 a multiple of 4 the
+  //    codes of a lane's blocks are one aligned 16- or 32-bit word and share
+  //    their scale2 (they never straddle a multiple of 256); otherwise byte
+  //    loads.  The loads run two boxes ahead of their use.
   constexpr int NBL = BB / 2;
-  const int srow = lane & 15, sjb = NBL * (lane >> 4);
+  const int srow = lane & 15, hw = lane >> 4, sjb = NBL * hw;
   const bool kb4 = (KB & 3) == 0;
   struct Raw {
     uint32_t q;       // NBL int8 codes (block j in byte j)
@@ -487,19 +494,26 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       }
     }
   };
-  // word offset of float (j, r) in the slot
-  auto slot_word = [](int j, int r) -> uint32_t {
-    const int idx = 16 * j + r;
-    return static_cast<uint32_t>((idx & ~31) + (((idx & 31) + 16 * (j / NBL)) & 31));
-  };
   const uint32_t slot0 = lut_piece(kLutPieceScale + (BB / 2) * warp);
-  auto slot_addr = [&](uint32_t word) { return slot0 + 256u * (word >> 5) + 4u * (word & 31); };
+  auto slot_group = [](int r) { return static_cast<uint32_t>(((r >> 1) + 4 * (r & 1)) & 7); };
+  // where this lane writes its NBL scales
+  const uint32_t slot_w =
+      slot0 + 256u * static_cast<uint32_t>((srow & 1) + (BB == 8 ? 2 * hw : 0)) +
+      16u * slot_group(srow) + (BB == 4 ? 8u * static_cast<uint32_t>(hw ^ (srow & 1)) : 0u);
+  auto slot_put = [&](const float (&v)[NBL]) {
+    if constexpr (NBL == 4)
+      sts128(slot_w, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                                __float_as_uint(v[2]), __float_as_uint(v[3])));
+    else
+      sts64(slot_w, __float_as_uint(v[0]), __float_as_uint(v[1]));
+  };
   // with M = 1 the slot holds s * 2^F of row 0 of x (the same for every lane)
   const float fs =
       M != 1 ? 1.f
              : (DT == 0 ? __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(lds32(misc))) << 23)
                         : 1.f);
   auto scale_store = [&](const Raw& r) {
+    float v[NBL];
 #pragma unroll
     for (int j = 0; j < NBL; ++j) {
       float sc = 0.f;  // rows past N and blocks past K get scale 0
@@ -507,36 +521,41 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
         sc = DQ ? __fmaf_rn(static_cast<float>(static_cast<int8_t>((r.q >> (8 * j)) & 0xFFu)),
                             r.s[j], r.off)
                 : r.s[j];
-      sts32(slot_addr(slot_word(sjb + j, srow)), __float_as_uint(sc * fs));
+      v[j] = sc * fs;
     }
+    slot_put(v);
   };
 
   // Chunked scale loads (EP: double quant with K / 64 a multiple of 16).  A
-  // chunk is 16 blocks of the tile's 16 rows: lanes 0..15 hold the 16 int8
-  // scale codes of row `lane` (one 16-byte load), lanes 16..31 the scale2 of
-  // row `lane - 16` (16 blocks aligned to 16 never straddle a 256-block
-  // group).  Chunks are loaded two ahead of the one in use, in the order the
-  // warp meets them: its units' chunks c0 .. c0 + nch - 1 of each tile.
+  // chunk is 16 blocks of the tile's 16 rows; both lanes of row r hold its
+  // 16 int8 scale codes (one 16-byte load) and its scale2 (16 blocks
+  // aligned to 16 never straddle a 256-block group).  A chunk is loaded one
+  // ahead of the one in use, in the order the warp meets them: its units'
+  // chunks c0 .. c0 + nch - 1 of each tile.  The factor 2^F (M = 1) is
+  // folded into scale2 and the offset, which is exact: s * 2^F and
+  // (q scale2 + offset) 2^F round alike.
   const int c0 = (pb0 * BB) / 16;
   const int nch = nmy > 0 ? (pb1 * BB - 1) / 16 - c0 + 1 : 0;
   float offs[kLutMaxGroup];
 #pragma unroll
   for (int i = 0; i < kLutMaxGroup; ++i)
-    offs[i] = (EP && i < G.count) ? __ldg(G.sv[i].offset) : 0.f;
-  auto chunk_load = [&](int tile, int ci) -> uint4 {
-    uint4 v = make_uint4(0, 0, 0, 0);
+    offs[i] = (EP && i < G.count) ? __ldg(G.sv[i].offset) * fs : 0.f;
+  struct Chunk {
+    uint4 q;
+    float s2;
+  };
+  auto chunk_load = [&](int tile, int ci) -> Chunk {
+    Chunk c{make_uint4(0, 0, 0, 0), 0.f};
     if (EP && tile < T) {
       const int m = mat_of(tile);
-      const int row = (tile - G.off[m]) * 16 + (lane & 15);
+      const int row = (tile - G.off[m]) * 16 + srow;
       if (row < G.N[m]) {
         const int64_t b0 = static_cast<int64_t>(row) * KB + 16 * (c0 + ci);
-        if (lane < 16)
-          v = __ldg(reinterpret_cast<const uint4*>(G.sv[m].absmax_q + b0));
-        else
-          v.x = __float_as_uint(__ldg(G.sv[m].scale2 + (b0 >> 8)));
+        c.q = __ldg(reinterpret_cast<const uint4*>(G.sv[m].absmax_q + b0));
+        c.s2 = __ldg(G.sv[m].scale2 + (b0 >> 8));
       }
     }
-    return v;
+    return c;
   };
   auto chunk_next = [&](int& tile, int& ci) {
     if (++ci == nch) {
@@ -544,44 +563,49 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       tile += tile_stride;
     }
   };
-  uint4 E0 = make_uint4(0, 0, 0, 0), E1 = E0, E2 = E0;
-  int k_tile = tile0, k_ci = 0;  // chunk held in E0
+  Chunk E0{make_uint4(0, 0, 0, 0), 0.f}, E1 = E0;
   int e_tile = tile0, e_ci = 0;  // next chunk to load
+  float s2c = 0.f, offc = 0.f;   // scale2 * 2^F and offset * 2^F of chunk E0
+  auto chunk_use = [&](int tile) {
+    float off = offs[0];
+#pragma unroll
+    for (int i = 1; i < kLutMaxGroup; ++i)
+      if (i < G.count && tile >= G.off[i]) off = offs[i];
+    offc = off;
+    s2c = E0.s2 * fs;
+  };
   if (EP && total > 0) {
     E0 = chunk_load(e_tile, e_ci);
     chunk_next(e_tile, e_ci);
     E1 = chunk_load(e_tile, e_ci);
     chunk_next(e_tile, e_ci);
-    E2 = chunk_load(e_tile, e_ci);
-    chunk_next(e_tile, e_ci);
+    chunk_use(tile0);
   }
   auto word_of = [](const uint4& v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
   };
-  // scales of box bb of `tile` into the slot, from the chunk registers
-  auto scale_store_ep = [&](int tile, int bb) {
-    const int ci = (bb * BB) / 16 - c0;
-    while (tile != k_tile || ci != k_ci) {
+  // scales of box pb0 + bi of `tile` into the slot, from the chunk
+  // registers; a box that starts a unit or a chunk moves to the next chunk
+  // (except the very first box).  An int8 code q becomes a float through
+  // the bit pattern 2^23 + (q + 128): exact.
+  auto scale_store_ep = [&](int tile, int bi, bool first) {
+    const int bb = pb0 + bi;
+    if (!first && (bi == 0 || ((bb * BB) & 15) == 0)) {
       E0 = E1;
-      E1 = E2;
-      E2 = chunk_load(e_tile, e_ci);
+      E1 = chunk_load(e_tile, e_ci);
       chunk_next(e_tile, e_ci);
-      chunk_next(k_tile, k_ci);
+      chunk_use(tile);
     }
     const int o = (bb * BB) & 15;  // first block of the box in the chunk
-    const float s2 = __uint_as_float(__shfl_sync(0xFFFFFFFFu, E0.x, 16 + (lane & 15)));
-    const uint32_t other = __shfl_sync(0xFFFFFFFFu, word_of(E0, (o + NBL) >> 2), lane & 15);
-    const uint32_t qw = lane < 16 ? word_of(E0, o >> 2) : other;
-    const int sh = 8 * ((o + sjb) & 3);
-    float off = offs[0];
-#pragma unroll
-    for (int i = 1; i < kLutMaxGroup; ++i)
-      if (i < G.count && tile >= G.off[i]) off = offs[i];
+    const uint32_t qw = word_of(E0.q, (o >> 2) + (NBL == 4 ? hw : 0)) ^ 0x80808080u;
+    float v[NBL];
 #pragma unroll
     for (int j = 0; j < NBL; ++j) {
-      const float qv = static_cast<float>(static_cast<int8_t>((qw >> (sh + 8 * j)) & 0xFFu));
-      sts32(slot_addr(slot_word(sjb + j, srow)), __float_as_uint(__fmaf_rn(qv, s2, off) * fs));
+      const uint32_t sel = 0x7650u + static_cast<uint32_t>(NBL == 4 ? j : 2 * hw + j);
+      const float qv = __fsub_rn(__uint_as_float(prmt_lut(qw, 0x4B000000u, sel)), 8388736.f);
+      v[j] = __fmaf_rn(qv, s2c, offc);
     }
+    slot_put(v);
   };
 
   // 5. per-lane constants.  MMA row g is tile row 2g, MMA row g + 8 is tile
@@ -597,6 +621,9 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   const uint32_t xo1 = static_cast<uint32_t>((32 * t + 16 + 16 * mx_row) & 127);
   // table address = [lane * 4, code byte, 0x01, 0]: the table sits at 0x10000
   const uint32_t L = kLutTable | (static_cast<uint32_t>(lane) << 2);
+  // the slot groups of tile rows 2g (line 0 + 2 cb) and 2g + 1 (line 1 + 2 cb)
+  const uint32_t slot_ra = slot0 + 16u * slot_group(2 * g);
+  const uint32_t slot_rb = slot0 + 256u + 16u * slot_group(2 * g + 1);
 
   // raw scales (without EP): box q + 1 in rA, box q + 2 in rB while box q
   // is consumed
@@ -604,7 +631,7 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   int s_tile = tile0, s_bi = 0;
   if (EP) {
     if (total > 0) {
-      scale_store_ep(s_tile, pb0 + s_bi);
+      scale_store_ep(s_tile, s_bi, true);
       advance(s_tile, s_bi);
     }
   } else {
@@ -641,8 +668,13 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     const uint32_t stage = stage_addr(st);
     const uint32_t w0 = stage + SB0, w1 = stage + SB1;
     const uint32_t xbox = xrow + static_cast<uint32_t>((pb0 + c_bi) * BB * 128);
+    uint4 sva = make_uint4(0, 0, 0, 0), svb = sva;  // scales of rows 2g, 2g + 1, 4 blocks
 #pragma unroll
     for (int j = 0; j < BB; ++j) {
+      if ((j & 3) == 0) {
+        sva = lds128_lut(slot_ra + 512u * (j >> 2));
+        svb = lds128_lut(slot_rb + 512u * (j >> 2));
+      }
       const uint32_t hb = kLutBoxBytes * (j >> 2);  // second TMA box of an 8-block stage
       const uint2 wg = lds64((w0 + hb) ^ (32u * (j & 3)));
       const uint2 wh = lds64((w1 + hb) ^ (32u * (j & 3)));
@@ -671,9 +703,10 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
         else
           mma_f16_acc(d, a0, a1, a2, a3, xr[2 * i], xr[2 * i + 1]);
       }
-      // (s of tile row 2g, of row 2g + 1) for block j: adjacent words
-      const uint2 sg = lds64(slot_addr(slot_word(j, 0) + 2u * g));
-      const float sa = __uint_as_float(sg.x), sb = __uint_as_float(sg.y);
+      // s of tile rows 2g and 2g + 1 for block j (BB = 4: an odd row's
+      // group holds blocks 2, 3, 0, 1)
+      const float sa = __uint_as_float(word_of(sva, j & 3));
+      const float sb = __uint_as_float(word_of(svb, BB == 4 ? (j & 3) ^ 2 : (j & 3)));
       if (M == 1) {
         acc[0] = __fmaf_rn(d[0], sa, acc[0]);
         acc[2] = __fmaf_rn(d[2], sb, acc[2]);
@@ -695,7 +728,7 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     // box's); raw loads for box q + 3
     if (q + 1 < total) {
       if (EP) {
-        scale_store_ep(s_tile, pb0 + s_bi);
+        scale_store_ep(s_tile, s_bi, false);
         advance(s_tile, s_bi);
       } else {
         scale_store(rA);

@@ -577,11 +577,34 @@ int lut_box(int64_t K, int32_t M) {
   return 0;
 }
 
+int lut_parts(int64_t T, int64_t nbox, int64_t sms) {
+  int bestP = 1;
+  double best = 0.0;
+  for (int P = 1; P <= kLutWarps && P <= nbox; P *= 2) {
+    const int64_t SL = kLutWarps / P;
+    const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
+    const int64_t rounds = (T + grid * SL - 1) / (grid * SL);
+    const int64_t per = (nbox + P - 1) / P;
+    const double unit_end = P == 1 ? 0.0 : (P < kLutWarps ? 0.25 : 0.5);
+    const double cost = static_cast<double>(rounds) * (static_cast<double>(per) + unit_end);
+    if (P == 1 || cost < best - 1e-9) {
+      best = cost;
+      bestP = P;
+    }
+  }
+  return bestP;
+}
+
 // The block-scale-folded GEMV (gemv_lut.cuh) over a group of 1..4 weights
 // with the same cols, code, double quant and compute dtype, sharing x.
 // Chooses the number of K parts P a tile is split into (over P warps of a
-// CTA) by the modelled efficiency: tiles per round of the grid times boxes
-// per part.
+// CTA) by a modelled time in box-times: rounds of the grid times (boxes per
+// part + the cost of a unit's end).  With P > 1 a unit ends in a barrier of
+// the P warps and a sum of their partials in shared memory: measured at a
+// quarter of a box-time for P = 2..8 and half of one for P = 16 (which also
+// puts every warp of the CTA in lock step), against nothing for P = 1.
+// Efficiency alone (tiles per round x boxes per part) picked P = 16 on
+// 28672 x 8192, 25 % slower than P = 8.
 nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void* x, int32_t M,
                             void* const* y, cudaStream_t s) {
   nf4q_status st = gemv_lut_attr_ready();
@@ -603,21 +626,7 @@ nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void*
   for (int i = count; i <= kLutMaxGroup; ++i) G.off[i] = static_cast<int>(T);
   const int64_t nbox = (K / kBlock + bb - 1) / bb;
   const int64_t sms = sm_count();
-  int bestP = 1;
-  double best = -1.0;
-  for (int P = 1; P <= kLutWarps; P *= 2) {
-    if (P > nbox) break;
-    const int64_t SL = kLutWarps / P;
-    const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
-    const int64_t rounds = (T + grid * SL - 1) / (grid * SL);
-    const int64_t per = (nbox + P - 1) / P;
-    const double eff = static_cast<double>(T) * nbox /
-                       (static_cast<double>(sms) * kLutWarps * rounds * per);
-    if (eff > best + 1e-9) {
-      best = eff;
-      bestP = P;
-    }
-  }
+  const int bestP = lut_parts(T, nbox, sms);
   const int64_t SL = kLutWarps / bestP;
   const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
   const auto k = gemv_lut_kernel_for(wq[0]->compute_dtype == NF4Q_DT_BF16 ? 0 : 1,
