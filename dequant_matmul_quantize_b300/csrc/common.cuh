@@ -40,6 +40,14 @@ __device__ __forceinline__ float block_scale(const ScaleView& sv, int64_t b) {
   return __ldg(sv.absmax + b);
 }
 
+// Relaxed atomic add on a shared-memory word (a 32-bit shared address);
+// returns the value before the add.
+__device__ __forceinline__ uint32_t atom_add_shared(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

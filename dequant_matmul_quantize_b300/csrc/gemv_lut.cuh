@@ -35,12 +35,15 @@
 // Work split.  One CTA per SM (the table takes 64 KB), 16 warps, each with
 // its own TMA ring of boxes of 16 rows x BB 64-blocks of packed codes (BB = 8:
 // two 2 KB boxes per stage, two stages; BB = 4: one box, three stages; the
-// 128-byte swizzle).  A warp owns one 16-row tile at a time and one of P
-// parts of the K range; the P warps of a tile add their partial sums in a
-// fixed order in shared memory, so y is deterministic.  Tiles go to the CTAs
-// round robin.  One launch may cover up to four weights that share x and
-// K (a group: q, k and v of an attention block; gate and up of an MLP):
-// their tiles are numbered one after the other.
+// 128-byte swizzle).  Each CTA takes a contiguous range of 16-row tiles (the
+// ranges differ by at most one tile), and its boxes, in row-major order over
+// those tiles, are cut into equal contiguous runs, one per warp: every warp
+// streams ceil or floor of the CTA's boxes / 16, with no barrier between
+// warps.  A tile whose boxes fall to several warps is finished by the last
+// of them to arrive (a shared-memory counter), which adds the partial sums
+// in warp order, so y is deterministic.  One launch may cover up to four
+// weights that share x and K (a group: q, k and v of an attention block;
+// gate and up of an MLP): their tiles are numbered one after the other.
 #pragma once
 
 #include "common.cuh"
@@ -80,7 +83,7 @@ __device__ __forceinline__ uint32_t lut_piece(int p) { return kLutTable + 256u *
 constexpr int kLutPieceBars = 0;    // per warp 32 B (up to 3 stages x 8 B)     (4 pieces)
 constexpr int kLutPieceScale = 4;   // per warp BB * 16 floats (BB / 2 pieces)  (<= 64)
 constexpr int kLutPieceRed = 68;    // per warp 2 x 512 B                       (128 pieces)
-constexpr int kLutPieceMisc = 196;  // F factors, reduction scratch             (5 pieces)
+constexpr int kLutPieceMisc = 196;  // F factors, tile counters, scratch       (5 pieces)
 
 // fp16 bits of the 16 code values, built on the host.
 struct __align__(16) HalfCodes {
@@ -190,14 +193,13 @@ __device__ __forceinline__ uint32_t lut_x_addr(uint32_t xbase, int kbx, int m, i
 
 // Launch: grid <= SM count, 512 threads, kLutSmemTop bytes of dynamic shared
 // memory (the layout uses absolute shared addresses and checks that the
-// dynamic area starts below kLutMaxBase).  P = parts of K (1, 2, 4, 8 or 16,
-// at most the boxes of a row), kbx = 64-blocks of staged x per row (a
-// multiple of BB, >= K/64).  Requires M <= 8 and M * kbx * 128 <= the x room
+// dynamic area starts below kLutMaxBase).  kbx = 64-blocks of staged x per
+// row (a multiple of BB, >= K/64).  Requires M <= 8 and M * kbx * 128 <= the x room
 // of BB.  Launched as a programmatic dependent of the previous kernel.
 template <int DT, bool DQ, int BB, bool EP, bool M1>
 __global__ void __launch_bounds__(kLutThreads, 1)
 gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__ x, int K,
-                int M_arg, int P, int kbx, const __grid_constant__ HalfCodes hc) {
+                int M_arg, int kbx, const __grid_constant__ HalfCodes hc) {
   const int M = M1 ? 1 : M_arg;  // M1: compiled for a single row of x
   using Cfg = LutCfg<BB>;
   constexpr int NS = Cfg::kStages;
@@ -212,15 +214,38 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   const uint32_t xbase = kLutMaxBase;
   const int KB = K / kBlock;
   const int nbox = (KB + BB - 1) / BB;
-  const int SL = kLutWarps / P;
-  const int slot = warp / P, part = warp % P;
-  const int pb0 = part * nbox / P, pb1 = (part + 1) * nbox / P;
-  const int nmy = pb1 - pb0;
   const int T = G.off[G.count];
-  const int tile_stride = static_cast<int>(gridDim.x) * SL;
-  const int tile0 = static_cast<int>(blockIdx.x) * SL + slot;
-  const int nunits = (tile0 < T && nmy > 0) ? (T - tile0 + tile_stride - 1) / tile_stride : 0;
-  const int total = nunits * nmy;
+  // this CTA's tiles [ct0, ct1); its Bc boxes (tile-major) go to Wc warps,
+  // warp w taking boxes [w Bc / Wc, (w + 1) Bc / Wc): one box each when
+  // Bc < 16.  (The host keeps T * grid and 16 Bc below 2^31.)
+  const int ct0 = static_cast<int>(blockIdx.x) * T / static_cast<int>(gridDim.x);
+  const int ct1 = static_cast<int>(blockIdx.x + 1) * T / static_cast<int>(gridDim.x);
+  const int Bc = nbox > 0 ? (ct1 - ct0) * nbox : 0;
+  const int Wc = min(kLutWarps, Bc);
+  auto run_start = [&](int w) { return Bc >= kLutWarps ? (w * Bc) >> 4 : w; };
+  const int wb0 = warp < Wc ? run_start(warp) : 0;
+  const int total = warp < Wc ? run_start(warp + 1) - wb0 : 0;
+  const int tile0 = nbox > 0 ? ct0 + wb0 / nbox : ct0;  // first box: (tile0, bx0)
+  const int bx0 = wb0 - (tile0 - ct0) * nbox;
+  // The tiles this warp may share with others are its first and its last.
+  // For each: the first and last warps whose runs reach into it (wf, wl,
+  // found by walking from this warp), and wf's slot for it (0 if the tile
+  // is wf's first tile), packed as wf | wl << 4 | slot << 8.  All of this
+  // reads only the launch parameters, so it runs before the wait for the
+  // previous kernel.
+  auto share_of = [&](int tile) -> uint32_t {
+    const int fb = (tile - ct0) * nbox, lb = fb + nbox - 1;
+    int wf = warp, wl = warp;
+    while (wf > 0 && run_start(wf) > fb) --wf;
+    while (wl + 1 < Wc && run_start(wl + 1) <= lb) ++wl;
+    return static_cast<uint32_t>(wf | (wl << 4) | ((run_start(wf) == fb ? 0 : 1) << 8));
+  };
+  uint32_t share_first = 0, share_last = 0;
+  if (total > 0) {
+    const int tile_last = tile0 + (bx0 + total - 1) / nbox;
+    share_first = share_of(tile0);
+    share_last = tile_last == tile0 ? share_first : share_of(tile_last);
+  }
   // the weight a (group-wide) tile belongs to
   auto mat_of = [&](int tile) {
     int m = 0;
@@ -273,12 +298,12 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     for (int k = 0; k < 4; ++k) sts128(a + 16 * k, vv);
   }
 
-  // stream positions: consumer, scale loader (two boxes ahead), producer
-  // (NS boxes ahead, lane 0); each advances one box at a time
-  auto advance = [&](int& tile, int& bi) {
-    if (++bi == nmy) {
-      bi = 0;
-      tile += tile_stride;
+  // stream positions (tile, box): consumer, scale loader (one box ahead),
+  // producer (NS boxes ahead, lane 0); each advances one box at a time
+  auto advance = [&](int& tile, int& bx) {
+    if (++bx == nbox) {
+      bx = 0;
+      ++tile;
     }
   };
 
@@ -286,23 +311,67 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   // depends on finish: the weights are read-only here, and an L2 prefetch
   // is safe even if they were still being written.
   if (lane == 0) {
-    int f_tile = tile0, f_bi = 0;
+    int f_tile = tile0, f_bx = bx0;
     for (int q = 0; q < min(NS, total); ++q) {
       const int m = mat_of(f_tile);
 #pragma unroll
       for (int h = 0; h < BB / 4; ++h)
-        tma_prefetch_2d(&G.tmap[m], ((pb0 + f_bi) * (BB / 4) + h) * 128, (f_tile - G.off[m]) * 16);
-      advance(f_tile, f_bi);
+        tma_prefetch_2d(&G.tmap[m], (f_bx * (BB / 4) + h) * 128, (f_tile - G.off[m]) * 16);
+      advance(f_tile, f_bx);
     }
   }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  int p_tile = tile0, p_bi = 0;
+  int p_tile = tile0, p_bx = bx0;
   if (lane == 0) {
     for (int q = 0; q < min(NS, total); ++q) {
-      issue_at(p_tile, pb0 + p_bi, q);
-      advance(p_tile, p_bi);
+      issue_at(p_tile, p_bx, q);
+      advance(p_tile, p_bx);
     }
+  }
+
+  // Chunked scale loads (EP: double quant with K / 64 a multiple of 16).  A
+  // chunk is 16 blocks of the tile's 16 rows; both lanes of row r hold its
+  // 16 int8 scale codes (one 16-byte load) and its scale2 (16 blocks
+  // aligned to 16 never straddle a 256-block group).  A chunk is loaded one
+  // ahead of the one in use, in the order the warp meets them (row-major
+  // over its run of boxes); the first two are issued here, before x is
+  // staged, so that their latency hides behind it.
+  const int nch = KB / 16;  // chunks per row
+  struct Chunk {
+    uint4 q;
+    float s2;
+  };
+  auto chunk_load = [&](int tile, int ci) -> Chunk {
+    Chunk c{make_uint4(0, 0, 0, 0), 0.f};
+    if (EP && tile < T) {
+      const int m = mat_of(tile);
+      const int row = (tile - G.off[m]) * 16 + (lane & 15);
+      if (row < G.N[m]) {
+        const int64_t b0 = static_cast<int64_t>(row) * KB + 16 * ci;
+        c.q = __ldg(reinterpret_cast<const uint4*>(G.sv[m].absmax_q + b0));
+        c.s2 = __ldg(G.sv[m].scale2 + (b0 >> 8));
+      }
+    }
+    return c;
+  };
+  auto chunk_next = [&](int& tile, int& ci) {
+    if (++ci == nch) {
+      ci = 0;
+      ++tile;
+    }
+  };
+  Chunk E0{make_uint4(0, 0, 0, 0), 0.f}, E1 = E0;
+  int e_tile = tile0, e_ci = (bx0 * BB) / 16;  // next chunk to load
+  float offs[kLutMaxGroup];  // the weights' double-quant offsets
+#pragma unroll
+  for (int i = 0; i < kLutMaxGroup; ++i)
+    offs[i] = (EP && i < G.count) ? __ldg(G.sv[i].offset) : 0.f;
+  if (EP && total > 0) {
+    E0 = chunk_load(e_tile, e_ci);
+    chunk_next(e_tile, e_ci);
+    E1 = chunk_load(e_tile, e_ci);
+    chunk_next(e_tile, e_ci);
   }
 
   // 3. x -> fp16 with a power-of-two scale per row (bf16), staged
@@ -413,6 +482,11 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       sts128(lut_x_addr(xbase, kbx, m, j, 16 * c), out);
     }
   }
+
+  // split-tile counters, one per warp (the first warp of the tile), zeroed
+  // before the barrier below
+  auto tile_ctr = [&](int w) { return misc + 64u + 4u * static_cast<uint32_t>(w); };
+  if (threadIdx.x < kLutWarps) sts32(tile_ctr(threadIdx.x), 0u);
 
   // per-lane fold factors 2^F for its D columns 2t, 2t+1
   float f0 = 0.f, f1 = 0.f;
@@ -526,46 +600,11 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     slot_put(v);
   };
 
-  // Chunked scale loads (EP: double quant with K / 64 a multiple of 16).  A
-  // chunk is 16 blocks of the tile's 16 rows; both lanes of row r hold its
-  // 16 int8 scale codes (one 16-byte load) and its scale2 (16 blocks
-  // aligned to 16 never straddle a 256-block group).  A chunk is loaded one
-  // ahead of the one in use, in the order the warp meets them: its units'
-  // chunks c0 .. c0 + nch - 1 of each tile.  The factor 2^F (M = 1) is
-  // folded into scale2 and the offset, which is exact: s * 2^F and
-  // (q scale2 + offset) 2^F round alike.
-  const int c0 = (pb0 * BB) / 16;
-  const int nch = nmy > 0 ? (pb1 * BB - 1) / 16 - c0 + 1 : 0;
-  float offs[kLutMaxGroup];
+  // The factor 2^F (M = 1) is folded into scale2 and the offsets, which is
+  // exact: s * 2^F and (q scale2 + offset) 2^F round alike.
 #pragma unroll
-  for (int i = 0; i < kLutMaxGroup; ++i)
-    offs[i] = (EP && i < G.count) ? __ldg(G.sv[i].offset) * fs : 0.f;
-  struct Chunk {
-    uint4 q;
-    float s2;
-  };
-  auto chunk_load = [&](int tile, int ci) -> Chunk {
-    Chunk c{make_uint4(0, 0, 0, 0), 0.f};
-    if (EP && tile < T) {
-      const int m = mat_of(tile);
-      const int row = (tile - G.off[m]) * 16 + srow;
-      if (row < G.N[m]) {
-        const int64_t b0 = static_cast<int64_t>(row) * KB + 16 * (c0 + ci);
-        c.q = __ldg(reinterpret_cast<const uint4*>(G.sv[m].absmax_q + b0));
-        c.s2 = __ldg(G.sv[m].scale2 + (b0 >> 8));
-      }
-    }
-    return c;
-  };
-  auto chunk_next = [&](int& tile, int& ci) {
-    if (++ci == nch) {
-      ci = 0;
-      tile += tile_stride;
-    }
-  };
-  Chunk E0{make_uint4(0, 0, 0, 0), 0.f}, E1 = E0;
-  int e_tile = tile0, e_ci = 0;  // next chunk to load
-  float s2c = 0.f, offc = 0.f;   // scale2 * 2^F and offset * 2^F of chunk E0
+  for (int i = 0; i < kLutMaxGroup; ++i) offs[i] *= fs;
+  float s2c = 0.f, offc = 0.f;  // scale2 * 2^F and offset * 2^F of chunk E0
   auto chunk_use = [&](int tile) {
     float off = offs[0];
 #pragma unroll
@@ -574,23 +613,16 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     offc = off;
     s2c = E0.s2 * fs;
   };
-  if (EP && total > 0) {
-    E0 = chunk_load(e_tile, e_ci);
-    chunk_next(e_tile, e_ci);
-    E1 = chunk_load(e_tile, e_ci);
-    chunk_next(e_tile, e_ci);
-    chunk_use(tile0);
-  }
+  if (EP && total > 0) chunk_use(tile0);
   auto word_of = [](const uint4& v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
   };
-  // scales of box pb0 + bi of `tile` into the slot, from the chunk
-  // registers; a box that starts a unit or a chunk moves to the next chunk
-  // (except the very first box).  An int8 code q becomes a float through
-  // the bit pattern 2^23 + (q + 128): exact.
-  auto scale_store_ep = [&](int tile, int bi, bool first) {
-    const int bb = pb0 + bi;
-    if (!first && (bi == 0 || ((bb * BB) & 15) == 0)) {
+  // scales of box bb of `tile` into the slot, from the chunk registers; a
+  // box that starts a chunk moves to the next chunk (except the warp's
+  // first box).  An int8 code q becomes a float through the bit pattern
+  // 2^23 + (q + 128): exact.
+  auto scale_store_ep = [&](int tile, int bb, bool first) {
+    if (!first && ((bb * BB) & 15) == 0) {
       E0 = E1;
       E1 = chunk_load(e_tile, e_ci);
       chunk_next(e_tile, e_ci);
@@ -628,25 +660,25 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   // raw scales (without EP): box q + 1 in rA, box q + 2 in rB while box q
   // is consumed
   Raw rA, rB;
-  int s_tile = tile0, s_bi = 0;
+  int s_tile = tile0, s_bx = bx0;
   if (EP) {
     if (total > 0) {
-      scale_store_ep(s_tile, s_bi, true);
-      advance(s_tile, s_bi);
+      scale_store_ep(s_tile, s_bx, true);
+      advance(s_tile, s_bx);
     }
   } else {
     if (total > 0) {
-      scale_load(s_tile, pb0 + s_bi, rA);
+      scale_load(s_tile, s_bx, rA);
       scale_store(rA);
-      advance(s_tile, s_bi);
+      advance(s_tile, s_bx);
     }
     if (total > 1) {
-      scale_load(s_tile, pb0 + s_bi, rA);
-      advance(s_tile, s_bi);
+      scale_load(s_tile, s_bx, rA);
+      advance(s_tile, s_bx);
     }
     if (total > 2) {
-      scale_load(s_tile, pb0 + s_bi, rB);
-      advance(s_tile, s_bi);
+      scale_load(s_tile, s_bx, rB);
+      advance(s_tile, s_bx);
     }
   }
 
@@ -654,7 +686,7 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   bool dead = false;
   int waited_q = -1;  // last box whose stage wait succeeded (waits go in order)
   int issued_n = min(NS, total);
-  int c_tile = tile0, c_bi = 0, u = 0;
+  int c_tile = tile0, c_bx = bx0, u_bx = bx0;  // u_bx: first box of the unit
   int st = 0;
   uint32_t ph = 0;
 
@@ -667,7 +699,7 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     }
     const uint32_t stage = stage_addr(st);
     const uint32_t w0 = stage + SB0, w1 = stage + SB1;
-    const uint32_t xbox = xrow + static_cast<uint32_t>((pb0 + c_bi) * BB * 128);
+    const uint32_t xbox = xrow + static_cast<uint32_t>(c_bx * BB * 128);
     uint4 sva = make_uint4(0, 0, 0, 0), svb = sva;  // scales of rows 2g, 2g + 1, 4 blocks
 #pragma unroll
     for (int j = 0; j < BB; ++j) {
@@ -720,22 +752,22 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     __syncwarp();
     if (lane == 0 && !dead && q + NS < total) {
       fence_proxy_async_smem();
-      issue_at(p_tile, pb0 + p_bi, st);
-      advance(p_tile, p_bi);
+      issue_at(p_tile, p_bx, st);
+      advance(p_tile, p_bx);
       ++issued_n;
     }
     // scales of the next box into the slot (every lane is done with this
     // box's); raw loads for box q + 3
     if (q + 1 < total) {
       if (EP) {
-        scale_store_ep(s_tile, s_bi, false);
-        advance(s_tile, s_bi);
+        scale_store_ep(s_tile, s_bx, false);
+        advance(s_tile, s_bx);
       } else {
         scale_store(rA);
         rA = rB;
         if (q + 3 < total) {
-          scale_load(s_tile, pb0 + s_bi, rB);
-          advance(s_tile, s_bi);
+          scale_load(s_tile, s_bx, rB);
+          advance(s_tile, s_bx);
         }
       }
     }
@@ -743,8 +775,11 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       st = 0;
       ph ^= 1u;
     }
-    // end of a unit (tile, part): reduce over the P parts and store y
-    if (++c_bi == nmy) {
+    // end of a unit (the warp's boxes of one tile): a tile the warp covers
+    // whole is stored; otherwise the partial sum goes to the warp's slot
+    // (0 for the first tile of its run, 1 for the last) and the last of the
+    // tile's warps to arrive adds the slots in warp order and stores y
+    if (c_bx == nbox - 1 || q == total - 1) {
       const int m = mat_of(c_tile);
       const int Nm = G.N[m];
       uint16_t* __restrict__ ym = G.y[m];
@@ -760,20 +795,29 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
           if (c1 < M) ym[static_cast<int64_t>(c1) * Nm + row + 1] = round_to_dt<DT>(v[3]);
         }
       };
-      if (P == 1) {
+      if (u_bx == 0 && c_bx == nbox - 1) {
         store(acc);
       } else {
         auto red_addr = [&](int w, int par, int l) {
           return lut_piece(kLutPieceRed + 8 * w + 4 * par + (l >> 3)) + 16u * (l & 7);
         };
-        sts128(red_addr(warp, u & 1, lane),
+        const uint32_t sh = c_tile == tile0 ? share_first : share_last;
+        const int wf = static_cast<int>(sh & 15u), wl = static_cast<int>((sh >> 4) & 15u);
+        // slots: every warp after wf has this tile as its first
+        auto slot_of = [&](int w) { return w > wf ? 0 : static_cast<int>(sh >> 8); };
+        sts128(red_addr(warp, c_tile == tile0 ? 0 : 1, lane),
                make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
                           __float_as_uint(acc[2]), __float_as_uint(acc[3])));
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + slot), "r"(P * 32) : "memory");
-        if (part == 0) {
+        __threadfence_block();
+        __syncwarp();
+        uint32_t before = 0;
+        if (lane == 0) before = atom_add_shared(tile_ctr(wf), 1u);
+        before = __shfl_sync(0xFFFFFFFFu, before, 0);
+        if (before == static_cast<uint32_t>(wl - wf)) {
+          __threadfence_block();
           float v[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int p = 0; p < P; ++p) {
-            const uint4 r = lds128_lut(red_addr(slot * P + p, u & 1, lane));
+          for (int w = wf; w <= wl; ++w) {
+            const uint4 r = lds128_lut(red_addr(w, slot_of(w), lane));
             v[0] += __uint_as_float(r.x);
             v[1] += __uint_as_float(r.y);
             v[2] += __uint_as_float(r.z);
@@ -783,10 +827,9 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
         }
       }
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-      c_bi = 0;
-      c_tile += tile_stride;
-      ++u;
+      u_bx = 0;
     }
+    advance(c_tile, c_bx);
   }
   // drain copies still landing (only after a wait gave up)
   if (lane == 0 && dead) {

@@ -73,15 +73,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// Release count of a stage.  The arriving warp has already used every
-// word it read from the stage (the values fed its MMAs), and shared-memory
-// accesses of a thread complete in order, so a relaxed add suffices; the
-// last arriver's proxy fence then orders the refill after all of them.
-__device__ __forceinline__ uint32_t atom_add_shared(uint32_t addr, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-  return old;
-}
 
 template <int R>
 struct GemvGeom {
@@ -268,7 +259,12 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
       }
     }
     __syncwarp();
-    if (lane == 0) {  // release the stage; the fourth warp to do so refills it
+    // Release the stage; the fourth warp to do so refills it.  The arriving
+    // warp has already used every word it read from the stage (the values
+    // fed its MMAs), and shared-memory accesses of a thread complete in
+    // order, so a relaxed add suffices; the last arriver's proxy fence then
+    // orders the refill after all of them.
+    if (lane == 0) {
       const uint32_t prev = atom_add_shared(cnt + 4 * st, 1u);
       if ((prev & (kGemvWarps - 1)) == kGemvWarps - 1 && i + stages < nmine) {
         fence_proxy_async_smem();

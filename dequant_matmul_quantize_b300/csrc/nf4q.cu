@@ -136,7 +136,7 @@ nf4q_status gemv_attr_ready() {
 
 // Opt the block-scale-folded GEMV kernels in to their shared memory (once
 // per device).
-using LutKernelFn = void (*)(LutGroup, const uint16_t*, int, int, int, int, HalfCodes);
+using LutKernelFn = void (*)(LutGroup, const uint16_t*, int, int, int, HalfCodes);
 
 // The folded-GEMV instantiation for a compute dtype, double quant, box size,
 // whether the scales are read in 16-block chunks (double quant with K / 64
@@ -577,34 +577,19 @@ int lut_box(int64_t K, int32_t M) {
   return 0;
 }
 
-int lut_parts(int64_t T, int64_t nbox, int64_t sms) {
-  int bestP = 1;
-  double best = 0.0;
-  for (int P = 1; P <= kLutWarps && P <= nbox; P *= 2) {
-    const int64_t SL = kLutWarps / P;
-    const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
-    const int64_t rounds = (T + grid * SL - 1) / (grid * SL);
-    const int64_t per = (nbox + P - 1) / P;
-    const double unit_end = P == 1 ? 0.0 : (P < kLutWarps ? 0.25 : 0.5);
-    const double cost = static_cast<double>(rounds) * (static_cast<double>(per) + unit_end);
-    if (P == 1 || cost < best - 1e-9) {
-      best = cost;
-      bestP = P;
-    }
-  }
-  return bestP;
+// The kernel numbers tiles, a CTA's boxes and its warps' runs in 32-bit
+// ints: T x grid and (tiles of the largest CTA) x (boxes per row) x 16 must
+// stay below 2^31.
+bool lut_runs_fit(int64_t T, int64_t K, int bb, int64_t grid) {
+  const int64_t nbox = (K / kBlock + bb - 1) / bb;
+  return grid > 0 && T * grid < (int64_t{1} << 31) &&
+         (T + grid - 1) / grid * nbox * kLutWarps < (int64_t{1} << 31);
 }
 
 // The block-scale-folded GEMV (gemv_lut.cuh) over a group of 1..4 weights
 // with the same cols, code, double quant and compute dtype, sharing x.
-// Chooses the number of K parts P a tile is split into (over P warps of a
-// CTA) by a modelled time in box-times: rounds of the grid times (boxes per
-// part + the cost of a unit's end).  With P > 1 a unit ends in a barrier of
-// the P warps and a sum of their partials in shared memory: measured at a
-// quarter of a box-time for P = 2..8 and half of one for P = 16 (which also
-// puts every warp of the CTA in lock step), against nothing for P = 1.
-// Efficiency alone (tiles per round x boxes per part) picked P = 16 on
-// 28672 x 8192, 25 % slower than P = 8.
+// One CTA per SM (at most one per 16-row tile); the kernel splits each
+// CTA's tiles into equal runs of boxes over its warps.
 nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void* x, int32_t M,
                             void* const* y, cudaStream_t s) {
   nf4q_status st = gemv_lut_attr_ready();
@@ -624,11 +609,8 @@ nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void*
     T += (wq[i]->rows + 15) / 16;
   }
   for (int i = count; i <= kLutMaxGroup; ++i) G.off[i] = static_cast<int>(T);
-  const int64_t nbox = (K / kBlock + bb - 1) / bb;
-  const int64_t sms = sm_count();
-  const int bestP = lut_parts(T, nbox, sms);
-  const int64_t SL = kLutWarps / bestP;
-  const int64_t grid = std::min<int64_t>(sms, (T + SL - 1) / SL);
+  const int64_t grid = std::min<int64_t>(sm_count(), T);
+  if (!lut_runs_fit(T, K, bb, grid)) return NF4Q_ERR_UNSUPPORTED;
   const auto k = gemv_lut_kernel_for(wq[0]->compute_dtype == NF4Q_DT_BF16 ? 0 : 1,
                                      wq[0]->double_quant != 0, bb, (K / kBlock) % 16 == 0,
                                      M == 1);
@@ -637,7 +619,7 @@ nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   return launch("gemv_lut_kernel", k, dim3(static_cast<unsigned>(grid)), dim3(kLutThreads),
                 kLutSmemTop, s, attr, 1, G, static_cast<const uint16_t*>(x), K,
-                static_cast<int>(M), bestP, static_cast<int>(lut_kbx(K, bb)),
+                static_cast<int>(M), static_cast<int>(lut_kbx(K, bb)),
                 half_codes(wq[0]->code));
 }
 
@@ -701,7 +683,10 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
   bool done = false;
   nf4q_status st = gemv_checks(wq, x, M, y, s, &done);
   if (st != NF4Q_OK || done) return st;
-  if (M <= NF4Q_GEMV_FOLD_MAX_M && lut_box(wq->cols, M)) return gemv_lut_launch(&wq, 1, x, M, &y, s);
+  if (M <= NF4Q_GEMV_FOLD_MAX_M && lut_box(wq->cols, M) &&
+      lut_runs_fit((wq->rows + 15) / 16, wq->cols, lut_box(wq->cols, M),
+                   std::min<int64_t>(sm_count(), (wq->rows + 15) / 16)))
+    return gemv_lut_launch(&wq, 1, x, M, &y, s);
   return gemv_exact_launch(wq, x, M, y, s);
 }
 

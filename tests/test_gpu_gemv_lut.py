@@ -7,9 +7,14 @@ fp16) instead of by w_hat = bf16(code_value * s_b); it is held to the same
 tolerance as every matmul here, |y - y_ref| <= 2e-3 * sum|x w_hat| + one ulp
 of y_ref, with y_ref the fp64 product of x and the ORACLE's w_hat.
 
-Shapes are chosen so that the launch picks each split of K over the warps of
-a CTA (P = 1, 2, 4, 8, 16), with ragged row tiles and a K that is not a
-multiple of the 256-column boxes.  The error analysis of the fold is checked
+The launch gives each CTA a contiguous range of 16-row tiles and cuts the
+CTA's boxes (16 rows x 8 or 4 blocks) into equal runs over its 16 warps; a
+tile whose boxes fall to several warps is summed by the last to arrive.
+Shapes cover every regime of that split on a 148-SM B300: fewer boxes than
+warps, one tile per CTA split over all 16 warps, runs that cross tile
+boundaries (with and without 16-block scale chunks), and group launches
+whose CTA ranges cross from one weight to the next; with ragged row tiles
+and a K that is not a multiple of the 256-column boxes.  The error analysis of the fold is checked
 on its own inputs: random activations, activations whose signs follow the
 rounding of w_hat (the sign-adversarial case, inside the tolerance because
 the mean relative bf16 rounding error is below 2e-3), and activations that
@@ -43,8 +48,10 @@ def folded(qw, x):
     return nq.gemv_multi([qw], x)[0]
 
 
-# (rows, cols) -> the split the launch picks: (37, 320) P=2, (256, 1024) P=4,
-# (129, 4160) P=16, (4000, 256) P=1, (2400, 1024) P=4, (700, 2112) P=8
+# (rows, cols): (37, 320) 3 CTAs of one box; (256, 1024) 16 CTAs, 4 boxes
+# each; (129, 4160) 9 CTAs, one tile of 17 boxes over 16 warps; (4000, 256)
+# 250 tiles of one box, 1-2 per CTA; (2400, 1024) 150 tiles, 1-2 per CTA;
+# (700, 2112) 44 tiles of 5 boxes
 SHAPES = [(37, 320), (256, 1024), (129, 4160), (4000, 256), (2400, 1024), (700, 2112)]
 
 
@@ -155,6 +162,38 @@ def test_folded_gemv_error_analysis(code):
     err = abs(ya - y_ref[0, 0])
     analytic = (2.0 ** -8 + 2.0 ** -11 + 2.0 ** -20) * bound[0, 0] + o.ulp_bf16(y_ref[0, 0])
     assert err <= analytic, (err, analytic)
+
+
+# Larger splits (148 CTAs): (1600, 8192) one tile per CTA, 16 boxes, one per
+# warp; (1600, 16384) 4-block boxes at M = 1 (x past the 8-block layout's
+# room), 64 boxes per tile, 4 per warp; (7104, 3584) three tiles of 7 boxes
+# per CTA, runs of 1-2 boxes crossing tiles, scales without chunks (K/64 =
+# 56); (7104, 5120) the same with chunked scales (K/64 = 80, 10 boxes).
+SPLITS = [(1600, 8192), (1600, 16384), (7104, 3584), (7104, 5120)]
+
+
+@pytest.mark.parametrize("shape", SPLITS)
+def test_folded_gemv_work_splits(shape):
+    w = synth.normal_weight(*shape, 0.02, seed=shape[0] + shape[1], outlier_frac=1e-3)
+    qw, w_hat = full_check(w, "nf4", True, f"split {shape}")
+    for M in (1, 2):
+        x = synth.activations(M, shape[1], seed=200 + M)
+        y = folded(qw, x.cuda())
+        check_matmul(bf16_bits(y), bf16_bits(x), w_hat, f"folded M={M} {shape}")
+
+
+def test_grouped_gemv_ranges_cross_weights():
+    """A group of 300 + 144 tiles (K = 5120): three tiles per CTA, so one
+    CTA's range and some warps' runs start in the first weight and end in
+    the second."""
+    shapes = [(4800, 5120), (2304, 5120)]
+    ws = [synth.normal_weight(n, k, 0.02, seed=80 + i) for i, (n, k) in enumerate(shapes)]
+    checked = [full_check(w, "nf4", True, f"cross {i}") for i, w in enumerate(ws)]
+    for M in (1, 2):
+        x = synth.activations(M, 5120, seed=83 + M)
+        ys = nq.gemv_multi([q for q, _ in checked], x.cuda())
+        for (qw, w_hat), y in zip(checked, ys):
+            check_matmul(bf16_bits(y), bf16_bits(x), w_hat, f"cross M={M}")
 
 
 def test_gemv_dispatch_by_m():
