@@ -287,15 +287,15 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     fence_proxy_async_smem();
   }
 
-  // 2. the byte-pair table: thread i writes entry i/2, replicas 16*(i&1) .. +15
-  {
-    const int e = threadIdx.x >> 1;
+  // 2. the byte-pair table: in pass k thread i writes replicas 4 (i & 7) ..
+  //    + 3 of entry 64 k + i / 8, so that each quarter-warp stores one
+  //    entry's 128 bytes (all 32 banks)
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = 64 * k + (threadIdx.x >> 3);
     const uint32_t v = static_cast<uint32_t>(hc.h[e >> 4]) |
                        (static_cast<uint32_t>(hc.h[e & 15]) << 16);
-    const uint4 vv = make_uint4(v, v, v, v);
-    const uint32_t a = kLutTable + 256u * e + 64u * (threadIdx.x & 1);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) sts128(a + 16 * k, vv);
+    sts128(kLutTable + 256u * e + 16u * (threadIdx.x & 7), make_uint4(v, v, v, v));
   }
 
   // stream positions (tile, box): consumer, scale loader (one box ahead),
