@@ -300,8 +300,9 @@ def _mm(name: str, qw: QuantizedWeight, x: torch.Tensor, out, stream):
 
 
 def gemv(qw, x, out=None, stream=None):
-    """y = x . w_hat^T for 1 <= M <= 16 (decode); for M <= 2 the block scale
-    is folded after an fp16 contraction with the code values (see nf4q.h)."""
+    """y = x . w_hat^T for 1 <= M <= 16 (decode); for M <= 6 (when x fits the
+    kernel's staging room) the block scale is folded after an fp16
+    contraction with the code values (see nf4q.h)."""
     return _mm("nf4q_gemv", qw, x, out, stream)
 
 

@@ -1,5 +1,5 @@
 """The block-scale-folded GEMV against the oracle.  nf4q_gemv takes it for
-M <= 2; nf4q_gemv_multi (here with a single weight) for M <= 8, which is
+M <= 6; nf4q_gemv_multi (here with a single weight) for M <= 8, which is
 how the tests reach it at every M.
 
 The folded kernel multiplies x by code_value * s_b (code values rounded to
@@ -197,13 +197,19 @@ def test_grouped_gemv_ranges_cross_weights():
 
 
 def test_gemv_dispatch_by_m():
-    """nf4q_gemv: the folded kernel for M <= 2, the exact one from M = 3."""
+    """nf4q_gemv: the folded kernel for M <= 6 when x fits its staging room
+    (M * K <= 30720 here), the exact one above."""
     w = synth.normal_weight(300, 1024, 0.02, seed=31)
     qw = nq.quantize(w.cuda())
-    for M in (1, 2, 3, 8, 16):
+    for M in (1, 2, 3, 6, 7, 8, 16):
         x = synth.activations(M, 1024, seed=32 + M).cuda()
-        want = folded(qw, x) if M <= 2 else nq.gemv_exact(qw, x)
+        want = folded(qw, x) if M <= 6 else nq.gemv_exact(qw, x)
         assert torch.equal(nq.gemv(qw, x), want), M
+    # x past the staging room (4 x 16384 > 30720): the exact kernel
+    w = synth.normal_weight(64, 16384, 0.02, seed=39)
+    qw = nq.quantize(w.cuda())
+    x = synth.activations(4, 16384, seed=40).cuda()
+    assert torch.equal(nq.gemv(qw, x), nq.gemv_exact(qw, x))
 
 
 def test_grouped_gemv_matches_the_oracle_per_weight():
