@@ -307,9 +307,10 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     }
   };
 
-  // The first NS boxes of each warp go to L2 while the kernels this one
-  // depends on finish: the weights are read-only here, and an L2 prefetch
-  // is safe even if they were still being written.
+  // The first NS boxes of each warp, and x, go to L2 while the kernels this
+  // one depends on finish: an L2 prefetch is safe even if the data were
+  // still being written (L2 is the point of coherence).
+  if (threadIdx.x == 0) bulk_prefetch_l2(x, static_cast<uint32_t>(M) * K * 2u);
   if (lane == 0) {
     int f_tile = tile0, f_bx = bx0;
     for (int q = 0; q < min(NS, total); ++q) {
@@ -322,6 +323,19 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // M = 1 and at most 16384 staged columns: one read of x, kept in
+  // registers (4 x 16 bytes per thread) from the maximum to the conversion.
+  // Its loads go out first, ahead of the weight stream.
+  const int n8 = K / 8;  // 16-byte groups per row
+  const bool x1 = M1 && kbx * 8 <= 4 * kLutThreads;
+  uint4 xv[4];
+  if (x1) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = threadIdx.x + r * kLutThreads;
+      xv[r] = i < n8 ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
+    }
+  }
   int p_tile = tile0, p_bx = bx0;
   if (lane == 0) {
     for (int q = 0; q < min(NS, total); ++q) {
@@ -381,18 +395,11 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     const int i = w * kLutMaxM + m;
     return lut_piece(kLutPieceMisc + 1 + i / 32) + 4u * (i % 32);
   };
-  const int n8 = K / 8;  // 16-byte groups per row
-  // M = 1 and at most 16384 staged columns: one read of x, kept in
-  // registers (4 x 16 bytes per thread) from the maximum to the conversion
-  const bool x1 = M1 && kbx * 8 <= 4 * kLutThreads;
   int F1 = 0;  // the F of the single row (x1)
   if (x1) {
-    uint4 xv[4];
     float mx = 0.f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int i = threadIdx.x + r * kLutThreads;
-      xv[r] = i < n8 ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
       const uint32_t wv[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k)
