@@ -100,6 +100,7 @@ struct __align__(64) LutGroup {
   int N[kLutMaxGroup];
   int off[kLutMaxGroup + 1];
   int count;
+  int map3d;  // 1: tmap is the 3-D view {128 bytes, rows, 128-byte columns} (K % 256 == 0)
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -270,9 +271,13 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     const uint32_t bar = bar_of(st);
     const uint32_t dst = stage_addr(st);
     mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+    if (G.map3d) {
+      tma_load_3d(dst, &G.tmap[m], 0, row0, bb * (BB / 4), bar);
+    } else {
 #pragma unroll
-    for (int h = 0; h < BB / 4; ++h)
-      tma_load_2d(dst + h * kLutBoxBytes, &G.tmap[m], (bb * (BB / 4) + h) * 128, row0, bar);
+      for (int h = 0; h < BB / 4; ++h)
+        tma_load_2d(dst + h * kLutBoxBytes, &G.tmap[m], (bb * (BB / 4) + h) * 128, row0, bar);
+    }
   };
 
   // Programmatic dependent launch: the next kernel on the stream may start
@@ -315,9 +320,13 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     int f_tile = tile0, f_bx = bx0;
     for (int q = 0; q < min(NS, total); ++q) {
       const int m = mat_of(f_tile);
+      if (G.map3d) {
+        tma_prefetch_3d(&G.tmap[m], 0, (f_tile - G.off[m]) * 16, f_bx * (BB / 4));
+      } else {
 #pragma unroll
-      for (int h = 0; h < BB / 4; ++h)
-        tma_prefetch_2d(&G.tmap[m], (f_bx * (BB / 4) + h) * 128, (f_tile - G.off[m]) * 16);
+        for (int h = 0; h < BB / 4; ++h)
+          tma_prefetch_2d(&G.tmap[m], (f_bx * (BB / 4) + h) * 128, (f_tile - G.off[m]) * 16);
+      }
       advance(f_tile, f_bx);
     }
   }

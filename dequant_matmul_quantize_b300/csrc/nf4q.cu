@@ -564,6 +564,27 @@ nf4q_status gemv_weight_map(const nf4q_weight* wq, int box_rows, CUtensorMap* tw
                   "cuTensorMapEncodeTiled (GEMV weight)");
 }
 
+// Packed weights of the folded GEMV as a 3-D view {128 bytes, rows, 128-byte
+// columns of a row} when K is a multiple of 256 (the view then covers each
+// row exactly): one copy brings a stage of 16 rows x (BB / 4) such columns,
+// laid out column after column, each the 2 KB of 16 rows in the 128-byte
+// swizzle - the layout of BB / 4 separate 2-D boxes, in one operation.
+nf4q_status gemv_lut_weight_map(const nf4q_weight* wq, int depth, CUtensorMap* tw) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cuda_fail("cuTensorMapEncodeTiled: driver entry point not found");
+  nf4q_status st = ensure_context();
+  if (st != NF4Q_OK) return st;
+  cuuint64_t dims[3] = {kGemvSeg / 2, static_cast<cuuint64_t>(wq->rows),
+                        static_cast<cuuint64_t>(wq->cols / kGemvSeg)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(wq->cols / 2), kGemvSeg / 2};
+  cuuint32_t box[3] = {kGemvSeg / 2, 16, static_cast<cuuint32_t>(depth)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return cu_check(enc(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq->packed, dims, strides, box, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE),
+                  "cuTensorMapEncodeTiled (folded GEMV weight)");
+}
+
 // Staged x of the folded GEMV: 64-blocks per row, a multiple of the box.
 int64_t lut_kbx(int64_t K, int bb) { return (K / kBlock + bb - 1) / bb * bb; }
 
@@ -599,13 +620,16 @@ nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void*
   LutGroup G;
   std::memset(&G, 0, sizeof(G));
   G.count = count;
+  G.map3d = K % kGemvSeg == 0 ? 1 : 0;
   int64_t T = 0;
   for (int i = 0; i < count; ++i) {
     G.off[i] = static_cast<int>(T);
     G.N[i] = static_cast<int>(wq[i]->rows);
     G.sv[i] = scale_view(wq[i]);
     G.y[i] = static_cast<uint16_t*>(y[i]);
-    if ((st = gemv_weight_map(wq[i], 16, &G.tmap[i])) != NF4Q_OK) return st;
+    st = G.map3d ? gemv_lut_weight_map(wq[i], bb / 4, &G.tmap[i])
+                 : gemv_weight_map(wq[i], 16, &G.tmap[i]);
+    if (st != NF4Q_OK) return st;
     T += (wq[i]->rows + 15) / 16;
   }
   for (int i = count; i <= kLutMaxGroup; ++i) G.off[i] = static_cast<int>(T);
