@@ -23,13 +23,17 @@
 namespace nf4q {
 
 
-// Layout of the double-quant workspace (cleared before pass 1).
+// Layout of the double-quant workspace (cleared before pass 1).  The exact
+// total of a * 2^55 over the in-range values (below 2^128) is kept as three
+// 43-bit chunks, each summed over the CTAs on its own: a CTA's chunk is
+// below 2^43 and there are fewer than 2^20 CTAs, so no chunk sum carries
+// out of 64 bits and the CTAs add without reading anything back.
+constexpr int kDqChunkBits = 43;
 struct DqWorkspace {
-  unsigned long long lo;   // total of a * 2^55 over in-range values,
-  unsigned long long hi;   //   low and high 64 bits
-  uint32_t out_of_range;   // some non-zero value outside [2^-32, 2^8)
-  uint32_t ticket;         // CTAs finished
-  uint32_t pad[10];
+  unsigned long long chunk[3];  // bits [0, 43), [43, 86), [86, 128) of the total, summed
+  uint32_t out_of_range;        // some non-zero value outside [2^-32, 2^8)
+  uint32_t ticket;              // CTAs finished
+  uint32_t pad[8];
 };
 static_assert(sizeof(DqWorkspace) == 64, "workspace layout");
 constexpr int kDqFixShift = 55;  // fixed point: a * 2^55
@@ -133,7 +137,9 @@ __device__ __forceinline__ bool dq_commit(DqStats st, DqWorkspace* ws) {
   const int oor = __any_sync(0xFFFFFFFFu, st.oor);
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) { s_lo[wid] = st.lo; s_hi[wid] = st.hi; s_oor[wid] = oor; }
-  __threadfence();
+  // Every thread's earlier global writes happen before the barrier, and
+  // thread 0's fence after it is cumulative: they are visible grid-wide
+  // before its ticket.
   __syncthreads();
   if (threadIdx.x == 0) {
     int any = s_oor[0];
@@ -142,8 +148,12 @@ __device__ __forceinline__ bool dq_commit(DqStats st, DqWorkspace* ws) {
       st.hi += s_hi[k] + (st.lo < s_lo[k] ? 1ull : 0ull);
       any |= s_oor[k];
     }
-    const unsigned long long old = atomicAdd(&ws->lo, st.lo);
-    atomicAdd(&ws->hi, st.hi + (old + st.lo < old ? 1ull : 0ull));
+    // the CTA's 128-bit total in three carry-free chunks (reductions whose
+    // results are not read back, then one fence before the ticket)
+    constexpr unsigned long long kMask = (1ull << kDqChunkBits) - 1ull;
+    atomicAdd(&ws->chunk[0], st.lo & kMask);
+    atomicAdd(&ws->chunk[1], ((st.lo >> kDqChunkBits) | (st.hi << (64 - kDqChunkBits))) & kMask);
+    atomicAdd(&ws->chunk[2], st.hi >> (2 * kDqChunkBits - 64));
     if (any) atomicOr(&ws->out_of_range, 1u);
     __threadfence();
     const uint32_t t = atomicAdd(&ws->ticket, 1u);
@@ -189,7 +199,7 @@ __device__ __noinline__ void dq_finalize(const float* __restrict__ absmax, int64
                                         float* __restrict__ offset) {
   __shared__ unsigned long long s_hist[256];
   __threadfence();
-  const bool oor = atomicAdd(&ws->out_of_range, 0u) != 0u;
+  const bool oor = __ldcg(&ws->out_of_range) != 0u;
   if (oor) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) s_hist[i] = 0ull;
     __syncthreads();
@@ -208,7 +218,12 @@ __device__ __noinline__ void dq_finalize(const float* __restrict__ absmax, int64
       for (int e = 1; e < 255; ++e)
         if (s_hist[e]) big_add_shifted(A, s_hist[e], e - 1);
     } else {
-      const unsigned long long lo = atomicAdd(&ws->lo, 0ull), hi = atomicAdd(&ws->hi, 0ull);
+      // the total from its three chunk sums
+      const unsigned long long c0 = __ldcg(&ws->chunk[0]), c1 = __ldcg(&ws->chunk[1]),
+                               c2 = __ldcg(&ws->chunk[2]);
+      const unsigned long long lo = c0 + (c1 << kDqChunkBits);
+      const unsigned long long hi = (c1 >> (64 - kDqChunkBits)) + (c2 << (2 * kDqChunkBits - 64)) +
+                                    (lo < c0 ? 1ull : 0ull);
       float m;
       if (dq_round_fixed(lo, hi, static_cast<uint32_t>(nb), &m)) {
         *offset = m;

@@ -234,11 +234,45 @@ quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
   __shared__ int s_dq_oor;
   if (DQ && (threadIdx.x & 3) == 0) s_dq[threadIdx.x >> 2][0] = s_dq[threadIdx.x >> 2][1] = 0ull;
   if (DQ && threadIdx.x == 0) s_dq_oor = 0;
-  for (int i = threadIdx.x; i < kLutWords; i += blockDim.x) {
-    const int e = i >> 5;
-    s_lut[2 * i] = __float_as_uint(-(P.lut_t[e] * kTwo19));
-    s_lut[2 * i + 1] = __float_as_uint(8388608.0f + static_cast<float>(P.lut_lo[e]));
-    if (CODE == 1) s_lut[2 * kLutWords + i] = __float_as_uint(static_cast<float>(P.lut_dl[e]));
+  // 16-byte stores: two pairs (same entry) per store, four steps per store.
+  // Every parameter load of the build is issued before the first store, so
+  // that their latency (the parameters are not yet cached at kernel start)
+  // is paid once.
+  static_assert(kLutWords % 4 == 0, "table stores");
+  {
+    constexpr int kPairIt = (kLutWords / 2 + kQuantThreads - 1) / kQuantThreads;
+    constexpr int kStepIt = (kLutWords / 4 + kQuantThreads - 1) / kQuantThreads;
+    float tv[kPairIt], lv[kPairIt], dv[kStepIt];
+#pragma unroll
+    for (int k = 0; k < kPairIt; ++k) {
+      const int e = min((static_cast<int>(threadIdx.x) + k * kQuantThreads) >> 4, kLutEntries - 1);
+      tv[k] = P.lut_t[e];
+      lv[k] = static_cast<float>(P.lut_lo[e]);
+    }
+#pragma unroll
+    for (int k = 0; k < kStepIt; ++k) {
+      const int e = min((static_cast<int>(threadIdx.x) + k * kQuantThreads) >> 3, kLutEntries - 1);
+      dv[k] = CODE == 1 ? static_cast<float>(P.lut_dl[e]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kPairIt; ++k) {
+      const int i = threadIdx.x + k * kQuantThreads;
+      if (i < kLutWords / 2) {
+        const uint32_t a = __float_as_uint(-(tv[k] * kTwo19));
+        const uint32_t b = __float_as_uint(8388608.0f + lv[k]);
+        reinterpret_cast<uint4*>(s_lut)[i] = make_uint4(a, b, a, b);
+      }
+    }
+    if (CODE == 1) {
+#pragma unroll
+      for (int k = 0; k < kStepIt; ++k) {
+        const int i = threadIdx.x + k * kQuantThreads;
+        if (i < kLutWords / 4) {
+          const uint32_t d = __float_as_uint(dv[k]);
+          reinterpret_cast<uint4*>(s_lut + 2 * kLutWords)[i] = make_uint4(d, d, d, d);
+        }
+      }
+    }
   }
   __syncthreads();
 
