@@ -82,7 +82,7 @@ struct LutCfg {
 __device__ __forceinline__ uint32_t lut_piece(int p) { return kLutTable + 256u * p + 128u; }
 constexpr int kLutPieceBars = 0;    // per warp 32 B (up to 3 stages x 8 B)     (4 pieces)
 constexpr int kLutPieceScale = 4;   // per warp BB * 16 floats (BB / 2 pieces)  (<= 64)
-constexpr int kLutPieceRed = 68;    // per warp 2 x 512 B                       (128 pieces)
+constexpr int kLutPieceRed = 68;    // per warp 2 partial-sum slots x 512 B     (128 pieces)
 constexpr int kLutPieceMisc = 196;  // F factors, tile counters, scratch       (5 pieces)
 
 // fp16 bits of the 16 code values, built on the host.
@@ -529,10 +529,11 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   //    an odd row's group swapped), and a reader loads the scales of tile
   //    rows 2g and 2g + 1 for 4 blocks with two 16-byte loads - the eight
   //    rows of either parity sit on distinct banks.  With M = 1 the slot
-  //    holds s * 2^F of the single row of x.  With K / 64 a multiple of 4 the
-  //    codes of a lane's blocks are one aligned 16- or 32-bit word and share
-  //    their scale2 (they never straddle a multiple of 256); otherwise byte
-  //    loads.  The loads run two boxes ahead of their use.
+  //    holds s * 2^F of the single row of x.  Without the 16-block chunks
+  //    below: with K / 64 a multiple of 4 the codes of a lane's blocks are
+  //    one aligned 16- or 32-bit word and share their scale2 (they never
+  //    straddle a multiple of 256), otherwise byte loads; the loads run two
+  //    boxes ahead of their use.
   constexpr int NBL = BB / 2;
   const int srow = lane & 15, hw = lane >> 4, sjb = NBL * hw;
   const bool kb4 = (KB & 3) == 0;
