@@ -759,14 +759,12 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       // group holds blocks 2, 3, 0, 1)
       const float sa = __uint_as_float(word_of(sva, j & 3));
       const float sb = __uint_as_float(word_of(svb, BB == 4 ? (j & 3) ^ 2 : (j & 3)));
-      if (M == 1) {
-        acc[0] = __fmaf_rn(d[0], sa, acc[0]);
-        acc[2] = __fmaf_rn(d[2], sb, acc[2]);
-      } else {
-        acc[0] = __fmaf_rn(d[0], sa * f0, acc[0]);
-        acc[1] = __fmaf_rn(d[1], sa * f1, acc[1]);
-        acc[2] = __fmaf_rn(d[2], sb * f0, acc[2]);
-        acc[3] = __fmaf_rn(d[3], sb * f1, acc[3]);
+      // (M > 1: the rows' factors 2^F are applied once, when y is stored)
+      acc[0] = __fmaf_rn(d[0], sa, acc[0]);
+      acc[2] = __fmaf_rn(d[2], sb, acc[2]);
+      if (M != 1) {
+        acc[1] = __fmaf_rn(d[1], sa, acc[1]);
+        acc[3] = __fmaf_rn(d[3], sb, acc[3]);
       }
     }
     __syncwarp();
@@ -804,15 +802,18 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       const int Nm = G.N[m];
       uint16_t* __restrict__ ym = G.y[m];
       const int row = (c_tile - G.off[m]) * 16 + 2 * g;
+      // y = the sum times 2^F of the row of x (M > 1; with M = 1 it is in
+      // the scales): a power of two, so this equals scaling every term
       auto store = [&](const float (&v)[4]) {
         const int c0 = 2 * t, c1 = 2 * t + 1;
+        const float g0 = M != 1 ? f0 : 1.f, g1 = M != 1 ? f1 : 1.f;
         if (row < Nm) {
-          if (c0 < M) ym[static_cast<int64_t>(c0) * Nm + row] = round_to_dt<DT>(v[0]);
-          if (c1 < M) ym[static_cast<int64_t>(c1) * Nm + row] = round_to_dt<DT>(v[1]);
+          if (c0 < M) ym[static_cast<int64_t>(c0) * Nm + row] = round_to_dt<DT>(v[0] * g0);
+          if (c1 < M) ym[static_cast<int64_t>(c1) * Nm + row] = round_to_dt<DT>(v[1] * g1);
         }
         if (row + 1 < Nm) {
-          if (c0 < M) ym[static_cast<int64_t>(c0) * Nm + row + 1] = round_to_dt<DT>(v[2]);
-          if (c1 < M) ym[static_cast<int64_t>(c1) * Nm + row + 1] = round_to_dt<DT>(v[3]);
+          if (c0 < M) ym[static_cast<int64_t>(c0) * Nm + row + 1] = round_to_dt<DT>(v[2] * g0);
+          if (c1 < M) ym[static_cast<int64_t>(c1) * Nm + row + 1] = round_to_dt<DT>(v[3] * g1);
         }
       };
       if (u_bx == 0 && c_bx == nbox - 1) {
