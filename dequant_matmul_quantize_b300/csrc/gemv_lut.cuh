@@ -83,6 +83,10 @@ __device__ __forceinline__ uint32_t lut_piece(int p) { return kLutTable + 256u *
 constexpr int kLutPieceBars = 0;    // per warp 32 B (up to 3 stages x 8 B)     (4 pieces)
 constexpr int kLutPieceScale = 4;   // per warp BB * 16 floats (BB / 2 pieces)  (<= 64)
 constexpr int kLutPieceRed = 68;    // per warp 2 partial-sum slots x 512 B     (128 pieces)
+// Chunk mode (M = 1, 8-block boxes, chunked scales): per warp a 16-block
+// scale slot (8 pieces, pieces 4 .. 131) and 2 partial-sum slots of 64 B
+// (one piece, 132 .. 147)
+constexpr int kLutPieceRedCm = 132;
 constexpr int kLutPieceMisc = 196;  // F factors, tile counters, scratch       (5 pieces)
 
 // fp16 bits of the 16 code values, built on the host.
@@ -585,7 +589,11 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       }
     }
   };
-  const uint32_t slot0 = lut_piece(kLutPieceScale + (BB / 2) * warp);
+  // chunk mode: the slot holds a whole 16-block chunk, written when a box
+  // starts one (every other box), and the partial sums of split tiles are
+  // the 8 rows' pairs of the single column
+  constexpr bool CM = M1 && EP && BB == 8;
+  const uint32_t slot0 = lut_piece(kLutPieceScale + (CM ? 8 : BB / 2) * warp);
   auto slot_group = [](int r) { return static_cast<uint32_t>(((r >> 1) + 4 * (r & 1)) & 7); };
   // where this lane writes its NBL scales
   const uint32_t slot_w =
@@ -656,6 +664,32 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     }
     slot_put(v);
   };
+  // chunk mode: lane (r, h) writes blocks 8h .. 8h + 7 of row r, two 16-byte
+  // groups (blocks 4c .. 4c + 3 at line (r & 1) + 2c)
+  const uint32_t slot_cm = slot0 + 256u * static_cast<uint32_t>((srow & 1) + 4 * hw) +
+                           16u * slot_group(srow);
+  auto scale_chunk_cm = [&](int tile, int bb, bool first) {
+    if (((bb * BB) & 15) != 0 && !first) return;  // second box of a chunk
+    if (!first) {
+      E0 = E1;
+      E1 = chunk_load(e_tile, e_ci);
+      chunk_next(e_tile, e_ci);
+      chunk_use(tile);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t qw = (hw ? (c ? E0.q.w : E0.q.z) : (c ? E0.q.y : E0.q.x)) ^ 0x80808080u;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float qv =
+            __fsub_rn(__uint_as_float(prmt_lut(qw, 0x4B000000u, 0x7650u + j)), 8388736.f);
+        v[j] = __fmaf_rn(qv, s2c, offc);
+      }
+      sts128(slot_cm + 512u * c, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                                           __float_as_uint(v[2]), __float_as_uint(v[3])));
+    }
+  };
 
   // 5. per-lane constants.  MMA row g is tile row 2g, MMA row g + 8 is tile
   //    row 2g + 1, so that the four rows a half-warp reads in one load sit
@@ -680,7 +714,10 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   int s_tile = tile0, s_bx = bx0;
   if (EP) {
     if (total > 0) {
-      scale_store_ep(s_tile, s_bx, true);
+      if constexpr (CM)
+        scale_chunk_cm(s_tile, s_bx, true);
+      else
+        scale_store_ep(s_tile, s_bx, true);
       advance(s_tile, s_bx);
     }
   } else {
@@ -724,8 +761,10 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
 #pragma unroll kJUnroll
     for (int j = 0; j < BB; ++j) {
       if ((j & 3) == 0) {
-        sva = lds128_lut(slot_ra + 512u * (j >> 2));
-        svb = lds128_lut(slot_rb + 512u * (j >> 2));
+        // chunk mode: the second box of a chunk reads its upper half
+        const uint32_t so = 512u * (j >> 2) + (CM ? 1024u * (c_bx & 1) : 0u);
+        sva = lds128_lut(slot_ra + so);
+        svb = lds128_lut(slot_rb + so);
       }
       const uint32_t hb = kLutBoxBytes * (j >> 2);  // second TMA box of an 8-block stage
       const uint2 wg = lds64((w0 + hb) ^ (32u * (j & 3)));
@@ -778,7 +817,10 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     // box's); raw loads for box q + 3
     if (q + 1 < total) {
       if (EP) {
-        scale_store_ep(s_tile, s_bx, false);
+        if constexpr (CM)
+          scale_chunk_cm(s_tile, s_bx, false);
+        else
+          scale_store_ep(s_tile, s_bx, false);
         advance(s_tile, s_bx);
       } else {
         scale_store(rA);
@@ -822,13 +864,23 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
         auto red_addr = [&](int w, int par, int l) {
           return lut_piece(kLutPieceRed + 8 * w + 4 * par + (l >> 3)) + 16u * (l & 7);
         };
+        // chunk mode: lane (g, 0) holds rows 2g, 2g + 1 of the one column
+        auto red_addr_cm = [&](int w, int par) {
+          return lut_piece(kLutPieceRedCm + w) + 64u * par + 8u * g;
+        };
         const uint32_t sh = c_tile == tile0 ? share_first : share_last;
         const int wf = static_cast<int>(sh & 15u), wl = static_cast<int>((sh >> 4) & 15u);
         // slots: every warp after wf has this tile as its first
         auto slot_of = [&](int w) { return w > wf ? 0 : static_cast<int>(sh >> 8); };
-        sts128(red_addr(warp, c_tile == tile0 ? 0 : 1, lane),
-               make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                          __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+        if constexpr (CM) {
+          if (t == 0)
+            sts64(red_addr_cm(warp, c_tile == tile0 ? 0 : 1), __float_as_uint(acc[0]),
+                  __float_as_uint(acc[2]));
+        } else {
+          sts128(red_addr(warp, c_tile == tile0 ? 0 : 1, lane),
+                 make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                            __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+        }
         __threadfence_block();
         __syncwarp();
         uint32_t before = 0;
@@ -837,12 +889,22 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
         if (before == static_cast<uint32_t>(wl - wf)) {
           __threadfence_block();
           float v[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int w = wf; w <= wl; ++w) {
-            const uint4 r = lds128_lut(red_addr(w, slot_of(w), lane));
-            v[0] += __uint_as_float(r.x);
-            v[1] += __uint_as_float(r.y);
-            v[2] += __uint_as_float(r.z);
-            v[3] += __uint_as_float(r.w);
+          if constexpr (CM) {
+            if (t == 0) {
+              for (int w = wf; w <= wl; ++w) {
+                const uint2 r = lds64(red_addr_cm(w, slot_of(w)));
+                v[0] += __uint_as_float(r.x);
+                v[2] += __uint_as_float(r.y);
+              }
+            }
+          } else {
+            for (int w = wf; w <= wl; ++w) {
+              const uint4 r = lds128_lut(red_addr(w, slot_of(w), lane));
+              v[0] += __uint_as_float(r.x);
+              v[1] += __uint_as_float(r.y);
+              v[2] += __uint_as_float(r.z);
+              v[3] += __uint_as_float(r.w);
+            }
           }
           store(v);
         }
