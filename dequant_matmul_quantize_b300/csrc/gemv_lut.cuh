@@ -196,11 +196,13 @@ __device__ __forceinline__ uint32_t lut_x_addr(uint32_t xbase, int kbx, int m, i
          static_cast<uint32_t>((byte + 16 * m) & 127);
 }
 
-// Launch: grid <= SM count, 512 threads, kLutSmemTop bytes of dynamic shared
-// memory (the layout uses absolute shared addresses and checks that the
-// dynamic area starts below kLutMaxBase).  kbx = 64-blocks of staged x per
-// row (a multiple of BB, >= K/64).  Requires M <= 8 and M * kbx * 128 <= the x room
-// of BB.  Launched as a programmatic dependent of the previous kernel.
+// Launch: grid = min(SM count, 16-row tiles), 512 threads, kLutSmemTop bytes
+// of dynamic shared memory (the layout uses absolute shared addresses and
+// checks that the dynamic area starts below kLutMaxBase).  kbx = 64-blocks of
+// staged x per row (a multiple of BB, >= K/64).  Requires M <= 8,
+// M * kbx * 128 <= the x room of BB, and the run arithmetic within 32 bits
+// (checked on the host).  Launched as a programmatic dependent of the
+// previous kernel.
 template <int DT, bool DQ, int BB, bool EP, bool M1>
 __global__ void __launch_bounds__(kLutThreads, 1)
 gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__ x, int K,
@@ -285,8 +287,9 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   };
 
   // Programmatic dependent launch: the next kernel on the stream may start
-  // as soon as SMs free up; this one touches no global memory before the
-  // kernels it depends on have finished (griddepcontrol.wait below).
+  // as soon as SMs free up; this one reads no global memory before the
+  // kernels it depends on have finished (griddepcontrol.wait below) - it
+  // only asks L2 to prefetch.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // 1. barriers
