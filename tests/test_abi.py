@@ -211,3 +211,16 @@ def test_binding_rejects_bad_tensors_before_any_call():
     with pytest.raises(ValueError):
         nq.int8_matmul(nq.Int8Weight(torch.empty(0), torch.empty(0), 4, 64),
                        torch.zeros(1, 64, dtype=torch.float16))
+
+
+def test_bench_traffic_digest_ignores_comments():
+    """bench.py's measured DRAM traffic is tied to the step kernel's code:
+    the digest must not move on a comment or blank-space edit, and must move
+    on a code edit."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_digest", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    src = "int f(int a) { // the sum\n  return a + 1; /* one\n more */ }\n"
+    assert b.code_of(src) == b.code_of("int f(int a) {\n\n   return a + 1;   }")
+    assert b.code_of(src) != b.code_of(src.replace("a + 1", "a + 2"))
