@@ -189,9 +189,11 @@ __device__ __forceinline__ uint32_t split_partial_addr(uint32_t base, int bn, in
          static_cast<uint32_t>((((col >> 2) ^ (r & 7)) << 4) + (col & 3) * 4);
 }
 
+// With mt accumulators per CTA (dX), rank r's accumulator a goes to partial
+// region (r - 1) mt + a + 1.
 template <int BN>
 __device__ __forceinline__ void send_partials(uint32_t tmem, int warp, int lane, uint32_t base,
-                                              uint32_t rank) {
+                                              uint32_t rank, int acc = 0, int mt = 1) {
   static_assert(BN % 32 == 0, "split K runs with whole 32-column chunks");
   const int q = warp & 3;
   if ((((warp - 2) >> 2) & 1) != 0) return;
@@ -203,7 +205,8 @@ __device__ __forceinline__ void send_partials(uint32_t tmem, int warp, int lane,
     tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col, v);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint32_t local = split_partial_addr(base, BN, static_cast<int>(rank), r, col + 4 * c);
+      const uint32_t local =
+          split_partial_addr(base, BN, (static_cast<int>(rank) - 1) * mt + acc + 1, r, col + 4 * c);
       uint32_t remote;
       asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(local));
       asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(remote),
@@ -218,7 +221,7 @@ __device__ __forceinline__ void send_partials(uint32_t tmem, int warp, int lane,
 template <int BN, int DT>
 __device__ __forceinline__ void store_split_sum(uint32_t tmem, int warp, int lane, uint32_t base,
                                                 int S, uint16_t* __restrict__ Y, int M, int ncols,
-                                                int m0, int c0) {
+                                                int m0, int c0, int acc = 0, int mt = 1) {
   const int q = warp & 3;
   if ((((warp - 2) >> 2) & 1) != 0) return;
   const int cc = ((warp - 2) >> 3) * 32;
@@ -236,7 +239,7 @@ __device__ __forceinline__ void store_split_sum(uint32_t tmem, int warp, int lan
         uint4 w;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                     : "r"(split_partial_addr(base, BN, p, r, col + 4 * c))
+                     : "r"(split_partial_addr(base, BN, (p - 1) * mt + acc + 1, r, col + 4 * c))
                      : "memory");
         v[4 * c] = __float_as_uint(__uint_as_float(v[4 * c]) + __uint_as_float(w.x));
         v[4 * c + 1] = __float_as_uint(__uint_as_float(v[4 * c + 1]) + __uint_as_float(w.y));

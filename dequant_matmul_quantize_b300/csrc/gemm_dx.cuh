@@ -66,7 +66,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
-template <int CODE, int BN, int DT, int MT>
+// SP: the split epilogue is compiled in (always with one accumulator; with
+// two only in the instantiation that splits, which keeps the others free of
+// its register pressure).
+template <int CODE, int BN, int DT, int MT, bool SP>
 __global__ void __launch_bounds__(GemmDxCfg<BN, MT>::kThreads, 1)
 gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
                const __grid_constant__ CUtensorMap tmap_w, ScaleView sv,
@@ -242,10 +245,11 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
       store_accumulators<BN, DT, MT>(tmem, warp, lane, dX, M, K, m0, k0);
     }
   }
-  if constexpr (MT == 1 && BN % 32 == 0) {
+  if constexpr (SP && BN % 32 == 0) {
    if (S > 1) {
     // split of the contraction: every thread of the cluster passes both
-    // barriers (as in the forward kernel)
+    // barriers (as in the forward kernel); with two accumulators each rank
+    // sends both (rows m0 .. m0 + 127 and m0 + 128 .. m0 + 255)
     __syncwarp();
     const bool epi = warp >= 2 && warp < 18;
     bool ok = true;
@@ -255,13 +259,18 @@ gemm_dx_kernel(const __grid_constant__ CUtensorMap tmap_dy,
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     if (epi && ok && rank > 0) {
       tc_fence_after();
-      send_partials<BN>(tmem, warp, lane, base, rank);
+#pragma unroll 1
+      for (int a = 0; a < MT; ++a)
+        send_partials<BN>(tmem + 256u * a, warp, lane, base, rank, a, MT);
     }
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     if (epi && ok && rank == 0) {
       tc_fence_after();
-      store_split_sum<BN, DT>(tmem, warp, lane, base, S, dX, M, K, m0, k0);
+#pragma unroll 1
+      for (int a = 0; a < MT; ++a)
+        store_split_sum<BN, DT>(tmem + 256u * a, warp, lane, base, S, dX, M, K,
+                                m0 + kGemmBM * a, k0, a, MT);
     }
    }
   }
@@ -296,7 +305,7 @@ inline int gemm_dx_pick_bn(int64_t M, int64_t K, int sms) {
   return best;
 }
 
-template <int CODE, int BN, int DT, int MT = 2>
+template <int CODE, int BN, int DT, int MT = 2, bool SP = (MT == 1)>
 inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* wq,
                                      const ScaleView& sv, const CodeValues& C, int64_t M,
                                      void* dX, cudaStream_t stream, int sms) {
@@ -327,7 +336,7 @@ inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* 
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev]) {
-      st = cuda_check(cudaFuncSetAttribute(gemm_dx_kernel<CODE, BN, DT, MT>,
+      st = cuda_check(cudaFuncSetAttribute(gemm_dx_kernel<CODE, BN, DT, MT, SP>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(Cfg::kSmem)),
                       "cudaFuncSetAttribute (dX GEMM)");
@@ -336,9 +345,9 @@ inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* 
     }
   }
   const int64_t tiles = ((K + BN - 1) / BN) * ((M + MT * kGemmBM - 1) / (MT * kGemmBM));
-  const int S = (MT == 1 && BN % 32 == 0)
+  const int S = (SP && BN % 32 == 0)
                     ? gemm_split_k(tiles, (N + kDxRows - 1) / kDxRows, sms,
-                                   int64_t{kGemmBM} * BN * 4,
+                                   int64_t{MT} * kGemmBM * BN * 4,
                                    int64_t{Cfg::kAStages} * Cfg::kAStage +
                                        int64_t{Cfg::kBStages} * Cfg::kBTile)
                     : 1;
@@ -350,7 +359,7 @@ inline nf4q_status gemm_dx_launch_bn(const CUtensorMap& tdy, const nf4q_weight* 
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = static_cast<unsigned>(S);
-  return launch("gemm_dx_kernel", gemm_dx_kernel<CODE, BN, DT, MT>, grid, dim3(Cfg::kThreads),
+  return launch("gemm_dx_kernel", gemm_dx_kernel<CODE, BN, DT, MT, SP>, grid, dim3(Cfg::kThreads),
                 Cfg::kSmem, stream, attr, S > 1 ? 1u : 0u, tdy, tw, sv,
                 static_cast<uint16_t*>(dX), static_cast<int>(M), static_cast<int>(N),
                 static_cast<int>(K), C);
@@ -361,8 +370,14 @@ inline nf4q_status gemm_dx_launch_code(const CUtensorMap& tdy, const nf4q_weight
                                        const ScaleView& sv, const CodeValues& C, int64_t M,
                                        void* dX, cudaStream_t stream, int bn, int sms) {
   // 128 x 128 tiles with one accumulator (then the split) when they fit one
-  // wave: at M = 256 on a 4096-column weight 64 CTAs x 2 instead of 16
+  // wave: at M = 256 on a 4096-column weight 64 CTAs x 2 instead of 16.
+  // When that wave leaves no room for a split but 256 x 128 tiles would
+  // (M = 512 on such a weight: 128 CTAs walking all rows of w_hat), the two
+  // accumulators share each dequantized tile and the split halves the walk.
   const int64_t t1 = ((M + kGemmBM - 1) / kGemmBM) * ((wq->cols + 127) / 128);
+  const int64_t t2 = ((M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * ((wq->cols + 127) / 128);
+  if (t1 <= sms && t1 * 2 > sms && t2 * 2 <= sms)
+    return gemm_dx_launch_bn<CODE, 128, DT, 2, true>(tdy, wq, sv, C, M, dX, stream, sms);
   if (t1 <= sms) return gemm_dx_launch_bn<CODE, 128, DT, 1>(tdy, wq, sv, C, M, dX, stream, sms);
   switch (bn) {
     case 192: return gemm_dx_launch_bn<CODE, 192, DT>(tdy, wq, sv, C, M, dX, stream, sms);

@@ -47,7 +47,11 @@ SHAPES = [(1, 64, 64), (5, 200, 320), (64, 256, 256), (300, 1000, 1024), (129, 1
           (513, 512, 512), (2048, 256, 4096), (3000, 136, 4096),
           # the contraction split over a cluster: S = 4 over 65 stages (ragged
           # last stage) and over 37 stages, one-accumulator tiles
-          (200, 4160, 320), (77, 2368, 960)]
+          (200, 4160, 320), (77, 2368, 960),
+          # 256-row tiles (two accumulators) split over a 2-CTA cluster: their
+          # 128-row tiles would fill one wave with no room for a split
+          # (148 SMs); ragged M and a ragged last stage
+          (500, 1024, 4096), (512, 4160, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
