@@ -15,6 +15,7 @@ Each case builds its seeded synthetic input, runs the library call twice
     layer        the same four launches for layer 0 only, twice
     gateup       nf4q_gemv_multi(gate, up) of layer 0, twice
     gemv4096     nf4q_gemv M=1 on the 4096x4096 decode weight
+    gemv4096_exact  nf4q_gemv_exact M=1 on the same weight
     gemv11008    nf4q_gemv M=1 on the 11008x4096 decode weight
     gemv70b_m16  nf4q_gemv M=16 on the 28672x8192 weight (NF4)
     gemm2048     nf4q_gemm M=2048 on the 14336x4096 prefill weight
@@ -86,13 +87,14 @@ def _run(case: str, torch, nq, synth) -> None:
         y = torch.empty(M, qw.rows, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
             ok(fn(R(s), x.data_ptr(), M, y.data_ptr(), sp), "gemv")
-    elif case in ("gemv4096", "gemv11008"):
-        w, x = synth.llama7b_decode(0 if case == "gemv4096" else 1, device=dev)
+    elif case in ("gemv4096", "gemv11008", "gemv4096_exact"):
+        w, x = synth.llama7b_decode(1 if case == "gemv11008" else 0, device=dev)
+        fn = L.nf4q_gemv_exact if case.endswith("exact") else L.nf4q_gemv
         qw = nq.quantize(w)
         s = qw.struct()
         y = torch.empty(1, qw.rows, dtype=torch.bfloat16, device=dev)
         for _ in range(2):
-            ok(L.nf4q_gemv(R(s), x.data_ptr(), 1, y.data_ptr(), sp), "gemv")
+            ok(fn(R(s), x.data_ptr(), 1, y.data_ptr(), sp), "gemv")
     elif case in ("gemm2048", "gemm64"):
         M = 2048 if case == "gemm2048" else 64
         qw = nq.quantize(synth.prefill_weight(device=dev))
