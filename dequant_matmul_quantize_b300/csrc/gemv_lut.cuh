@@ -774,8 +774,12 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
       const uint2 wh = lds64((w1 + hb) ^ (32u * (j & 3)));
       // x: values 16t .. 16t+15 of block j of row g; lanes whose column
       // g is past M load nothing (their outputs are never stored), so a
-      // load moves only the M rows' bytes
-      uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+      // load moves only the M rows' bytes, and their B registers keep
+      // whatever they hold (they feed only D columns that are never read:
+      // no zero fill)
+      uint4 xa, xb;
+      asm("" : "=r"(xa.x), "=r"(xa.y), "=r"(xa.z), "=r"(xa.w), "=r"(xb.x), "=r"(xb.y), "=r"(xb.z),
+               "=r"(xb.w));
       if (g < M) {
         xa = lds128_lut(xbox + 128u * j + xo0);
         xb = lds128_lut(xbox + 128u * j + xo1);
