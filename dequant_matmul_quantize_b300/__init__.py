@@ -31,6 +31,7 @@ IN_F32, IN_BF16, IN_F16 = 0, 1, 2
 DTYPES = {"bf16": 0, "f16": 1}          # compute dtype codes of nf4q_weight
 BLOCKSIZE, DQ_BLOCKSIZE = 64, 256
 GEMV_MAX_M = 16
+GEMV_WEIGHTS_STATIC = 1                  # nf4q_gemv_multi_ex flag (nf4q.h)
 
 STATUS = {
     0: "NF4Q_OK", 1: "NF4Q_ERR_INVALID_ARG", 2: "NF4Q_ERR_ALIGNMENT",
@@ -117,6 +118,8 @@ def lib() -> ctypes.CDLL:
         "nf4q_gemv_exact": (i32, [W, vp, i32, vp, vp]),
         "nf4q_gemv_multi": (i32, [ctypes.POINTER(W), i32, vp, i32,
                                   ctypes.POINTER(vp), vp]),
+        "nf4q_gemv_multi_ex": (i32, [ctypes.POINTER(W), i32, vp, i32,
+                                     ctypes.POINTER(vp), i32, vp]),
         "nf4q_gemm": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul": (i32, [W, vp, i64, vp, vp]),
         "nf4q_matmul_dx": (i32, [W, vp, i64, i64, vp, vp]),
@@ -306,9 +309,13 @@ def gemv(qw, x, out=None, stream=None):
     return _mm("nf4q_gemv", qw, x, out, stream)
 
 
-def gemv_multi(qws, x, outs=None, stream=None):
+def gemv_multi(qws, x, outs=None, stream=None, static_weights=False):
     """y_i = x . w_hat_i^T for a group of 1..4 weights sharing x (same cols,
-    code, double quant and compute dtype), in one launch where possible."""
+    code, double quant and compute dtype), in one launch where possible.
+    static_weights: the caller guarantees that no kernel still running when
+    this one starts writes the weights (true for weights quantized once and
+    reused); their first tiles then load before the wait for the preceding
+    kernel (nf4q_gemv_multi_ex with NF4Q_GEMV_WEIGHTS_STATIC; same results)."""
     _require(1 <= len(qws) <= 4, "a group has 1 to 4 weights")
     _require(x.is_cuda and x.dtype == qws[0].torch_dtype and x.is_contiguous() and x.dim() == 2,
              "x must be a contiguous 2-D CUDA tensor of the compute dtype")
@@ -319,8 +326,9 @@ def gemv_multi(qws, x, outs=None, stream=None):
     structs = [q.struct() for q in qws]
     ptrs = (ctypes.POINTER(NF4QWeight) * len(qws))(*[ctypes.pointer(st) for st in structs])
     ys = (ctypes.c_void_p * len(qws))(*[_ptr(o) for o in outs])
-    _check("nf4q_gemv_multi", lib().nf4q_gemv_multi(ptrs, len(qws), _ptr(x), M, ys,
-                                                     _stream(stream)))
+    flags = GEMV_WEIGHTS_STATIC if static_weights else 0
+    _check("nf4q_gemv_multi_ex", lib().nf4q_gemv_multi_ex(ptrs, len(qws), _ptr(x), M, ys, flags,
+                                                           _stream(stream)))
     return outs
 
 

@@ -202,11 +202,13 @@ __device__ __forceinline__ uint32_t lut_x_addr(uint32_t xbase, int kbx, int m, i
 // staged x per row (a multiple of BB, >= K/64).  Requires M <= 8,
 // M * kbx * 128 <= the x room of BB, and the run arithmetic within 32 bits
 // (checked on the host).  Launched as a programmatic dependent of the
-// previous kernel.
+// previous kernel.  early != 0: the caller guarantees that no kernel still
+// running when this one starts writes the weights or their scales, so
+// their first stages are loaded before the wait for that kernel.
 template <int DT, bool DQ, int BB, bool EP, bool M1>
 __global__ void __launch_bounds__(kLutThreads, 1)
 gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__ x, int K,
-                int M_arg, int kbx, const __grid_constant__ HalfCodes hc) {
+                int M_arg, int kbx, const __grid_constant__ HalfCodes hc, int early) {
   const int M = M1 ? 1 : M_arg;  // M1: compiled for a single row of x
   using Cfg = LutCfg<BB>;
   constexpr int NS = Cfg::kStages;
@@ -319,11 +321,12 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     }
   };
 
-  // The first NS boxes of each warp, and x, go to L2 while the kernels this
-  // one depends on finish: an L2 prefetch is safe even if the data were
-  // still being written (L2 is the point of coherence).
+  // The first NS boxes of each warp (unless they are loaded outright below,
+  // `early`), and x, go to L2 while the kernels this one depends on finish:
+  // an L2 prefetch is safe even if the data were still being written (L2 is
+  // the point of coherence).
   if (threadIdx.x == 0) bulk_prefetch_l2(x, static_cast<uint32_t>(M) * K * 2u);
-  if (lane == 0) {
+  if (lane == 0 && !early) {
     int f_tile = tile0, f_bx = bx0;
     for (int q = 0; q < min(NS, total); ++q) {
       const int m = mat_of(f_tile);
@@ -338,35 +341,24 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
     }
   }
 
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // M = 1 and at most 16384 staged columns: one read of x, kept in
-  // registers (4 x 16 bytes per thread) from the maximum to the conversion.
-  // Its loads go out first, ahead of the weight stream.
-  const int n8 = K / 8;  // 16-byte groups per row
-  const bool x1 = M1 && kbx * 8 <= 4 * kLutThreads;
-  uint4 xv[4];
-  if (x1) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = threadIdx.x + r * kLutThreads;
-      xv[r] = i < n8 ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
-    }
-  }
+  // the first NS stage copies of the warp (lane 0)
   int p_tile = tile0, p_bx = bx0;
-  if (lane == 0) {
-    for (int q = 0; q < min(NS, total); ++q) {
-      issue_at(p_tile, p_bx, q);
-      advance(p_tile, p_bx);
+  auto issue_first = [&]() {
+    if (lane == 0) {
+      for (int q = 0; q < min(NS, total); ++q) {
+        issue_at(p_tile, p_bx, q);
+        advance(p_tile, p_bx);
+      }
     }
-  }
+  };
 
   // Chunked scale loads (EP: double quant with K / 64 a multiple of 16).  A
   // chunk is 16 blocks of the tile's 16 rows; both lanes of row r hold its
   // 16 int8 scale codes (one 16-byte load) and its scale2 (16 blocks
   // aligned to 16 never straddle a 256-block group).  A chunk is loaded one
   // ahead of the one in use, in the order the warp meets them (row-major
-  // over its run of boxes); the first two are issued here, before x is
-  // staged, so that their latency hides behind it.
+  // over its run of boxes); the first two go out with the first stage
+  // copies, before x is staged, so that their latency hides behind it.
   const int nch = KB / 16;  // chunks per row
   struct Chunk {
     uint4 q;
@@ -394,14 +386,46 @@ gemv_lut_kernel(const __grid_constant__ LutGroup G, const uint16_t* __restrict__
   Chunk E0{make_uint4(0, 0, 0, 0), 0.f}, E1 = E0;
   int e_tile = tile0, e_ci = (bx0 * BB) / 16;  // next chunk to load
   float offs[kLutMaxGroup];  // the weights' double-quant offsets
+  auto load_first = [&]() {
 #pragma unroll
-  for (int i = 0; i < kLutMaxGroup; ++i)
-    offs[i] = (EP && i < G.count) ? __ldg(G.sv[i].offset) : 0.f;
-  if (EP && total > 0) {
-    E0 = chunk_load(e_tile, e_ci);
-    chunk_next(e_tile, e_ci);
-    E1 = chunk_load(e_tile, e_ci);
-    chunk_next(e_tile, e_ci);
+    for (int i = 0; i < kLutMaxGroup; ++i)
+      offs[i] = (EP && i < G.count) ? __ldg(G.sv[i].offset) : 0.f;
+    if (EP && total > 0) {
+      E0 = chunk_load(e_tile, e_ci);
+      chunk_next(e_tile, e_ci);
+      E1 = chunk_load(e_tile, e_ci);
+      chunk_next(e_tile, e_ci);
+    }
+  };
+  // M = 1 and at most 16384 staged columns: one read of x, kept in
+  // registers (4 x 16 bytes per thread) from the maximum to the conversion.
+  const int n8 = K / 8;  // 16-byte groups per row
+  const bool x1 = M1 && kbx * 8 <= 4 * kLutThreads;
+  uint4 xv[4];
+  auto load_x = [&]() {
+    if (x1) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = threadIdx.x + r * kLutThreads;
+        xv[r] = i < n8 ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  // x is read only after the wait for the kernel this one follows.  By
+  // default its loads go out first after the wait, ahead of the weight
+  // stream.  `early`: the weights and their scales were written before that
+  // kernel began (the caller's guarantee), so their first stages and chunks
+  // load while it finishes, and x after it.  (One call site for the stage
+  // and chunk loads: two cost registers on the default path.)
+  if (!early) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    load_x();
+  }
+  issue_first();
+  load_first();
+  if (early) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    load_x();
   }
 
   // 3. x -> fp16 with a power-of-two scale per row (bf16), staged

@@ -136,7 +136,7 @@ nf4q_status gemv_attr_ready() {
 
 // Opt the block-scale-folded GEMV kernels in to their shared memory (once
 // per device).
-using LutKernelFn = void (*)(LutGroup, const uint16_t*, int, int, int, HalfCodes);
+using LutKernelFn = void (*)(LutGroup, const uint16_t*, int, int, int, HalfCodes, int);
 
 // The folded-GEMV instantiation for a compute dtype, double quant, box size,
 // whether the scales are read in 16-block chunks (double quant with K / 64
@@ -610,9 +610,10 @@ bool lut_runs_fit(int64_t T, int64_t K, int bb, int64_t grid) {
 // The block-scale-folded GEMV (gemv_lut.cuh) over a group of 1..4 weights
 // with the same cols, code, double quant and compute dtype, sharing x.
 // One CTA per SM (at most one per 16-row tile); the kernel splits each
-// CTA's tiles into equal runs of boxes over its warps.
+// CTA's tiles into equal runs of boxes over its warps.  flags: the
+// nf4q_gemv_multi_ex flags (NF4Q_GEMV_WEIGHTS_STATIC).
 nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void* x, int32_t M,
-                            void* const* y, cudaStream_t s) {
+                            void* const* y, cudaStream_t s, int32_t flags) {
   nf4q_status st = gemv_lut_attr_ready();
   if (st != NF4Q_OK) return st;
   const int K = static_cast<int>(wq[0]->cols);
@@ -644,7 +645,7 @@ nf4q_status gemv_lut_launch(const nf4q_weight* const* wq, int count, const void*
   return launch("gemv_lut_kernel", k, dim3(static_cast<unsigned>(grid)), dim3(kLutThreads),
                 kLutSmemTop, s, attr, 1, G, static_cast<const uint16_t*>(x), K,
                 static_cast<int>(M), static_cast<int>(lut_kbx(K, bb)),
-                half_codes(wq[0]->code));
+                half_codes(wq[0]->code), (flags & NF4Q_GEMV_WEIGHTS_STATIC) ? 1 : 0);
 }
 
 // The bit-faithful GEMV (gemv_mma.cuh): w_hat rebuilt exactly inside the
@@ -696,6 +697,20 @@ nf4q_status gemv_exact_launch(const nf4q_weight* wq, const void* x, int32_t M, v
                 split > 1 ? 1u : 0u, tw, sv, xp, yp, N, K, static_cast<int>(M), per, stages, C);
 }
 
+// One weight: the folded kernel where it applies (M <= NF4Q_GEMV_FOLD_MAX_M,
+// x fits its staging room, run arithmetic in 32 bits), else the exact one.
+nf4q_status gemv_one(const nf4q_weight* wq, const void* x, int32_t M, void* y, cudaStream_t s,
+                     int32_t flags) {
+  bool done = false;
+  nf4q_status st = gemv_checks(wq, x, M, y, s, &done);
+  if (st != NF4Q_OK || done) return st;
+  if (M <= NF4Q_GEMV_FOLD_MAX_M && lut_box(wq->cols, M) &&
+      lut_runs_fit((wq->rows + 15) / 16, wq->cols, lut_box(wq->cols, M),
+                   std::min<int64_t>(sm_count(), (wq->rows + 15) / 16)))
+    return gemv_lut_launch(&wq, 1, x, M, &y, s, flags);
+  return gemv_exact_launch(wq, x, M, y, s);
+}
+
 }  // namespace
 }  // namespace nf4q
 
@@ -703,19 +718,17 @@ extern "C" {
 
 nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M, void* y,
                       void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  bool done = false;
-  nf4q_status st = gemv_checks(wq, x, M, y, s, &done);
-  if (st != NF4Q_OK || done) return st;
-  if (M <= NF4Q_GEMV_FOLD_MAX_M && lut_box(wq->cols, M) &&
-      lut_runs_fit((wq->rows + 15) / 16, wq->cols, lut_box(wq->cols, M),
-                   std::min<int64_t>(sm_count(), (wq->rows + 15) / 16)))
-    return gemv_lut_launch(&wq, 1, x, M, &y, s);
-  return gemv_exact_launch(wq, x, M, y, s);
+  return nf4q::gemv_one(wq, x, M, y, static_cast<cudaStream_t>(stream), 0);
 }
 
 nf4q_status nf4q_gemv_multi(const nf4q_weight* const* wq, int32_t count, const void* x,
                             int32_t M, void* const* y, void* stream) {
+  return nf4q_gemv_multi_ex(wq, count, x, M, y, 0, stream);
+}
+
+nf4q_status nf4q_gemv_multi_ex(const nf4q_weight* const* wq, int32_t count, const void* x,
+                               int32_t M, void* const* y, int32_t flags, void* stream) {
+  if ((flags & ~NF4Q_GEMV_WEIGHTS_STATIC) != 0) return NF4Q_ERR_INVALID_ARG;
   if (!wq || !y || count < 1 || count > kLutMaxGroup) return NF4Q_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     if (!wq[i]) return NF4Q_ERR_INVALID_ARG;
@@ -738,7 +751,7 @@ nf4q_status nf4q_gemv_multi(const nf4q_weight* const* wq, int32_t count, const v
   }
   if (!one) {
     for (int i = 0; i < count; ++i) {
-      nf4q_status st = nf4q_gemv(wq[i], x, M, y[i], stream);
+      nf4q_status st = nf4q::gemv_one(wq[i], x, M, y[i], s, flags);
       if (st != NF4Q_OK) return st;
     }
     return NF4Q_OK;
@@ -746,7 +759,7 @@ nf4q_status nf4q_gemv_multi(const nf4q_weight* const* wq, int32_t count, const v
   int64_t tiles = 0;
   for (int i = 0; i < count; ++i) tiles += (wq[i]->rows + 15) / 16;
   if (tiles > 0x7FFFFFFF) return NF4Q_ERR_UNSUPPORTED;
-  return gemv_lut_launch(wq, count, x, M, y, s);
+  return gemv_lut_launch(wq, count, x, M, y, s, flags);
 }
 
 nf4q_status nf4q_gemv_exact(const nf4q_weight* wq, const void* x, int32_t M, void* y,

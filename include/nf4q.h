@@ -223,6 +223,26 @@ nf4q_status nf4q_gemv(const nf4q_weight* wq, const void* x, int32_t M,
 nf4q_status nf4q_gemv_multi(const nf4q_weight* const* wq, int32_t count, const void* x,
                             int32_t M, void* const* y, void* stream);
 
+/* nf4q_gemv_multi with flags (0 = nf4q_gemv_multi itself; any bit other than
+ * those below: NF4Q_ERR_INVALID_ARG).
+ *
+ * NF4Q_GEMV_WEIGHTS_STATIC: the caller guarantees that no kernel that may
+ * still be running when this call's kernel starts writes the weights -
+ * their packed codes and every scale array (absmax, absmax_q, scale2,
+ * offset) - i.e. they were last written before the kernel preceding this
+ * call on the stream began.  That holds for weights quantized once and
+ * reused, as in a decode loop.  The folded kernel, which starts while the
+ * preceding kernel finishes (programmatic dependent launch), then loads its
+ * first weight tiles and scales before waiting for that kernel; x is still
+ * read only after it.  The results are bit-identical to the call without the
+ * flag; the flag only moves loads earlier, so a caller that breaks the
+ * guarantee may get results computed from partly written weights.  The
+ * bit-faithful kernel (weights that go one by one through the exact path)
+ * ignores the flag. */
+#define NF4Q_GEMV_WEIGHTS_STATIC 1
+nf4q_status nf4q_gemv_multi_ex(const nf4q_weight* const* wq, int32_t count, const void* x,
+                               int32_t M, void* const* y, int32_t flags, void* stream);
+
 /* nf4q_gemv with w_hat rebuilt bit for bit inside the contraction: y =
  * x . w_hat^T with w_hat exactly as nf4q_dequantize produces it, fp32
  * accumulation (only the order of the additions differs from an exact

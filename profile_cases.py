@@ -9,11 +9,11 @@ Each case builds its seeded synthetic input, runs the library call twice
     gemv70b      nf4q_gemv M=1 on the 28672x8192 weight (NF4)
     gemv70b_exact  nf4q_gemv_exact M=1 on the same weight
     token        one Llama-3-8B decode token twice over the 224-weight stack:
-                 per layer nf4q_gemv_multi(q, k, v), nf4q_gemv(o),
-                 nf4q_gemv_multi(gate, up), nf4q_gemv(down) - 128 launches
-                 per token, as the benchmark step issues them
+                 per layer the groups (q, k, v), (o), (gate, up), (down), each
+                 one nf4q_gemv_multi_ex call with NF4Q_GEMV_WEIGHTS_STATIC -
+                 128 launches per token, as the benchmark step issues them
     layer        the same four launches for layer 0 only, twice
-    gateup       nf4q_gemv_multi(gate, up) of layer 0, twice
+    gateup       the (gate, up) launch of layer 0, twice
     gemv4096     nf4q_gemv M=1 on the 4096x4096 decode weight
     gemv4096_exact  nf4q_gemv_exact M=1 on the same weight
     gemv11008    nf4q_gemv M=1 on the 11008x4096 decode weight
@@ -63,10 +63,7 @@ def _run(case: str, torch, nq, synth) -> None:
         torch.cuda.synchronize()
         for _ in range(2):
             for qws, x, ys in launches:
-                if len(qws) == 1:
-                    nq.gemv(qws[0], x, out=ys[0])
-                else:
-                    nq.gemv_multi(qws, x, outs=ys)
+                nq.gemv_multi(qws, x, outs=ys, static_weights=True)
     elif case == "quant11008":
         w, _ = synth.llama7b_decode(1, device=dev)
         N, K = w.shape

@@ -174,6 +174,13 @@ def test_argument_checks_launch_nothing(L):
     assert L.nf4q_gemv(R(s), 16, 17, 16, None) == 3
     assert L.nf4q_gemm(R(s), 16, -1, 16, None) == 1
     assert L.nf4q_gemv(None, 16, 1, 16, None) == 1
+    # nf4q_gemv_multi_ex: unknown flag bits, then the group checks
+    W1 = (ctypes.POINTER(nq.NF4QWeight) * 1)(ctypes.pointer(s))
+    Y1 = (ctypes.c_void_p * 1)(16)
+    assert L.nf4q_gemv_multi_ex(W1, 1, 16, 1, Y1, 2, None) == 1
+    assert L.nf4q_gemv_multi_ex(W1, 1, 16, 1, Y1, -1, None) == 1
+    assert L.nf4q_gemv_multi_ex(W1, 0, 16, 1, Y1, nq.GEMV_WEIGHTS_STATIC, None) == 1
+    assert L.nf4q_gemv_multi_ex(W1, 1, 16, 0, Y1, nq.GEMV_WEIGHTS_STATIC, None) == 3
     # an unknown compute dtype is refused by every call on the weight
     dt = nq.NF4QWeight(None, None, None, None, None, 64, 64, 64, 256, 0, 1, 2)
     assert L.nf4q_quantize(16, 1, R(dt), None) == 1

@@ -196,6 +196,44 @@ def test_grouped_gemv_ranges_cross_weights():
             check_matmul(bf16_bits(y), bf16_bits(x), w_hat, f"cross M={M}")
 
 
+def test_static_weights_flag_changes_nothing_but_the_load_order():
+    """nf4q_gemv_multi_ex with NF4Q_GEMV_WEIGHTS_STATIC loads the first
+    weight tiles and scales before waiting for the preceding kernel; the
+    results are the flag-free call's, bit for bit, in every regime of the
+    kernel (3-D and 2-D weight views, chunked and per-box scales, no double
+    quant, FP4, fp16, M = 1..6, groups), also when each launch directly
+    follows another GEMV on the stream (so that it overlaps its tail), and
+    they pass the oracle check."""
+    cases = [([(4800, 5120), (2304, 5120)], "nf4", True, "bf16"),
+             ([(4096, 4096), (1024, 4096), (1024, 4096)], "nf4", True, "bf16"),
+             ([(700, 2112)], "nf4", True, "bf16"),
+             ([(1000, 1024)], "nf4", False, "bf16"),
+             ([(1500, 3072)], "fp4", True, "bf16"),
+             ([(1200, 2048)], "nf4", True, "f16")]
+    for i, (shapes, code, dq, cdt) in enumerate(cases):
+        K = shapes[0][1]
+        ws = [synth.normal_weight(n, k, 0.02, seed=120 + 7 * i + j)
+              for j, (n, k) in enumerate(shapes)]
+        qws = [nq.quantize(w.cuda(), code, dq, compute_dtype=cdt) for w in ws]
+        for M in (1, 2, 6):
+            x = synth.activations(M, K, seed=140 + M + i)
+            x = x.to(torch.float16).cuda() if cdt == "f16" else x.cuda()
+            want = nq.gemv_multi(qws, x)
+            # back to back on one stream: each launch follows a GEMV
+            outs = [nq.gemv_multi(qws, x, static_weights=True) for _ in range(3)]
+            torch.cuda.synchronize()
+            for got in outs:
+                for a, b in zip(got, want):
+                    assert torch.equal(a, b), (shapes, code, dq, cdt, M)
+    shapes = [(4800, 5120), (2304, 5120)]
+    ws = [synth.normal_weight(n, k, 0.02, seed=80 + i) for i, (n, k) in enumerate(shapes)]
+    checked = [full_check(w, "nf4", True, f"static {i}") for i, w in enumerate(ws)]
+    x = synth.activations(1, 5120, seed=84)
+    ys = nq.gemv_multi([q for q, _ in checked], x.cuda(), static_weights=True)
+    for (qw, w_hat), y in zip(checked, ys):
+        check_matmul(bf16_bits(y), bf16_bits(x), w_hat, "static M=1")
+
+
 def test_gemv_dispatch_by_m():
     """nf4q_gemv: the folded kernel for M <= 6 when x fits its staging room
     (M * K <= 30720 here), the exact one above."""
