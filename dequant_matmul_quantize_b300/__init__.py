@@ -238,8 +238,10 @@ def quantize_into(qw: QuantizedWeight, w: torch.Tensor, stream=None):
 
 
 def dq_workspace(n_b: int, device=None) -> torch.Tensor:
+    """A zero-filled double-quant workspace (every call leaves it zero, so
+    it may be reused by successive calls on one stream)."""
     nbytes = lib().nf4q_double_quant_workspace_bytes(n_b)
-    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
 
 
 def double_quant_into(qw: QuantizedWeight, workspace: Optional[torch.Tensor] = None,

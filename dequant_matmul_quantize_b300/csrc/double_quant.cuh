@@ -23,7 +23,9 @@
 namespace nf4q {
 
 
-// Layout of the double-quant workspace (cleared before pass 1).  The exact
+// Layout of the double-quant workspace.  It is zero before pass 1, and the
+// CTA that finalizes the mean reads it and clears it again, so a caller
+// zero-fills it once and reuses it without clearing.  The exact
 // total of a * 2^55 over the in-range values (below 2^128) is kept as three
 // 43-bit chunks, each summed over the CTAs on its own: a CTA's chunk is
 // below 2^43 and there are fewer than 2^20 CTAs, so no chunk sum carries
@@ -200,6 +202,22 @@ __device__ __noinline__ void dq_finalize(const float* __restrict__ absmax, int64
   __shared__ unsigned long long s_hist[256];
   __threadfence();
   const bool oor = __ldcg(&ws->out_of_range) != 0u;
+  unsigned long long c0 = 0ull, c1 = 0ull, c2 = 0ull;
+  if (threadIdx.x == 0) {
+    c0 = __ldcg(&ws->chunk[0]);
+    c1 = __ldcg(&ws->chunk[1]);
+    c2 = __ldcg(&ws->chunk[2]);
+  }
+  // every CTA has committed (this one holds the last ticket) and every
+  // thread here has read the record: leave it zero for the next call
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ws->chunk[0] = 0ull;
+    ws->chunk[1] = 0ull;
+    ws->chunk[2] = 0ull;
+    ws->out_of_range = 0u;
+    ws->ticket = 0u;
+  }
   if (oor) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) s_hist[i] = 0ull;
     __syncthreads();
@@ -219,8 +237,6 @@ __device__ __noinline__ void dq_finalize(const float* __restrict__ absmax, int64
         if (s_hist[e]) big_add_shifted(A, s_hist[e], e - 1);
     } else {
       // the total from its three chunk sums
-      const unsigned long long c0 = __ldcg(&ws->chunk[0]), c1 = __ldcg(&ws->chunk[1]),
-                               c2 = __ldcg(&ws->chunk[2]);
       const unsigned long long lo = c0 + (c1 << kDqChunkBits);
       const unsigned long long hi = (c1 >> (64 - kDqChunkBits)) + (c2 << (2 * kDqChunkBits - 64)) +
                                     (lo < c0 ? 1ull : 0ull);

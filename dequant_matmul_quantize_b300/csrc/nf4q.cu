@@ -358,8 +358,8 @@ nf4q_status nf4q_thresholds(int32_t code, float* out, int32_t* count) {
 namespace nf4q {
 namespace {
 // Quantize launch after the argument checks common to both entry points
-// (n > 0).  ws != nullptr: fused first double-quant pass into ws (cleared
-// here) and wq->offset.
+// (n > 0).  ws != nullptr: fused first double-quant pass into ws (zero on
+// entry, left zero by the kernel's last CTA) and wq->offset.
 nf4q_status quantize_launch(const void* w, int32_t in_dtype, const nf4q_weight* wq, void* ws,
                             cudaStream_t s) {
   const int64_t n = wq->rows * wq->cols;
@@ -381,9 +381,6 @@ nf4q_status quantize_launch(const void* w, int32_t in_dtype, const nf4q_weight* 
   const int64_t n_units = n / 16;  // 16 elements per lane and unit
   const int64_t grid = grid_for(n_units, kQuantThreads,
                                 static_cast<int64_t>(sm_count()) * quantize_ctas_per_sm(c));
-  if (ws && (st = cuda_check(cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s),
-                             "cudaMemsetAsync (double-quant workspace)")) != NF4Q_OK)
-    return st;
   return launch("quantize_kernel", quantize_kernel_for(c, in_dtype, ws != nullptr),
                 dim3(static_cast<unsigned>(grid)), dim3(kQuantThreads), quantize_smem_bytes(c), s,
                 nullptr, 0, w, reinterpret_cast<uint2*>(wq->packed), wq->absmax, n_units, P,
@@ -408,11 +405,10 @@ nf4q_status dq_quant_launch(const nf4q_weight* wq, int64_t nb, cudaStream_t s,
                 wq->absmax_q, wq->scale2);
 }
 
-// Both passes of the double quantization, on a cleared workspace record.
+// Both passes of the double quantization, on a zero workspace record (left
+// zero by the first pass's last CTA).
 nf4q_status dq_launch(const nf4q_weight* wq, int64_t nb, void* ws, cudaStream_t s) {
-  nf4q_status st = cuda_check(cudaMemsetAsync(ws, 0, sizeof(DqWorkspace), s),
-                              "cudaMemsetAsync (double-quant workspace)");
-  if (st != NF4Q_OK) return st;
+  nf4q_status st;
   const int64_t g1 = grid_for(nb / 4, kDqSumThreads, static_cast<int64_t>(sm_count()));
   st = launch("dq_sum_kernel", dq_sum_kernel, dim3(static_cast<unsigned>(g1)),
               dim3(kDqSumThreads), 0, s, nullptr, 0, static_cast<const float*>(wq->absmax), nb,
@@ -833,10 +829,11 @@ nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear) {
 }
 
 // ---------------------------------------------------------------- no-alloc
-// Static scratch of nf4q_double_quant_noalloc.  In host code the symbol is
-// only a handle: its device address comes from cudaGetSymbolAddress, looked
-// up once per device with that device current.
-static __device__ __align__(256) unsigned char g_dq_noalloc_scratch[256];
+// Static scratch of nf4q_double_quant_noalloc, zero when the module loads and
+// left zero by every call.  In host code the symbol is only a handle: its
+// device address comes from cudaGetSymbolAddress, looked up once per device
+// with that device current.
+static __device__ __align__(256) unsigned char g_dq_noalloc_scratch[256] = {};
 static_assert(sizeof(DqWorkspace) <= 256, "double-quant record must fit the static scratch");
 
 namespace {

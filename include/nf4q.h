@@ -160,8 +160,11 @@ size_t nf4q_double_quant_workspace_bytes(int64_t n_b);
  *   reads wq->absmax [n_b]; writes wq->absmax_q [n_b], wq->scale2 [n_d],
  *   wq->offset [1].  absmax must be 16-byte aligned.
  *   workspace: device, >= nf4q_double_quant_workspace_bytes(n_b) bytes,
- *   16-byte aligned; the call clears it itself (cudaMemsetAsync on `stream`),
- *   so its previous contents do not matter.
+ *   16-byte aligned, zero-filled before its first use (one cudaMemset).
+ *   Every call leaves it zero-filled again (the kernel that reads the sums
+ *   clears them), so successive calls on one stream reuse it without
+ *   clearing; a workspace that is not zero gives a wrong offset.  Calls whose
+ *   work overlaps on the GPU (other streams) need workspaces of their own.
  * offset = the float32 nearest to the exact mean of all absmax values (ties
  * to even; the sum is exact for any inputs); c = fp32(absmax - offset); per
  * 256-block scale2 = fp32(max|c| / 127); absmax_q = clamp(rint_even(
@@ -178,7 +181,7 @@ nf4q_status nf4q_double_quant(const nf4q_weight* wq, void* workspace,
  *   w, in_dtype  as for nf4q_quantize.
  *   wq   wq->double_quant must be 1; writes packed, absmax, absmax_q,
  *        scale2 and offset (alignments as for the two calls).
- *   workspace  as for nf4q_double_quant (cleared by the call). */
+ *   workspace  as for nf4q_double_quant (zero on entry, left zero). */
 nf4q_status nf4q_quantize_dq(const void* w, int32_t in_dtype, const nf4q_weight* wq,
                              void* workspace, size_t workspace_bytes, void* stream);
 
@@ -305,8 +308,9 @@ nf4q_status nf4q_device_error(uint32_t* flags, int32_t clear);
  *   with the id of the current context; a call in another context (after a
  *   cudaDeviceReset, for example) looks it up again.  Make the first call in
  *   a context before any stream capture.
- *   Sharing: every call on a device uses the same scratch; the call clears it
- *   (cudaMemsetAsync on `stream`) before use.  Calls whose work overlaps on
+ *   Sharing: every call on a device uses the same scratch, which is zero
+ *   when the library's device code loads and which every call leaves zero
+ *   (as a caller's workspace for nf4q_double_quant).  Calls whose work overlaps on
  *   the GPU (other streams, other threads) race on it and must be serialized
  *   by the caller.  Other arguments and errors as nf4q_double_quant. */
 nf4q_status nf4q_double_quant_noalloc(const nf4q_weight* wq, void* stream);

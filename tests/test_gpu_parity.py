@@ -191,6 +191,40 @@ def test_quantize_dq_fused_matches_two_calls(code, dtype):
             assert_bits_equal(a[k], ref[k], f"{code} case {i} {k} vs oracle")
 
 
+def test_double_quant_workspace_is_left_zero_and_reused():
+    """The double-quant workspace is zero on entry and every call leaves it
+    zero (the CTA that finalizes the mean clears it), so one workspace serves
+    successive calls: nf4q_quantize_dq and nf4q_double_quant on one
+    workspace, across tensors that take the fixed-point mean and the exact
+    re-sum path (absmax outside [2^-32, 2^8)), give the bits of calls that
+    each get a fresh workspace, which the oracle checks."""
+    rng = np.random.default_rng(11)
+    wide = (10.0 ** rng.uniform(-30, 30, 4000)).astype(np.float32)
+    wide[::7] = 0
+    cases = [np.abs(rng.standard_normal(3000) * 0.05).astype(np.float32), wide,
+             np.full(700, 0.125, np.float32), np.abs(rng.standard_normal(20000)).astype(np.float32)]
+    ws = nq.dq_workspace(1 << 20)
+    for i, am in enumerate(cases * 2):
+        w = torch.from_numpy(_weight_with_absmax(am, i)).to(torch.float32).cuda()
+        fresh = nq.quantize(w, "nf4")
+        reused = nq.quantize(w, "nf4", workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0, f"case {i}: workspace left non-zero"
+        two = nq.QuantizedWeight.empty(w.shape[0], w.shape[1], "nf4", True, w.device)
+        nq.quantize_into(two, w)
+        nq.double_quant_into(two, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0, f"case {i}: workspace left non-zero (two calls)"
+        a, b, c = gpu_state(fresh), gpu_state(reused), gpu_state(two)
+        for k in a:
+            assert_bits_equal(b[k], a[k], f"case {i} {k} reused")
+            assert_bits_equal(c[k], a[k], f"case {i} {k} two calls")
+        if i < len(cases):
+            ref = oracle_state(as_f32(w), "nf4")
+            for k in ("absmax_q", "scale2", "offset"):
+                assert_bits_equal(a[k], ref[k], f"case {i} {k} vs oracle")
+
+
 @pytest.mark.parametrize("shape", [(40, 64 * 33), (512, 1024)])
 def test_dequantize_unaligned_fp32_scales(shape):
     """Without double quantization the fp32 absmax only has to be 4-byte
