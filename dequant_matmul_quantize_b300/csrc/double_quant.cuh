@@ -276,6 +276,10 @@ dq_quant_kernel(const float* __restrict__ absmax, int64_t nb,
   // Launched as a programmatic dependent of the fused quantize kernel, this
   // waits here until that grid has completed and its writes (absmax, the
   // mean) are visible; launched normally it returns at once.
+  // The next kernel on the stream may launch at once (a quantize kernel
+  // builds its tables meanwhile); every kernel here launched as a
+  // programmatic dependent waits for this grid before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t nd = (nb + kDqBlock - 1) / kDqBlock;

@@ -381,9 +381,15 @@ nf4q_status quantize_launch(const void* w, int32_t in_dtype, const nf4q_weight* 
   const int64_t n_units = n / 16;  // 16 elements per lane and unit
   const int64_t grid = grid_for(n_units, kQuantThreads,
                                 static_cast<int64_t>(sm_count()) * quantize_ctas_per_sm(c));
+  // a programmatic dependent of the kernel before it (the kernel waits for
+  // it before any global access), so that its table build overlaps that
+  // kernel's tail
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   return launch("quantize_kernel", quantize_kernel_for(c, in_dtype, ws != nullptr),
                 dim3(static_cast<unsigned>(grid)), dim3(kQuantThreads), quantize_smem_bytes(c), s,
-                nullptr, 0, w, reinterpret_cast<uint2*>(wq->packed), wq->absmax, n_units, P,
+                attr, 1, w, reinterpret_cast<uint2*>(wq->packed), wq->absmax, n_units, P,
                 static_cast<DqWorkspace*>(ws), wq->offset);
 }
 

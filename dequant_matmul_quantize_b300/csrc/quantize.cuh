@@ -274,6 +274,10 @@ quantize_kernel(const void* __restrict__ w, uint2* __restrict__ packed,
       }
     }
   }
+  // Launched as a programmatic dependent of the kernel before it: the
+  // tables above are built while that kernel finishes; nothing in global
+  // memory is read or written before it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
 
   const uint32_t lane = threadIdx.x & 31u;
