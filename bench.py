@@ -409,8 +409,9 @@ def run_ours(args):
 
     # ---- e2e: the token as a serving loop runs it: x copied in from pinned
     # host memory and each layer's y read back into pinned host memory, the
-    # copies on their own streams so that they overlap the kernels (layer 0
-    # waits for its x, layer 1 for the rest; a layer's y is read as soon as
+    # copies on their own streams so that they overlap the kernels (x in
+    # copies of layers 0, 1, 2-3, 4-7, 8-15 and 16-31, each layer waiting for
+    # the one that holds its x; a layer's y is read as soon as
     # its launches are done), the public C-ABI calls of the token as above -
     # all of it one CUDA graph per step - and the host waiting for the last y
     host_x = x_all.cpu().pin_memory()
@@ -437,17 +438,22 @@ def run_ours(args):
         fork.record(gs)
         h2d_s.wait_event(fork)
         d2h_s.wait_event(fork)
-        # x in two copies: layer 0's, then the rest (which lands while layer 0
-        # runs), so that only two launches wait on a copy
-        x_ready = []
+        # x in copies that double in layers (0, 1, 2-3, 4-7, ...): each lands
+        # long before its first layer runs, and only the first launch of
+        # each waits for it
+        x_ready = {}
         with torch.cuda.stream(h2d_s):
-            for a, b in ((0, x_span[0][1]), (x_span[0][1], x_all.numel())):
+            lo = 0
+            while lo < synth.LLAMA3_8B_LAYERS:
+                hi = min(max(1, 2 * lo), synth.LLAMA3_8B_LAYERS)
+                a, b = x_span[lo][0], x_span[hi - 1][1]
                 x_all[a:b].copy_(host_x[a:b], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(h2d_s)
-                x_ready.append(ev)
+                x_ready[lo] = ev
+                lo = hi
         for layer in range(synth.LLAMA3_8B_LAYERS):
-            if layer < 2:
+            if layer in x_ready:
                 gs.wait_event(x_ready[layer])
             for g_ in groups[layer * per_layer:(layer + 1) * per_layer]:
                 launch_group(g_, gs.cuda_stream)
@@ -493,8 +499,9 @@ def run_ours(args):
                      "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                      "api": "the token's nf4q_gemv_multi_ex C-ABI calls (ctypes "
-                            "binding); every step x copied in from pinned host memory (layer 0's, "
-                            "then the rest while layer 0 runs) and each layer's y read back to "
+                            "binding); every step x copied in from pinned host memory (copies of "
+                            "layers 0, 1, 2-3, 4-7, 8-15, 16-31, each layer waiting for its own) "
+                            "and each layer's y read back to "
                             "pinned host memory as soon as its launches are done, on copy streams "
                             "that overlap the kernels, all of it captured once in a CUDA graph "
                             "and replayed per step; host synchronised per step, host wall clock "
