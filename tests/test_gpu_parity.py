@@ -225,6 +225,36 @@ def test_double_quant_workspace_is_left_zero_and_reused():
                 assert_bits_equal(a[k], ref[k], f"case {i} {k} vs oracle")
 
 
+def test_quantize_dq_chain_on_one_workspace():
+    """Back-to-back nf4q_quantize_dq calls on one stream with no
+    synchronisation between them share one workspace: each quantize kernel
+    starts (a programmatic dependent launch) while the previous call's
+    per-256 pass is still running, and relies on the previous call's last
+    CTA having cleared the workspace.  Twelve weights of mixed sizes and
+    absmax ranges (including the exact re-sum path), twice round: every
+    stored byte equals a call with a fresh workspace of its own."""
+    rng = np.random.default_rng(21)
+    ws_ = []
+    for i in range(12):
+        rows, cols = [(96, 1024), (1000, 2048), (17, 64 * 40), (512, 4096)][i % 4]
+        w = rng.standard_normal((rows, cols)).astype(np.float32) * (0.02 if i % 3 else 40.0)
+        if i % 5 == 0:
+            w[:, :64] *= 1e-12  # blocks with absmax below 2^-32
+        ws_.append(torch.from_numpy(w).to(torch.bfloat16).cuda())
+    fresh = [nq.quantize(w, "nf4") for w in ws_]
+    torch.cuda.synchronize()
+    want = [gpu_state(q) for q in fresh]
+    ws = nq.dq_workspace(1 << 20)
+    for _ in range(2):
+        got = [nq.quantize(w, "nf4", workspace=ws) for w in ws_]
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0
+        for i, (q, ref) in enumerate(zip(got, want)):
+            g = gpu_state(q)
+            for k in ref:
+                assert_bits_equal(g[k], ref[k], f"chain weight {i} {k}")
+
+
 @pytest.mark.parametrize("shape", [(40, 64 * 33), (512, 1024)])
 def test_dequantize_unaligned_fp32_scales(shape):
     """Without double quantization the fp32 absmax only has to be 4-byte
