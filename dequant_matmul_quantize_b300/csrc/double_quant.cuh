@@ -277,8 +277,11 @@ dq_quant_kernel(const float* __restrict__ absmax, int64_t nb,
   // waits here until that grid has completed and its writes (absmax, the
   // mean) are visible; launched normally it returns at once.
   // The next kernel on the stream may launch at once (a quantize kernel
-  // builds its tables meanwhile); every kernel here launched as a
-  // programmatic dependent waits for this grid before it touches memory.
+  // builds its tables meanwhile).  Every kernel here launched as a
+  // programmatic dependent waits for this grid before it reads or writes
+  // memory, save L2 prefetches and the first weight loads of a GEMV called
+  // with NF4Q_GEMV_WEIGHTS_STATIC, whose caller guarantees that no running
+  // kernel writes those weights.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
